@@ -1,0 +1,138 @@
+"""Seeded synthetic inputs for the nanochat-style GPT forward pass.
+
+This module is the only code shared between the fp64 oracle (``oracle/``) and
+the CUDA path (``dense_gpt_transformer_fwd_b300``).  It holds the model shapes,
+the workload table and the random-number recipes, and nothing of the model's
+arithmetic: no norm, rotation, attention, activation or softcap lives here.
+
+Sources for the shapes (pages on nanochat):
+  * d20: 1280 channels, 10 heads of dim 128, 20 layers, vocab 2**16, rows of
+    2048 tokens -- szyisi.cn article, "pre-training" section.
+  * dense transformer, RoPE, QK norm, parameter-free RMSNorm, untied
+    embedding/unembedding, ReLU^2, no biases, multi-query attention, logit
+    softcap -- yelogs.com story, architecture Q&A.
+  * d12/d24 widths follow the same depth rule: d_model = 64 * depth,
+    heads = depth/2 of dim 128, MLP = 4 * d_model.
+
+Canonical packed weight order (row-major ``[out, in]`` as a PyTorch Linear
+stores it): ``E[V, d]``; then for each layer ``Wqkv[(n_head + 2 n_kv) * hd, d]``
+(query heads, then key heads, then value heads), ``Wo[d, n_head * hd]``,
+``Wfc[F, d]``, ``Wproj[d, F]``; then ``Wu[V, d]``.
+
+Random recipe: every matrix entry is N(0, 0.02), drawn in that order from one
+``numpy.random.default_rng(seed)`` stream as float32 standard normals times
+0.02.  For bf16 workloads each value is then rounded to the nearest bf16
+(ties to even), so both sides consume exactly the same, bf16-representable
+numbers.  Token ids are uniform over ``[0, V)`` from ``default_rng(seed)``.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+import numpy as np
+
+__all__ = [
+    "ModelShape", "Workload", "SHAPES", "WORKLOADS", "param_count",
+    "layer_param_count", "gen_weights", "gen_tokens", "round_to_bf16",
+]
+
+
+@dataclass(frozen=True)
+class ModelShape:
+    name: str
+    n_layer: int
+    d_model: int
+    n_head: int
+    n_kv_head: int
+    head_dim: int
+    d_mlp: int
+    vocab: int
+    rope_base: float = 10000.0
+    softcap: float = 15.0
+    rms_eps: float = 1e-6
+    dtype: str = "bf16"          # "bf16" or "f32": the precision the model computes in
+
+    def with_(self, **kw) -> "ModelShape":
+        return replace(self, **kw)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    shape: ModelShape
+    batch: int
+    prompt_len: int
+    decode_steps: int
+    weight_seed: int
+    prompt_seed: int
+    decode_seed: int | None
+
+    @property
+    def max_seq(self) -> int:
+        return self.prompt_len + self.decode_steps
+
+
+TINY = ModelShape("tiny", 2, 128, 2, 1, 64, 512, 512, dtype="f32")
+D12 = ModelShape("d12", 12, 768, 6, 1, 128, 3072, 65536)
+D20 = ModelShape("d20", 20, 1280, 10, 1, 128, 5120, 65536)
+D24 = ModelShape("d24", 24, 1536, 12, 1, 128, 6144, 65536)
+SHAPES = {s.name: s for s in (TINY, D12, D20, D24)}
+
+# The five workloads: the tiny fp32 model (prefill + 16 decode steps), d12
+# prefill 8 x 2048, d12 decode 32 x (512 + 256), d20 prefill 16 x 2048 and
+# decode 64 x (1024 + 128), d24 prefill 8 x 2048 and decode 128 x (2048 + 128).
+WORKLOADS = {w.name: w for w in (
+    Workload("tiny", TINY, 1, 64, 16, 1000, 2000, 3000),
+    Workload("d12_prefill", D12, 8, 2048, 0, 1012, 2012, None),
+    Workload("d12_decode", D12, 32, 512, 256, 1012, 2112, 3012),
+    Workload("d20_prefill", D20, 16, 2048, 0, 1020, 2020, None),
+    Workload("d20_decode", D20, 64, 1024, 128, 1020, 2120, 3020),
+    Workload("d24_prefill", D24, 8, 2048, 0, 1024, 2024, None),
+    Workload("d24_decode", D24, 128, 2048, 128, 1024, 2124, 3024),
+)}
+
+
+def layer_param_count(s: ModelShape) -> int:
+    """Weights of one block in the canonical order (QKV, O, FC, PROJ)."""
+    hd = s.head_dim
+    qkv = (s.n_head + 2 * s.n_kv_head) * hd * s.d_model
+    o = s.d_model * s.n_head * hd
+    mlp = 2 * s.d_mlp * s.d_model
+    return qkv + o + mlp
+
+
+def param_count(s: ModelShape) -> int:
+    """Length of the packed weight vector: E, the blocks, Wu."""
+    return 2 * s.vocab * s.d_model + s.n_layer * layer_param_count(s)
+
+
+def round_to_bf16(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bfloat16 (ties to even), returned as float32.
+
+    Inputs are finite (normal draws), so no NaN/Inf handling is needed.
+    """
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32)
+    bias = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    r = ((u + bias) & np.uint32(0xFFFF0000)).astype(np.uint32)
+    return r.view(np.float32)
+
+
+def gen_weights(s: ModelShape, seed: int, std: float = 0.02) -> np.ndarray:
+    """Packed float32 weight vector in canonical order, N(0, std^2) entries."""
+    n = param_count(s)
+    rng = np.random.default_rng(seed)
+    w = rng.standard_normal(n, dtype=np.float32)
+    w *= np.float32(std)
+    if s.dtype == "bf16":
+        # chunked to bound the temporary memory on the largest models
+        step = 1 << 26
+        for i in range(0, n, step):
+            w[i:i + step] = round_to_bf16(w[i:i + step])
+    return w
+
+
+def gen_tokens(vocab: int, shape: tuple[int, ...], seed: int) -> np.ndarray:
+    """Uniform token ids over [0, vocab) as int32."""
+    rng = np.random.default_rng(seed)
+    return rng.integers(0, vocab, size=shape, dtype=np.int32)

@@ -1,0 +1,235 @@
+"""ORACLE -- test infrastructure only (imported by tests/, smoke() and bench.py's
+CPU baseline; never by the product path).
+
+Plain fp64 numpy statement of the forward pass of the nanochat-style GPT, used
+both as full-sequence prefill and as one-token decode over a KV cache.  Every
+step is written out literally, in the pages' order, with no fusion and no
+blocking; library matmuls are the only primitive used.
+
+Pages cited (titles abbreviated):
+  [yelogs]  yelogs.com story on the nanochat launch, section "technical details
+            and official Q&A" (architecture answer).
+  [geoz]    geoz.com.cn "NanoChat: Karpathy open-sources a low-cost LLM ...",
+            section "development tricks".
+  [apidog]  apidog.com/th "train your own ChatGPT for $50", section "how nanochat
+            works": 1 GPT model, 3 precision handling, 5 flash attention,
+            6 inference engine.
+  [szyisi]  szyisi.cn "$100, 8000 lines, a hand-built ChatGPT clone", sections
+            "pre-training" and inference engine paragraph.
+
+Readings taken where the pages are silent or garbled (identical in the CUDA path):
+  R1 RMSNorm eps = 1e-6, inside the square root; no learned scale [yelogs].
+  R2 Norms: after the token embedding, before attention, before the MLP and
+     before the unembedding (the last one is the Llama-like reading) [yelogs].
+  R3 RoPE: theta_j = p * base**(-2j/hd), j < hd/2, half-split pairs (j, j+hd/2),
+     y_j = x_j cos - x_{j+hd/2} sin, y_{j+hd/2} = x_j sin + x_{j+hd/2} cos;
+     positions start at 0; table precomputed [geoz], [apidog 1].
+  R4 QK-norm: parameter-free RMSNorm over hd of each query head and key head,
+     applied after RoPE (the two commute exactly) [yelogs], [apidog 1].
+  R5 attention scale 1/sqrt(hd) (the SDPA default) [apidog 5].
+  R6 ReLU^2 = relu(x)**2 (the formula itself was lost in extraction) [yelogs].
+  R7 softcap(z) = c * tanh(z / c), c = 15 [yelogs].
+  R8 no biases anywhere [yelogs]; untied E and Wu [yelogs], [apidog 1].
+  R9 weights enter as the bf16-rounded values for bf16 models, then fp64.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# --------------------------------------------------------------------------- #
+# shapes and the packed weight layout (PyTorch Linear [out, in], apidog 3)
+# --------------------------------------------------------------------------- #
+
+
+def block_param_count(d_model, n_head, n_kv_head, head_dim, d_mlp):
+    """Weights in one block: Wqkv, Wo, Wfc, Wproj (no biases, no norm gains)."""
+    q = n_head * head_dim
+    kv = n_kv_head * head_dim
+    return (q + 2 * kv) * d_model + d_model * q + d_mlp * d_model + d_model * d_mlp
+
+
+def total_param_count(n_layer, d_model, n_head, n_kv_head, head_dim, d_mlp, vocab):
+    """Untied embedding and unembedding plus the blocks [yelogs]."""
+    return vocab * d_model + n_layer * block_param_count(
+        d_model, n_head, n_kv_head, head_dim, d_mlp) + vocab * d_model
+
+
+def unpack_weights(flat, shape):
+    """Split the canonical packed vector into fp64 matrices.
+
+    Order: E[V,d]; per layer Wqkv[(n_h+2 n_kv) hd, d], Wo[d, n_h hd],
+    Wfc[F, d], Wproj[d, F]; then Wu[V, d].
+    """
+    s = shape
+    d, hd, V, F = s.d_model, s.head_dim, s.vocab, s.d_mlp
+    q, kv = s.n_head * hd, s.n_kv_head * hd
+    flat = np.asarray(flat)
+    off = 0
+
+    def take(rows, cols):
+        nonlocal off
+        m = flat[off:off + rows * cols].astype(np.float64).reshape(rows, cols)
+        off += rows * cols
+        return m
+
+    E = take(V, d)
+    layers = []
+    for _ in range(s.n_layer):
+        layers.append(dict(Wqkv=take(q + 2 * kv, d), Wo=take(d, q),
+                           Wfc=take(F, d), Wproj=take(d, F)))
+    Wu = take(V, d)
+    if off != flat.size:
+        raise ValueError(f"packed weights: consumed {off} of {flat.size} values")
+    return E, layers, Wu
+
+
+# --------------------------------------------------------------------------- #
+# the operations, one by one
+# --------------------------------------------------------------------------- #
+
+
+def rms_norm(x, eps):
+    """Parameter-free RMSNorm over the last axis (R1) [yelogs]."""
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps)
+
+
+def rope_tables(positions, head_dim, base):
+    """Precomputed rotary tables cos, sin of shape [len(positions), hd/2] (R3) [geoz]."""
+    j = np.arange(head_dim // 2, dtype=np.float64)
+    inv_freq = base ** (-2.0 * j / head_dim)
+    theta = np.asarray(positions, dtype=np.float64)[:, None] * inv_freq[None, :]
+    return np.cos(theta), np.sin(theta)
+
+
+def apply_rope(x, cos, sin):
+    """Rotate pairs (j, j + hd/2) of the last axis by the per-position angles (R3).
+
+    x: [T, heads, hd]; cos, sin: [T, hd/2].
+    """
+    half = x.shape[-1] // 2
+    a, b = x[..., :half], x[..., half:]
+    c, s = cos[:, None, :], sin[:, None, :]
+    return np.concatenate([a * c - b * s, a * s + b * c], axis=-1)
+
+
+def causal_attention(q, k, v, q_pos, k_pos):
+    """Causal multi-query attention (R5) [yelogs], [apidog 5].
+
+    q: [Tq, n_head, hd]; k, v: [Tk, n_kv, hd]; query head h reads key/value
+    head h // (n_head / n_kv) -- with one KV head every query head shares it.
+    A query at position p sees the keys at positions <= p.
+    Returns [Tq, n_head, hd].
+    """
+    n_head, hd = q.shape[1], q.shape[2]
+    n_kv = k.shape[1]
+    group = n_head // n_kv
+    allowed = np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None]   # [Tq, Tk]
+    out = np.empty_like(q)
+    for h in range(n_head):
+        kh, vh = k[:, h // group, :], v[:, h // group, :]
+        scores = (q[:, h, :] @ kh.T) / np.sqrt(hd)
+        scores = np.where(allowed, scores, -np.inf)
+        scores = scores - scores.max(axis=1, keepdims=True)
+        p = np.exp(scores)
+        p = p / p.sum(axis=1, keepdims=True)
+        out[:, h, :] = p @ vh
+    return out
+
+
+def relu_squared(x):
+    """ReLU^2 activation (R6) [yelogs], [geoz]."""
+    return np.maximum(x, 0.0) ** 2
+
+
+def softcap(z, cap):
+    """Logit softcap cap * tanh(z / cap) (R7) [yelogs]."""
+    return cap * np.tanh(z / cap)
+
+
+# --------------------------------------------------------------------------- #
+# the model
+# --------------------------------------------------------------------------- #
+
+
+class OracleModel:
+    """fp64 forward pass with a per-layer KV cache (post-RoPE, post-QK-norm k; v).
+
+    ``prefill(tokens[B, T])`` runs the full sequence from an empty cache and
+    returns logits [B, T, V]; ``decode(tokens[B])`` appends one position per row
+    and returns logits [B, V] [szyisi inference engine], [apidog 6].
+    """
+
+    def __init__(self, flat_weights, shape):
+        self.s = shape
+        self.E, self.layers, self.Wu = unpack_weights(flat_weights, shape)
+        self.reset()
+
+    def reset(self):
+        self.k_cache = [None] * self.s.n_layer     # each [B, len, n_kv, hd]
+        self.v_cache = [None] * self.s.n_layer
+        self.length = 0
+
+    # one block over the new positions of every row
+    def _block(self, li, x, positions):
+        s, W = self.s, self.layers[li]
+        B, T, _ = x.shape
+        hd, nh, nkv = s.head_dim, s.n_head, s.n_kv_head
+        cos, sin = rope_tables(positions, hd, s.rope_base)
+
+        h = rms_norm(x, s.rms_eps)                                  # pre-attention norm
+        qkv = h @ W["Wqkv"].T                                       # bias-free projection
+        q = qkv[..., :nh * hd].reshape(B, T, nh, hd)
+        k = qkv[..., nh * hd:(nh + nkv) * hd].reshape(B, T, nkv, hd)
+        v = qkv[..., (nh + nkv) * hd:].reshape(B, T, nkv, hd)
+
+        y = np.empty((B, T, nh, hd))
+        new_k, new_v = [], []
+        for b in range(B):
+            qb = rms_norm(apply_rope(q[b], cos, sin), s.rms_eps)   # RoPE, then QK-norm
+            kb = rms_norm(apply_rope(k[b], cos, sin), s.rms_eps)
+            vb = v[b]
+            if self.k_cache[li] is None:
+                kc, vc = kb, vb
+            else:
+                kc = np.concatenate([self.k_cache[li][b], kb], axis=0)
+                vc = np.concatenate([self.v_cache[li][b], vb], axis=0)
+            new_k.append(kc)
+            new_v.append(vc)
+            k_pos = np.arange(kc.shape[0])
+            y[b] = causal_attention(qb, kc, vc, positions, k_pos)
+        self.k_cache[li] = np.stack(new_k)
+        self.v_cache[li] = np.stack(new_v)
+
+        x = x + y.reshape(B, T, nh * hd) @ W["Wo"].T                # out-proj + residual
+        h = rms_norm(x, s.rms_eps)                                  # pre-MLP norm
+        x = x + relu_squared(h @ W["Wfc"].T) @ W["Wproj"].T          # ReLU^2 MLP + residual
+        return x
+
+    def _forward(self, tokens, logit_positions=None):
+        s = self.s
+        tokens = np.asarray(tokens)
+        B, T = tokens.shape
+        if np.any(tokens < 0) or np.any(tokens >= s.vocab):
+            raise ValueError("token id out of range")
+        positions = np.arange(self.length, self.length + T)
+        x = rms_norm(self.E[tokens], s.rms_eps)                     # embedding, then norm
+        for li in range(s.n_layer):
+            x = self._block(li, x, positions)
+        self.length += T
+        if logit_positions is not None:
+            x = x[:, logit_positions, :]
+        h = rms_norm(x, s.rms_eps)                                  # final norm (R2)
+        return softcap(h @ self.Wu.T, s.softcap)                    # unembed + softcap
+
+    def prefill(self, tokens, logit_positions=None):
+        """Logits [B, T, V] (or [B, len(logit_positions), V]) from an empty cache."""
+        self.reset()
+        return self._forward(tokens, logit_positions)
+
+    def decode(self, tokens):
+        """One new token per row at position ``self.length``; logits [B, V]."""
+        if self.length == 0:
+            raise RuntimeError("decode before prefill")
+        tokens = np.asarray(tokens).reshape(-1, 1)
+        return self._forward(tokens)[:, 0, :]
