@@ -1,0 +1,407 @@
+"""Throughput of the nanochat-style GPT forward pass on one B300 (per rank).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Default workload: d12 (12 layers, d_model 768, 6 query heads x 128, one KV
+head, MLP 3072, vocab 65536) prefill of 8 rows x 2048 uniform-random tokens,
+all-position fp32 logits.  One step = one nc_prefill over the whole batch.
+A second measurement (key "decode") times d12 decode: 32 rows, 512-token
+prompt, 256 decode steps, tokens/s over the decode steps.
+
+Prints ONE JSON line on rank 0.  Under torchrun every rank runs its own
+replica of the workload on its own GPU (rows are independent, no collective);
+value = tokens of all ranks / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import nc_inputs  # noqa: E402
+
+METRIC = "prefill tokens/s and decode tokens/s at 1 B300; % of bf16 TC peak / HBM BW"
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def prefill_flops(s, B, T, last_only=False):
+    """Algorithmic FLOPs of one prefill, per kernel class (2 per MAC; causal
+    attention counts the T(T+1)/2 unmasked pairs, QK^T and PV)."""
+    M = B * T
+    d, hd, nh, F, V, L = s.d_model, s.head_dim, s.n_head, s.d_mlp, s.vocab, s.n_layer
+    return {
+        "qkv": 2.0 * M * d * (nh + 2) * hd * L,
+        "attn": 4.0 * nh * hd * (T * (T + 1) / 2) * B * L,
+        "oproj": 2.0 * M * nh * hd * d * L,
+        "fc": 2.0 * M * d * F * L,
+        "proj": 2.0 * M * F * d * L,
+        "lm_head": 2.0 * (B if last_only else M) * d * V,
+    }
+
+
+def decode_bytes(s, B, ctx):
+    """Algorithmic HBM bytes of one decode step at context length ctx (keys
+    0..ctx-1 read, one new K/V row written): bf16 weights once, KV read+write,
+    embedding rows, fp32 logits."""
+    d, hd, nh, F, V, L = s.d_model, s.head_dim, s.n_head, s.d_mlp, s.vocab, s.n_layer
+    layer = (nh + 2) * hd * d + d * nh * hd + 2 * F * d
+    return (2.0 * (L * layer + V * d) + L * B * 2 * ctx * hd * 2 + L * B * 2 * hd * 2
+            + B * d * 2 + B * V * 4)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"nc_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [t.strip() for t in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_tokens_per_s(w, flat, prompt, rows, T):
+    """fp64 oracle prefill of `rows` x T tokens; returns (tokens/s, seconds, threads)."""
+    from threadpoolctl import threadpool_info
+    from oracle.gpt_oracle import OracleModel
+    o = OracleModel(flat, w.shape)
+    t0 = time.perf_counter()
+    o.prefill(prompt[rows, :T])
+    dt = time.perf_counter() - t0
+    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    return len(rows) * T / dt, dt, threads
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    """The oracle, as it stands, on the host cores: each step is the prefill of
+    row 0's first 512 tokens of the benchmark workload."""
+    if rank != 0:
+        return
+    w = nc_inputs.WORKLOADS[args.config]
+    flat = nc_inputs.gen_weights(w.shape, w.weight_seed)
+    prompt, _ = _tokens(w)
+    T = min(512, w.prompt_len)
+    from threadpoolctl import threadpool_info
+    from oracle.gpt_oracle import OracleModel
+    o = OracleModel(flat, w.shape)
+    for _ in range(args.warmup):
+        o.prefill(prompt[:1, :T])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.prefill(prompt[:1, :T])
+    dt = time.perf_counter() - t0
+    value = args.steps * T / dt
+    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    sample = f"row 0, tokens 0..{T - 1} of {w.name} ({w.batch}x{w.prompt_len}), all-position logits"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "global_batch": w.batch, "seq_len": w.prompt_len},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _tokens(w):
+    prompt = nc_inputs.gen_tokens(w.shape.vocab, (w.batch, w.prompt_len), w.prompt_seed)
+    nxt = (nc_inputs.gen_tokens(w.shape.vocab, (w.decode_steps, w.batch), w.decode_seed)
+           if w.decode_steps else None)
+    return prompt, nxt
+
+
+def bench_prefill(args, world, local, w, flat, prompt):
+    import torch
+    import dense_gpt_transformer_fwd_b300 as ncp
+    B, T, V = w.batch, w.prompt_len, w.shape.vocab
+    m = ncp.Model(w.shape, flat, max_batch=B, max_seq=T)
+    tok = torch.from_numpy(prompt).to("cuda")
+    logits = torch.empty((B * T, V), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        m.kv_reset()
+        m.prefill(tok, out=logits)
+
+    for _ in range(args.warmup):
+        step()
+    m.sync()
+    barrier(world)
+    torch.cuda.synchronize()
+    l0 = m.launch_count
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    m.sync()
+    launches = (m.launch_count - l0) // args.steps
+    ms = ev0.elapsed_time(ev1) / args.steps
+    barrier(world)
+    ms_max = max_over_ranks(world, ms)
+
+    # per-kernel-class device time (events around each launch), separate pass
+    m.profile_begin()
+    for _ in range(args.steps):
+        step()
+    prof = m.profile_end()
+    prof = {k: (t / args.steps, n // args.steps) for k, (t, n) in prof.items()}
+
+    # end to end through the public API with host buffers (pinned)
+    tok_h = torch.from_numpy(prompt).pin_memory()
+    out_h = torch.empty((B * T, V), dtype=torch.float32, pin_memory=True)
+    for _ in range(2):
+        m.kv_reset()
+        m.prefill(tok_h, out=out_h)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    e2e_steps = max(1, min(args.steps, 5))
+    for _ in range(e2e_steps):
+        m.kv_reset()
+        m.prefill(tok_h, out=out_h)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(world, (time.perf_counter() - t0) / e2e_steps)
+    m.sync()
+    m.close()
+    del logits, out_h
+    torch.cuda.empty_cache()
+    return {"ms": ms_max, "launches": launches, "prof": prof, "clocks": clk.summary(),
+            "e2e_s": e2e_s, "h2d": B * T * 4, "d2h": B * T * V * 4}
+
+
+def bench_decode(args, w, flat, prompt, nxt, steps=None):
+    import torch
+    import dense_gpt_transformer_fwd_b300 as ncp
+    B = w.batch
+    steps = steps or w.decode_steps
+    m = ncp.Model(w.shape, flat, max_batch=B, max_seq=w.max_seq)
+    tok = torch.from_numpy(prompt).to("cuda")
+    nxt_d = torch.from_numpy(nxt).to("cuda")
+    out = torch.empty((B, w.shape.vocab), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    # warm-up pass (prefill + a few steps), then the timed pass
+    m.prefill(tok, last_only=True)
+    for t in range(min(3, steps)):
+        m.decode_step(nxt_d[t], out=out)
+    m.kv_reset()
+    m.prefill(tok, last_only=True)
+    torch.cuda.synchronize()
+    l0 = m.launch_count
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for t in range(steps):
+        m.decode_step(nxt_d[t], out=out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    m.sync()
+    ms = ev0.elapsed_time(ev1) / steps
+    launches = (m.launch_count - l0) // steps
+    ctx_mean = w.prompt_len + (steps + 1) / 2.0
+    byts = np.mean([decode_bytes(w.shape, B, w.prompt_len + t + 1) for t in range(steps)])
+    m.close()
+    return {"ms": ms, "launches": launches, "bytes": float(byts), "ctx_mean": ctx_mean}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="d12_prefill", choices=sorted(nc_inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-decode", action="store_true", help="skip the d12 decode measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    from dense_gpt_transformer_fwd_b300 import build
+    build.build()
+
+    peaks, peak_src = load_peaks()
+    w = nc_inputs.WORKLOADS[args.config]
+    flat = nc_inputs.gen_weights(w.shape, w.weight_seed)
+    prompt, nxt = _tokens(w)
+    line = {"metric": METRIC, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.shape.dtype, "data": "synthetic"}
+
+    if w.decode_steps == 0:
+        r = bench_prefill(args, world, local, w, flat, prompt)
+        B, T = w.batch, w.prompt_len
+        value = world * B * T / (r["ms"] / 1e3)
+        flops = prefill_flops(w.shape, B, T)
+        prof = r["prof"]
+        # dominant kernel class by device time
+        dom = max(prof, key=lambda k: prof[k][0])
+        kern = {}
+        for k, (t, n) in prof.items():
+            if t > 0:
+                e = {"ms": round(t, 4), "launches": n, "share": round(t / sum(v[0] for v in prof.values()), 4)}
+                if k in flops:
+                    e["tflops"] = round(flops[k] / (t / 1e3) / 1e12, 1)
+                kern[k] = e
+        peak = peaks["bf16_tflops"]
+        if dom in flops:
+            ach = flops[dom] / (prof[dom][0] / 1e3) / 1e12
+            roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+                    "peak_source": f"{peak_src} bf16 dense (burst)"}
+        else:
+            roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": None, "traffic": None}
+        total_flops = sum(flops.values())
+        line.update({
+            "value": round(value, 1), "ms_per_step": round(r["ms"], 4),
+            "config": {"workload": w.name, "global_batch": B * world, "seq_len": T,
+                       "parallelism": f"replicas{world}", "logits": "fp32, all positions",
+                       "l2": "working set > L2 (weights 347 MB, logits 4.3 GB per step)"},
+            "gpu_launches": r["launches"],
+            "e2e": {"value": round(world * B * T / r["e2e_s"], 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "roofline": roof,
+            "step_tflops": round(total_flops / (r["ms"] / 1e3) / 1e12, 1),
+            "step_frac_of_peak": round(total_flops / (r["ms"] / 1e3) / 1e12 / peak, 4),
+            "kernels": kern,
+            "clocks": r["clocks"],
+        })
+        if not args.no_decode and rank == 0:
+            wd = nc_inputs.WORKLOADS["d12_decode"] if w.shape.name == "d12" else None
+            if wd is not None:
+                pd, nd = _tokens(wd)
+                rd = bench_decode(args, wd, flat, pd, nd)
+                gbs = rd["bytes"] / (rd["ms"] / 1e3) / 1e9
+                line["decode"] = {"workload": wd.name, "value": round(wd.batch / (rd["ms"] / 1e3), 1),
+                                  "unit": "tokens/s", "ms_per_step": round(rd["ms"], 4),
+                                  "gpu_launches_per_step": rd["launches"],
+                                  "hbm_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    else:
+        rd = bench_decode(args, w, flat, prompt, nxt)
+        value = world * w.batch / (rd["ms"] / 1e3)
+        gbs = rd["bytes"] / (rd["ms"] / 1e3) / 1e9
+        line.update({
+            "value": round(value, 1), "ms_per_step": round(rd["ms"], 4),
+            "config": {"workload": w.name, "global_batch": w.batch * world,
+                       "seq_len": w.prompt_len, "decode_steps": w.decode_steps,
+                       "parallelism": f"replicas{world}"},
+            "gpu_launches": rd["launches"],
+            "roofline": {"bound": "hbm", "kernel": "decode step", "achieved": round(gbs, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None},
+        })
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, dt, threads = oracle_tokens_per_s(w, flat, prompt, [0], w.prompt_len)
+        line["cpu_baseline"] = {"value": round(tps, 2), "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"fp64 prefill of row 0 ({w.prompt_len} tokens) of {w.name}; {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,369 @@
+// Persistent bf16 GEMM on the 5th-generation tensor cores (sm_103a):
+//   acc[m, n] = sum_k A[m, k] * W[n, k]          (A [M, K], W [N, K], both K-major)
+// with the consumer of each projection fused into the epilogue.
+//
+// The projections are the bias-free Linear layers of the nanochat-style GPT
+// (yelogs.com nanochat story, "technical details and official Q&A": no bias,
+// QK norm, ReLU^2, logit softcap; apidog.com/th "train your own ChatGPT",
+// "how nanochat works" item 3: F.linear with the weight in the compute dtype).
+//
+// Roles inside one CTA (192 threads, one CTA per SM):
+//   warp 0        TMA producer: A and W tiles (128 B swizzle) into a ring of
+//                 STAGES shared-memory slots, completion on mbarriers
+//   warp 1        TMEM owner + MMA issuer: tcgen05.mma kind::f16, M = 128,
+//                 N = BN, K = 16 per instruction; two TMEM accumulators so the
+//                 epilogue of tile i overlaps the main loop of tile i + 1
+//   warps 2..5    epilogue: tcgen05.ld (each warp owns 32 TMEM lanes = 32
+//                 rows), fused math, transpose through shared memory, coalesced
+//                 128-byte row stores
+// Tiles are visited m-fastest so that CTAs resident at the same time share
+// the W tile (and the whole A panel stays in L2).
+#pragma once
+
+#include <cuda.h>
+#include "nc_common.cuh"
+
+namespace nc {
+
+enum GemmEpi : int {
+  EPI_QKV = 0,     // RoPE + QK-norm on q and k heads; q -> Q, k/v -> KV cache
+  EPI_RESID = 1,   // x[m, n] += acc                     (fp32 residual stream)
+  EPI_RELU2 = 2,   // out = bf16(relu(acc)^2)            (MLP hidden)
+  EPI_LOGITS = 3,  // out = cap * tanh(acc / cap)        (fp32 logits)
+  EPI_STORE = 4,   // out = acc                          (fp32, tests)
+};
+
+struct GemmArgs {
+  int M, N, K;
+  int ldo;                        // leading dimension of the output (elements)
+  // EPI_QKV
+  __nv_bfloat16* q_out;           // [M, n_head * 128]
+  __nv_bfloat16* k_cache;         // this layer's K: [B_max][S][128]
+  __nv_bfloat16* v_cache;         // this layer's V: [B_max][S][128]
+  const float* rope_cos;          // [S][64]
+  const float* rope_sin;          // [S][64]
+  int n_head, T, pos0, cache_S;
+  float eps;
+  // EPI_RESID
+  float* x;
+  // EPI_RELU2
+  __nv_bfloat16* out_bf16;
+  // EPI_LOGITS / EPI_STORE
+  float* out_f32;
+  float softcap;
+  // error reporting
+  int* err;
+  unsigned long long wait_limit_ns;
+};
+
+template <int BN>
+struct TcCfg {
+  static constexpr int BM = 128, BK = 64;
+  static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr int EP_WORDS = 32 * 65;            // per epilogue warp: 32 rows x 65 words
+  static constexpr size_t SMEM = 1024 + STAGES * (size_t)STAGE_BYTES + 4 * EP_WORDS * 4 + 256;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+
+// softcap without a libm call: cap * tanh(y), tanh(y) = 1 - 2 / (exp(2y) + 1);
+// saturates correctly to +-cap when exp overflows to inf or underflows to 0.
+__device__ __forceinline__ float softcap_f(float z, float cap) {
+  const float e = __expf(2.0f * z / cap);
+  return cap * (1.0f - __fdividef(2.0f, e + 1.0f));
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs args) {
+  using C = TcCfg<BN>;
+  constexpr int BM = C::BM, BK = C::BK, STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * C::A_BYTES;
+  uint32_t* ep_stage = reinterpret_cast<uint32_t*>(sB + STAGES * C::B_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ep_stage + 4 * C::EP_WORDS);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = (args.M + BM - 1) / BM;
+  const int num_n = args.N / BN;
+  const int num_tiles = num_m * num_n;
+  const int KB = (args.K + BK - 1) / BK;
+  const uint64_t limit = args.wait_limit_ns;
+
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, TEMPTY = 2 * STAGES + 2,
+            DRAIN = 2 * STAGES + 4;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(FULL + s), 1);
+      mbar_init(bar(EMPTY + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar(TFULL + a), 1);
+      mbar_init(bar(TEMPTY + a), 128);
+    }
+    mbar_init(bar(DRAIN), 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto fail = [&]() {
+    atomicOr(args.err, NC_DEVFLAG_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = -1;   // parity of an outstanding load
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int m0 = (tile % num_m) * BM, n0 = (tile / num_m) * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (*abort_flag || !mbar_wait(bar(EMPTY + stage), phase ^ 1, limit)) {
+            if (!*abort_flag) fail();
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(FULL + stage), C::STAGE_BYTES);
+          tma_load_2d(smem_u32(sA + stage * C::A_BYTES), &tmA, bar(FULL + stage), kb * BK, m0);
+          tma_load_2d(smem_u32(sB + stage * C::B_BYTES), &tmB, bar(FULL + stage), kb * BK, n0);
+          issued[stage] = (int)phase;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        // let every copy still in flight land before the CTA exits
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s] >= 0) mbar_wait(bar(FULL + s), (uint32_t)issued[s], limit);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      uint32_t stage = 0, phase = 0;
+      int local = 0;
+      bool ok = true, any = false;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (*abort_flag || !mbar_wait(bar(TEMPTY + acc), acc_phase ^ 1, limit)) {
+          if (!*abort_flag) fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (*abort_flag || !mbar_wait(bar(FULL + stage), phase, limit)) {
+            if (!*abort_flag) fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma_f16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
+                       (kb | k) != 0);
+          any = true;
+          tc_commit(bar(EMPTY + stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (ok) tc_commit(bar(TFULL + acc));
+      }
+      if (!ok && any) {
+        // every issued MMA must finish before TMEM is released
+        tc_commit(bar(DRAIN));
+        mbar_wait(bar(DRAIN), 0, limit);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                         // TMEM lane quarter of this warp
+    uint32_t* st = ep_stage + (warp - 2) * C::EP_WORDS;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      const int acc = local & 1;
+      if (*abort_flag || !mbar_wait(bar(TFULL + acc), (local >> 1) & 1, limit)) {
+        if (!*abort_flag) fail();
+        break;
+      }
+      tc_fence_after();
+      const int m0 = (tile % num_m) * BM, n0 = (tile / num_m) * BN;
+      const int row0 = m0 + 32 * q;                 // first row of this warp
+      const int my_row = row0 + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc * BN;
+
+      if constexpr (EPI == EPI_RELU2) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 64) {
+          float v0[32], v1[32];
+          tmem_ld32(taddr + c, v0);
+          tmem_ld32(taddr + c + 32, v1);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float a0 = fmaxf(v0[2 * j], 0.f), a1 = fmaxf(v0[2 * j + 1], 0.f);
+            const float b0 = fmaxf(v1[2 * j], 0.f), b1 = fmaxf(v1[2 * j + 1], 0.f);
+            st[lane * 33 + j] = pack_bf16x2(a0 * a0, a1 * a1);
+            st[lane * 33 + 16 + j] = pack_bf16x2(b0 * b0, b1 * b1);
+          }
+          __syncwarp();
+#pragma unroll 4
+          for (int r = 0; r < 32; ++r) {
+            const int m = row0 + r;
+            if (m < args.M)
+              reinterpret_cast<uint32_t*>(args.out_bf16 + (size_t)m * args.ldo + n0 + c)[lane] =
+                  st[r * 33 + lane];
+          }
+          __syncwarp();
+        }
+      } else if constexpr (EPI == EPI_LOGITS || EPI == EPI_STORE) {
+        float* stf = reinterpret_cast<float*>(st);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(taddr + c, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            stf[lane * 33 + j] = (EPI == EPI_LOGITS) ? softcap_f(v[j], args.softcap) : v[j];
+          __syncwarp();
+#pragma unroll 4
+          for (int r = 0; r < 32; ++r) {
+            const int m = row0 + r;
+            if (m < args.M) args.out_f32[(size_t)m * args.ldo + n0 + c + lane] = stf[r * 33 + lane];
+          }
+          __syncwarp();
+        }
+      } else if constexpr (EPI == EPI_RESID) {
+        float* stf = reinterpret_cast<float*>(st);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+#pragma unroll 8
+          for (int r = 0; r < 32; ++r) {
+            const int m = row0 + r;
+            stf[r * 33 + lane] = (m < args.M) ? args.x[(size_t)m * args.ldo + n0 + c + lane] : 0.f;
+          }
+          tmem_ld32(taddr + c, v);
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) stf[lane * 33 + j] += v[j];
+          __syncwarp();
+#pragma unroll 8
+          for (int r = 0; r < 32; ++r) {
+            const int m = row0 + r;
+            if (m < args.M) args.x[(size_t)m * args.ldo + n0 + c + lane] = stf[r * 33 + lane];
+          }
+          __syncwarp();
+        }
+      } else if constexpr (EPI == EPI_QKV) {
+        // BN covers BN/128 whole heads (head_dim 128).  Columns [0, n_head*128)
+        // are query heads, then the key head, then the value head.
+        const int b = my_row / args.T;
+        const int pos = args.pos0 + (my_row - b * args.T);
+        const int pos_c = pos < args.cache_S ? pos : args.cache_S - 1;   // rows >= M only
+#pragma unroll 1
+        for (int hh = 0; hh < BN / 128; ++hh) {
+          const int head = (n0 >> 7) + hh;
+          const bool is_v = head == args.n_head + 1;
+          const uint32_t hbase = taddr + hh * 128;
+          float scale = 1.f;
+          if (!is_v) {
+            float ss = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 32) {
+              float v[32];
+              tmem_ld32(hbase + c, v);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+            }
+            scale = rsqrtf(ss * (1.f / 128.f) + args.eps);
+          }
+#pragma unroll 1
+          for (int c = 0; c < 64; c += 32) {
+            float a[32], bb[32];
+            tmem_ld32(hbase + c, a);
+            tmem_ld32(hbase + 64 + c, bb);
+            if (!is_v) {
+              const float4* cp = reinterpret_cast<const float4*>(args.rope_cos + (size_t)pos_c * 64 + c);
+              const float4* sp = reinterpret_cast<const float4*>(args.rope_sin + (size_t)pos_c * 64 + c);
+#pragma unroll
+              for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 cs = __ldg(cp + j4), sn = __ldg(sp + j4);
+                const float cc[4] = {cs.x, cs.y, cs.z, cs.w}, ssn[4] = {sn.x, sn.y, sn.z, sn.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int j = 4 * j4 + e;
+                  const float x0 = a[j] * scale, x1 = bb[j] * scale;
+                  a[j] = x0 * cc[e] - x1 * ssn[e];
+                  bb[j] = x0 * ssn[e] + x1 * cc[e];
+                }
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              st[lane * 65 + (c >> 1) + j] = pack_bf16x2(a[2 * j], a[2 * j + 1]);
+              st[lane * 65 + 32 + (c >> 1) + j] = pack_bf16x2(bb[2 * j], bb[2 * j + 1]);
+            }
+          }
+          __syncwarp();
+#pragma unroll 2
+          for (int r = 0; r < 32; ++r) {
+            const int m = row0 + r;
+            if (m < args.M) {
+              __nv_bfloat16* dst;
+              if (head < args.n_head) {
+                dst = args.q_out + (size_t)m * (args.n_head * 128) + head * 128;
+              } else {
+                const int rb = m / args.T;
+                const int rp = args.pos0 + (m - rb * args.T);
+                dst = (is_v ? args.v_cache : args.k_cache) + ((size_t)rb * args.cache_S + rp) * 128;
+              }
+              uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
+              d32[lane] = st[r * 65 + lane];
+              d32[lane + 32] = st[r * 65 + 32 + lane];
+            }
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(TEMPTY + acc));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+}  // namespace nc

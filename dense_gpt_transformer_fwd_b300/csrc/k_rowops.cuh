@@ -1,0 +1,177 @@
+// Row-wise kernels of the forward pass: token embedding + RMSNorm, the
+// parameter-free RMSNorm before each projection, the RoPE/QK-norm/KV-cache
+// write that follows an unfused QKV projection, and an fp32 SIMT GEMM used by
+// the fp32 model.
+//
+// Sources: yelogs.com nanochat story, "technical details and official Q&A"
+// (RMSNorm without learnable parameters after the token embedding and before
+// the MLP, QK norm, RoPE without absolute positions, untied embedding);
+// geoz.com.cn NanoChat article, "development tricks" (precomputed rotary
+// embeddings, KV cache).
+#pragma once
+
+#include "nc_common.cuh"
+
+namespace nc {
+
+// One warp per row: x[m] = rms(E[tok[m]]) in fp32, h[m] = TA(rms(x[m])).
+// An out-of-range token raises NC_DEVFLAG_TOKEN and reads row 0 instead.
+template <typename TW, typename TA>
+__global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tok, const TW* __restrict__ E,
+                                     float* __restrict__ x, TA* __restrict__ h, int M, int d,
+                                     int vocab, float eps, int* err) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= M) return;
+  int t = tok[warp];
+  if (t < 0 || t >= vocab) {
+    if (lane == 0) atomicOr(err, NC_DEVFLAG_TOKEN);
+    t = 0;
+  }
+  const TW* e = E + (size_t)t * d;
+  float ss = 0.f;
+  for (int j = lane; j < d; j += 32) {
+    const float v = to_f(e[j]);
+    ss = fmaf(v, v, ss);
+  }
+  ss = warp_sum(ss);
+  const float r0 = rsqrtf(ss / d + eps);
+  // second norm of the (already normalised) row: its mean square is ss*r0^2/d
+  float ss1 = 0.f;
+  for (int j = lane; j < d; j += 32) {
+    const float v = to_f(e[j]) * r0;
+    x[(size_t)warp * d + j] = v;
+    ss1 = fmaf(v, v, ss1);
+  }
+  ss1 = warp_sum(ss1);
+  const float r1 = rsqrtf(ss1 / d + eps);
+  for (int j = lane; j < d; j += 32) h[(size_t)warp * d + j] = from_f<TA>(x[(size_t)warp * d + j] * r1);
+}
+
+// One warp per output row: h[i] = TA(rms(x[src_row(i)])), src_row(i) = i*stride + offset
+// (stride 1, offset 0 for all rows; stride T, offset T-1 for the last position of each row).
+template <typename TA>
+__global__ void rmsnorm_kernel(const float* __restrict__ x, TA* __restrict__ h, int rows, int d,
+                               int stride, int offset, float eps) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= rows) return;
+  const float* xr = x + ((size_t)warp * stride + offset) * d;
+  float ss = 0.f;
+  if ((d & 127) == 0) {
+    for (int j = lane * 4; j < d; j += 128) {
+      const float4 v = *reinterpret_cast<const float4*>(xr + j);
+      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+  } else {
+    for (int j = lane; j < d; j += 32) ss = fmaf(xr[j], xr[j], ss);
+  }
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss / d + eps);
+  TA* hr = h + (size_t)warp * d;
+  for (int j = lane; j < d; j += 32) hr[j] = from_f<TA>(xr[j] * r);
+}
+
+// fp32 SIMT GEMM, C = A W^T with an elementwise epilogue.  64x64 tile per
+// 256-thread block, 4x4 outputs per thread.
+enum SimtEpi : int { SEPI_STORE = 0, SEPI_RESID = 1, SEPI_RELU2 = 2, SEPI_LOGITS = 3 };
+
+template <int EPI>
+__global__ void __launch_bounds__(256) gemm_simt_f32_kernel(const float* __restrict__ A,
+                                                             const float* __restrict__ W,
+                                                             float* __restrict__ out, int M, int N,
+                                                             int K, int ldo, float cap) {
+  constexpr int BMS = 64, BNS = 64, BKS = 16;
+  __shared__ float As[BKS][BMS + 4];
+  __shared__ float Ws[BKS][BNS + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * BMS, n0 = blockIdx.x * BNS;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += BKS) {
+    for (int i = threadIdx.x; i < BMS * BKS; i += 256) {
+      const int r = i / BKS, kk = i % BKS;
+      const int m = m0 + r, k = k0 + kk, n = n0 + r;
+      As[kk][r] = (m < M && k < K) ? A[(size_t)m * K + k] : 0.f;
+      Ws[kk][r] = (n < N && k < K) ? W[(size_t)n * K + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BKS; ++kk) {
+      float a[4], w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = Ws[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], w[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n >= N) continue;
+      float* o = out + (size_t)m * ldo + n;
+      const float v = acc[i][j];
+      if constexpr (EPI == SEPI_STORE) *o = v;
+      if constexpr (EPI == SEPI_RESID) *o += v;
+      if constexpr (EPI == SEPI_RELU2) { const float r = fmaxf(v, 0.f); *o = r * r; }
+      if constexpr (EPI == SEPI_LOGITS) *o = cap * tanhf(v / cap);
+    }
+  }
+}
+
+// One warp per (row m, head slot): slots [0, n_head) are query heads, n_head
+// the key head, n_head + 1 the value head.  q and k: RoPE at the row's
+// position, then RMSNorm over head_dim; v: copied.  q goes to Q [M, n_head*hd],
+// k and v to the cache row (b, pos).  Each lane holds elements lane + 32 i, so
+// both members of a rotation pair (j, j + hd/2) sit in the same lane.
+template <typename TA, typename TC>
+__global__ void qkv_post_kernel(const float* __restrict__ qkv, TA* __restrict__ q_out,
+                                TC* __restrict__ k_cache, TC* __restrict__ v_cache,
+                                const float* __restrict__ rope_cos, const float* __restrict__ rope_sin,
+                                int M, int n_head, int hd, int T, int pos0, int cache_S, float eps) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int slots = n_head + 2;
+  if (warp >= M * slots) return;
+  const int m = warp / slots, head = warp % slots;
+  const int b = m / T, pos = pos0 + (m % T);
+  const int per = hd / 32, half = hd / 2;     // hd in {64, 128}
+  const float* src = qkv + (size_t)m * (slots * hd) + head * hd;
+  float v[4];
+  for (int i = 0; i < per; ++i) v[i] = src[lane + 32 * i];
+  if (head <= n_head) {
+    float ss = 0.f;
+    for (int i = 0; i < per; ++i) ss = fmaf(v[i], v[i], ss);
+    ss = warp_sum(ss);
+    const float r = rsqrtf(ss / hd + eps);
+    for (int i = 0; i < per / 2; ++i) {
+      const int j = lane + 32 * i;             // first member of the pair, j < hd/2
+      const float c = rope_cos[(size_t)pos * half + j], s = rope_sin[(size_t)pos * half + j];
+      const float x0 = v[i] * r, x1 = v[i + per / 2] * r;
+      v[i] = x0 * c - x1 * s;
+      v[i + per / 2] = x0 * s + x1 * c;
+    }
+  }
+  if (head < n_head) {
+    TA* dst = q_out + (size_t)m * (n_head * hd) + head * hd;
+    for (int i = 0; i < per; ++i) dst[lane + 32 * i] = from_f<TA>(v[i]);
+  } else {
+    TC* dst = (head == n_head ? k_cache : v_cache) + ((size_t)b * cache_S + pos) * hd;
+    for (int i = 0; i < per; ++i) dst[lane + 32 * i] = from_f<TC>(v[i]);
+  }
+}
+
+// fp32 -> bf16 (round to nearest even) weight conversion
+__global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+                                   size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = __float2bfloat16_rn(src[i]);
+}
+
+}  // namespace nc

@@ -1,0 +1,707 @@
+// Runtime behind the nc C ABI: model object, weight upload and bf16
+// conversion, RoPE table, KV cache, activation workspace, TMA descriptors,
+// and the per-call kernel sequence of the forward pass (prefill and decode).
+//
+// Forward pass, per the nanochat pages (yelogs.com story "technical details and
+// official Q&A"; geoz.com.cn "development tricks"; apidog.com/th "how nanochat
+// works" items 1, 3, 5, 6):
+//   x = rms(E[tok]);  h = rms(x)
+//   per layer: [q;k;v] = h Wqkv^T;  q, k <- rms(rope(.)) ;  cache <- k, v
+//              x += attn(q, cache) Wo^T;  h = rms(x)
+//              x += relu(h Wfc^T)^2 Wproj^T;  h = rms(x)
+//   logits = cap * tanh(h Wu^T / cap)
+#include "nc.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "k_attn_simt.cuh"
+#include "k_gemm_tc.cuh"
+#include "k_rowops.cuh"
+#include "nc_common.cuh"
+
+using namespace nc;
+
+namespace {
+
+constexpr int64_t kGuardElems = 2048;       // sentinel guard before and after each cache
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool load_encode() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] matrix, box = 64 columns
+// (128 bytes, one swizzle row) x box_rows rows, 128-byte swizzle, zero fill.
+bool make_tmap(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  if (!load_encode()) return false;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (cols * 2) % 16) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+nc_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return NC_OK;
+  return e == cudaErrorMemoryAllocation ? NC_ERR_OOM : NC_ERR_CUDA;
+}
+
+#define NC_TRY(expr)                                  \
+  do {                                                \
+    cudaError_t e_ = (expr);                          \
+    if (e_ != cudaSuccess) return from_cuda(e_);      \
+  } while (0)
+
+inline unsigned blocks_for_warps(int64_t warps, int threads = 256) {
+  return (unsigned)((warps * 32 + threads - 1) / threads);
+}
+
+}  // namespace
+
+struct nc_model {
+  nc_config cfg{};
+  int device = 0, num_sms = 148;
+  bool bf16 = true;
+  size_t wbytes = 2;                   // bytes per weight / activation / cache element
+  void* weights = nullptr;             // compute dtype, canonical order
+  const void* E = nullptr;
+  const void* Wu = nullptr;
+  std::vector<const void*> wqkv, wo, wfc, wproj;
+  float* rope_cos = nullptr;           // [max_seq][hd/2]
+  float* rope_sin = nullptr;
+  void* k_alloc = nullptr;             // [guard][L][B_max][S][hd][guard]
+  void* v_alloc = nullptr;
+  int64_t kv_elems = 0, layer_elems = 0;
+  int32_t length = 0, batch = 0;
+  int64_t max_rows = 0;
+  float* x = nullptr;                  // fp32 residual [max_rows][d]
+  void* h = nullptr;                   // normed activations [max_rows][d]
+  void* q = nullptr;                   // [max_rows][n_head*hd]
+  void* att = nullptr;                 // [max_rows][n_head*hd]
+  void* u = nullptr;                   // [max_rows][d_mlp]
+  float* c32 = nullptr;                // fp32 path: raw QKV [max_rows][(n_head+2)*hd]
+  void* h_last = nullptr;              // [max_batch][d]
+  int32_t* tok_stage = nullptr;
+  float* logit_stage = nullptr;
+  size_t logit_stage_bytes = 0;
+  int* err = nullptr;
+  int64_t launches = 0;
+  uint64_t wait_limit_ns = kDefaultWaitNs;
+  // per-kernel-class event timing (nc_profile_begin / nc_profile_end)
+  struct ProfRec {
+    int cls;
+    cudaEvent_t a, b;
+    int64_t launches;
+  };
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  std::vector<ProfRec> recs;
+  CUtensorMap tm_h{}, tm_att{}, tm_u{}, tm_hlast{}, tm_wu{};
+  std::vector<CUtensorMap> tm_wqkv, tm_wo, tm_wfc, tm_wproj;
+
+  void* kc(int l) const { return static_cast<char*>(k_alloc) + (kGuardElems + l * layer_elems) * wbytes; }
+  void* vc(int l) const { return static_cast<char*>(v_alloc) + (kGuardElems + l * layer_elems) * wbytes; }
+};
+
+namespace {
+
+void free_model(nc_model* m) {
+  if (!m) return;
+  for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
+  void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->k_alloc, m->v_alloc, m->x,
+                  m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
+                  m->tok_stage, m->logit_stage, m->err};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  delete m;
+}
+
+cudaEvent_t next_event(nc_model* m) {
+  if (m->ev_used == m->ev_pool.size()) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    m->ev_pool.push_back(e);
+  }
+  return m->ev_pool[m->ev_used++];
+}
+
+// Brackets the kernels launched in its lifetime with two events when the
+// model is profiling; attributes them to one kernel class.
+struct KScope {
+  nc_model* m;
+  cudaStream_t s;
+  size_t rec = SIZE_MAX;
+  int64_t l0 = 0;
+  KScope(nc_model* m_, int cls, cudaStream_t s_) : m(m_), s(s_) {
+    if (!m->profiling) return;
+    cudaEvent_t a = next_event(m), b = next_event(m);
+    if (!a || !b) return;
+    cudaEventRecord(a, s);
+    l0 = m->launches;
+    rec = m->recs.size();
+    m->recs.push_back({cls, a, b, 0});
+  }
+  ~KScope() {
+    if (rec == SIZE_MAX) return;
+    cudaEventRecord(m->recs[rec].b, s);
+    m->recs[rec].launches = m->launches - l0;
+  }
+};
+
+nc_status validate(const nc_config* c) {
+  if (!c) return NC_ERR_INVALID_ARG;
+  if (c->n_layer < 1 || c->d_model < 32 || c->n_head < 1 || c->head_dim < 32 || c->d_mlp < 1 ||
+      c->vocab < 1 || c->max_batch < 1 || c->max_seq < 1 || !(c->rope_base > 0.f) ||
+      !(c->softcap > 0.f) || !(c->rms_eps >= 0.f) || (c->dtype != NC_F32 && c->dtype != NC_BF16))
+    return NC_ERR_INVALID_ARG;
+  if (c->n_kv_head != 1) return NC_ERR_UNSUPPORTED;
+  if (c->dtype == NC_BF16) {
+    if (c->head_dim != 128 || c->d_model % 256 || c->d_mlp % 256 || c->vocab % 256 ||
+        ((c->n_head + 2) * 128) % 256)
+      return NC_ERR_UNSUPPORTED;
+  } else {
+    if ((c->head_dim != 64 && c->head_dim != 128) || c->d_model % 32) return NC_ERR_UNSUPPORTED;
+  }
+  return NC_OK;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_gemm_tc(nc_model* m, const CUtensorMap& ta, const CUtensorMap& tb,
+                           const GemmArgs& a, cudaStream_t s) {
+  using C = TcCfg<BN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int tiles = ((a.M + 127) / 128) * (a.N / BN);
+  if (tiles == 0) return cudaSuccess;
+  const int grid = tiles < m->num_sms ? tiles : m->num_sms;
+  gemm_tc_kernel<BN, EPI><<<grid, 192, C::SMEM, s>>>(ta, tb, a);
+  m->launches++;
+  return cudaGetLastError();
+}
+
+GemmArgs base_args(nc_model* m, int M, int N, int K) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.err = m->err;
+  a.wait_limit_ns = m->wait_limit_ns;
+  a.eps = m->cfg.rms_eps;
+  a.softcap = m->cfg.softcap;
+  return a;
+}
+
+template <int EPI>
+cudaError_t launch_simt_gemm(nc_model* m, const float* A, const float* W, float* out, int M, int N,
+                             int K, int ldo, cudaStream_t s) {
+  dim3 grid((N + 63) / 64, (M + 63) / 64);
+  gemm_simt_f32_kernel<EPI><<<grid, 256, 0, s>>>(A, W, out, M, N, K, ldo, m->cfg.softcap);
+  m->launches++;
+  return cudaGetLastError();
+}
+
+// The whole forward pass over M = B*T rows at positions pos0 .. pos0+T-1.
+nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float* logits,
+                  bool last_only, cudaStream_t s) {
+  const nc_config& c = m->cfg;
+  const int M = B * T, d = c.d_model, hd = c.head_dim, nh = c.n_head, F = c.d_mlp, V = c.vocab;
+  const int NQKV = (nh + 2) * hd, NQ = nh * hd;
+  const float eps = c.rms_eps;
+  const int out_rows = last_only ? B : M;
+  const bool bf = m->bf16;
+  using bf16 = __nv_bfloat16;
+
+  {  // x = rms(E[tok]); h = rms(x)
+    KScope ks(m, NC_K_EMBED, s);
+    if (bf)
+      embed_rmsnorm_kernel<bf16, bf16><<<blocks_for_warps(M), 256, 0, s>>>(
+          tok, static_cast<const bf16*>(m->E), m->x, static_cast<bf16*>(m->h), M, d, V, eps, m->err);
+    else
+      embed_rmsnorm_kernel<float, float><<<blocks_for_warps(M), 256, 0, s>>>(
+          tok, static_cast<const float*>(m->E), m->x, static_cast<float*>(m->h), M, d, V, eps, m->err);
+    m->launches++;
+    NC_TRY(cudaGetLastError());
+  }
+  for (int l = 0; l < c.n_layer; ++l) {
+    {  // [q;k;v] = h Wqkv^T; RoPE + QK-norm; q -> Q, k/v -> cache
+      KScope ks(m, NC_K_QKV, s);
+      if (bf) {
+        GemmArgs a = base_args(m, M, NQKV, d);
+        a.q_out = static_cast<bf16*>(m->q);
+        a.k_cache = static_cast<bf16*>(m->kc(l));
+        a.v_cache = static_cast<bf16*>(m->vc(l));
+        a.rope_cos = m->rope_cos;
+        a.rope_sin = m->rope_sin;
+        a.n_head = nh;
+        a.T = T;
+        a.pos0 = pos0;
+        a.cache_S = c.max_seq;
+        NC_TRY((launch_gemm_tc<256, EPI_QKV>(m, m->tm_h, m->tm_wqkv[l], a, s)));
+      } else {
+        NC_TRY(launch_simt_gemm<SEPI_STORE>(m, static_cast<const float*>(m->h),
+                                            static_cast<const float*>(m->wqkv[l]), m->c32, M, NQKV,
+                                            d, NQKV, s));
+        qkv_post_kernel<float, float><<<blocks_for_warps((int64_t)M * (nh + 2)), 256, 0, s>>>(
+            m->c32, static_cast<float*>(m->q), static_cast<float*>(m->kc(l)),
+            static_cast<float*>(m->vc(l)), m->rope_cos, m->rope_sin, M, nh, hd, T, pos0, c.max_seq,
+            eps);
+        m->launches++;
+        NC_TRY(cudaGetLastError());
+      }
+    }
+    {  // causal MQA attention over the cache
+      KScope ks(m, NC_K_ATTN, s);
+      if (bf)
+        attn_simt_kernel<bf16, bf16><<<blocks_for_warps((int64_t)M * nh), 256, 0, s>>>(
+            static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
+            static_cast<const bf16*>(m->vc(l)), static_cast<bf16*>(m->att), M, nh, hd, T, pos0,
+            c.max_seq);
+      else
+        attn_simt_kernel<float, float><<<blocks_for_warps((int64_t)M * nh), 256, 0, s>>>(
+            static_cast<const float*>(m->q), static_cast<const float*>(m->kc(l)),
+            static_cast<const float*>(m->vc(l)), static_cast<float*>(m->att), M, nh, hd, T, pos0,
+            c.max_seq);
+      m->launches++;
+      NC_TRY(cudaGetLastError());
+    }
+    {  // x += att Wo^T
+      KScope ks(m, NC_K_OPROJ, s);
+      if (bf) {
+        GemmArgs a = base_args(m, M, d, NQ);
+        a.x = m->x;
+        a.ldo = d;
+        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_att, m->tm_wo[l], a, s)));
+      } else {
+        NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->att),
+                                            static_cast<const float*>(m->wo[l]), m->x, M, d, NQ, d, s));
+      }
+    }
+    {  // h = rms(x)
+      KScope ks(m, NC_K_NORM, s);
+      if (bf)
+        rmsnorm_kernel<bf16><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<bf16*>(m->h), M, d, 1, 0, eps);
+      else
+        rmsnorm_kernel<float><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<float*>(m->h), M, d, 1, 0, eps);
+      m->launches++;
+      NC_TRY(cudaGetLastError());
+    }
+    {  // u = relu(h Wfc^T)^2
+      KScope ks(m, NC_K_FC, s);
+      if (bf) {
+        GemmArgs a = base_args(m, M, F, d);
+        a.out_bf16 = static_cast<bf16*>(m->u);
+        a.ldo = F;
+        NC_TRY((launch_gemm_tc<256, EPI_RELU2>(m, m->tm_h, m->tm_wfc[l], a, s)));
+      } else {
+        NC_TRY(launch_simt_gemm<SEPI_RELU2>(m, static_cast<const float*>(m->h),
+                                            static_cast<const float*>(m->wfc[l]),
+                                            static_cast<float*>(m->u), M, F, d, F, s));
+      }
+    }
+    {  // x += u Wproj^T
+      KScope ks(m, NC_K_PROJ, s);
+      if (bf) {
+        GemmArgs a = base_args(m, M, d, F);
+        a.x = m->x;
+        a.ldo = d;
+        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_u, m->tm_wproj[l], a, s)));
+      } else {
+        NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->u),
+                                            static_cast<const float*>(m->wproj[l]), m->x, M, d, F, d, s));
+      }
+    }
+    {  // h = rms(x): next block's pre-attention norm, or the final norm
+      KScope ks(m, NC_K_NORM, s);
+      const bool final_last = last_only && l == c.n_layer - 1;
+      const int rows = final_last ? B : M;
+      void* dst = final_last ? m->h_last : m->h;
+      if (bf)
+        rmsnorm_kernel<bf16><<<blocks_for_warps(rows), 256, 0, s>>>(
+            m->x, static_cast<bf16*>(dst), rows, d, final_last ? T : 1, final_last ? T - 1 : 0, eps);
+      else
+        rmsnorm_kernel<float><<<blocks_for_warps(rows), 256, 0, s>>>(
+            m->x, static_cast<float*>(dst), rows, d, final_last ? T : 1, final_last ? T - 1 : 0, eps);
+      m->launches++;
+      NC_TRY(cudaGetLastError());
+    }
+  }
+  {  // logits = cap * tanh(h Wu^T / cap)
+    KScope ks(m, NC_K_LMHEAD, s);
+    if (bf) {
+      GemmArgs a = base_args(m, out_rows, V, d);
+      a.out_f32 = logits;
+      a.ldo = V;
+      NC_TRY((launch_gemm_tc<256, EPI_LOGITS>(m, last_only ? m->tm_hlast : m->tm_h, m->tm_wu, a, s)));
+    } else {
+      NC_TRY(launch_simt_gemm<SEPI_LOGITS>(
+          m, static_cast<const float*>(last_only ? m->h_last : m->h),
+          static_cast<const float*>(m->Wu), logits, out_rows, V, d, V, s));
+    }
+  }
+  return NC_OK;
+}
+
+// Resolve the token and logit buffers to device memory, staging host buffers.
+nc_status run_call(nc_model* m, const int32_t* tokens, int B, int T, int pos0, float* logits,
+                   bool last_only, cudaStream_t s) {
+  const int M = B * T;
+  const int32_t* tok_dev = tokens;
+  if (!is_device_ptr(tokens)) {
+    NC_TRY(cudaMemcpyAsync(m->tok_stage, tokens, (size_t)M * 4, cudaMemcpyHostToDevice, s));
+    tok_dev = m->tok_stage;
+  }
+  const size_t out_bytes = (size_t)(last_only ? B : M) * m->cfg.vocab * 4;
+  float* out_dev = logits;
+  const bool host_out = !is_device_ptr(logits);
+  if (host_out) {
+    if (m->logit_stage_bytes < out_bytes) {
+      NC_TRY(cudaStreamSynchronize(s));
+      if (m->logit_stage) cudaFree(m->logit_stage);
+      m->logit_stage = nullptr;
+      m->logit_stage_bytes = 0;
+      NC_TRY(cudaMalloc(&m->logit_stage, out_bytes));
+      m->logit_stage_bytes = out_bytes;
+    }
+    out_dev = m->logit_stage;
+  }
+  nc_status st = forward(m, tok_dev, B, T, pos0, out_dev, last_only, s);
+  if (st != NC_OK) return st;
+  if (host_out) NC_TRY(cudaMemcpyAsync(logits, out_dev, out_bytes, cudaMemcpyDeviceToHost, s));
+  return NC_OK;
+}
+
+__global__ void wait_nothing_kernel(int* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, limit_ns)) atomicOr(err, NC_DEVFLAG_TIMEOUT);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nc_status_string(nc_status s) {
+  switch (s) {
+    case NC_OK: return "ok";
+    case NC_ERR_INVALID_ARG: return "invalid argument";
+    case NC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case NC_ERR_OOM: return "out of device memory";
+    case NC_ERR_STATE: return "invalid state for this call";
+    case NC_ERR_CAPACITY: return "KV cache full";
+    case NC_ERR_TOKEN: return "token id out of range";
+    case NC_ERR_TIMEOUT: return "device wait timed out";
+    case NC_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model** out) {
+  if (!out) return NC_ERR_INVALID_ARG;
+  *out = nullptr;
+  nc_status st = validate(cfg);
+  if (st != NC_OK) return st;
+  if (!weights) return NC_ERR_INVALID_ARG;
+  nc_model* m = new (std::nothrow) nc_model();
+  if (!m) return NC_ERR_OOM;
+  m->cfg = *cfg;
+  m->bf16 = cfg->dtype == NC_BF16;
+  m->wbytes = m->bf16 ? 2 : 4;
+  const nc_config& c = m->cfg;
+  const int64_t d = c.d_model, hd = c.head_dim, nh = c.n_head, F = c.d_mlp, V = c.vocab;
+  const int64_t NQKV = (nh + 2) * hd, NQ = nh * hd;
+  const int64_t layer_params = NQKV * d + d * NQ + F * d + d * F;
+  const int64_t n_params = 2 * V * d + c.n_layer * layer_params;
+
+#define CREATE_TRY(expr)                       \
+  do {                                         \
+    cudaError_t e_ = (expr);                   \
+    if (e_ != cudaSuccess) {                   \
+      free_model(m);                           \
+      return from_cuda(e_);                    \
+    }                                          \
+  } while (0)
+
+  CREATE_TRY(cudaGetDevice(&m->device));
+  CREATE_TRY(cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device));
+
+  // weights: upload fp32, convert to the compute dtype
+  CREATE_TRY(cudaMalloc(&m->weights, n_params * m->wbytes));
+  if (m->bf16) {
+    float* tmp = nullptr;
+    const bool dev_src = is_device_ptr(weights);
+    if (!dev_src) {
+      CREATE_TRY(cudaMalloc(&tmp, n_params * 4));
+      cudaError_t e = cudaMemcpy(tmp, weights, n_params * 4, cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) {
+        cudaFree(tmp);
+        free_model(m);
+        return from_cuda(e);
+      }
+    }
+    f32_to_bf16_kernel<<<4 * m->num_sms, 256>>>(dev_src ? weights : tmp,
+                                                 static_cast<__nv_bfloat16*>(m->weights), n_params);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (tmp) cudaFree(tmp);
+    CREATE_TRY(e);
+  } else {
+    CREATE_TRY(cudaMemcpy(m->weights, weights, n_params * 4, cudaMemcpyDefault));
+  }
+  {
+    const char* p = static_cast<const char*>(m->weights);
+    const size_t wb = m->wbytes;
+    m->E = p;
+    p += V * d * wb;
+    for (int l = 0; l < c.n_layer; ++l) {
+      m->wqkv.push_back(p);
+      p += NQKV * d * wb;
+      m->wo.push_back(p);
+      p += d * NQ * wb;
+      m->wfc.push_back(p);
+      p += F * d * wb;
+      m->wproj.push_back(p);
+      p += d * F * wb;
+    }
+    m->Wu = p;
+  }
+
+  // RoPE table, computed in double on the host: theta = p * base^(-2j/hd)
+  {
+    const int64_t half = hd / 2;
+    std::vector<float> cs(c.max_seq * half), sn(c.max_seq * half);
+    for (int64_t p = 0; p < c.max_seq; ++p)
+      for (int64_t j = 0; j < half; ++j) {
+        const double inv = std::pow((double)c.rope_base, -2.0 * (double)j / (double)hd);
+        const double th = (double)p * inv;
+        cs[p * half + j] = (float)std::cos(th);
+        sn[p * half + j] = (float)std::sin(th);
+      }
+    CREATE_TRY(cudaMalloc(&m->rope_cos, cs.size() * 4));
+    CREATE_TRY(cudaMalloc(&m->rope_sin, sn.size() * 4));
+    CREATE_TRY(cudaMemcpy(m->rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
+    CREATE_TRY(cudaMemcpy(m->rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
+  }
+
+  // KV cache with sentinel guards
+  m->layer_elems = (int64_t)c.max_batch * c.max_seq * hd;
+  m->kv_elems = 2 * kGuardElems + c.n_layer * m->layer_elems;
+  CREATE_TRY(cudaMalloc(&m->k_alloc, m->kv_elems * m->wbytes));
+  CREATE_TRY(cudaMalloc(&m->v_alloc, m->kv_elems * m->wbytes));
+  CREATE_TRY(cudaMemset(m->k_alloc, 0xFF, m->kv_elems * m->wbytes));
+  CREATE_TRY(cudaMemset(m->v_alloc, 0xFF, m->kv_elems * m->wbytes));
+
+  // workspace
+  m->max_rows = (int64_t)c.max_batch * c.max_seq;
+  const int64_t R = m->max_rows;
+  CREATE_TRY(cudaMalloc(&m->x, R * d * 4));
+  CREATE_TRY(cudaMalloc(&m->h, R * d * m->wbytes));
+  CREATE_TRY(cudaMalloc(&m->q, R * NQ * m->wbytes));
+  CREATE_TRY(cudaMalloc(&m->att, R * NQ * m->wbytes));
+  CREATE_TRY(cudaMalloc(&m->u, R * F * m->wbytes));
+  CREATE_TRY(cudaMalloc(&m->h_last, (int64_t)c.max_batch * d * m->wbytes));
+  if (!m->bf16) CREATE_TRY(cudaMalloc(&m->c32, R * NQKV * 4));
+  CREATE_TRY(cudaMalloc(&m->tok_stage, R * 4));
+  CREATE_TRY(cudaMalloc(&m->err, sizeof(int)));
+  CREATE_TRY(cudaMemset(m->h, 0, R * d * m->wbytes));
+  CREATE_TRY(cudaMemset(m->att, 0, R * NQ * m->wbytes));
+  CREATE_TRY(cudaMemset(m->u, 0, R * F * m->wbytes));
+  CREATE_TRY(cudaMemset(m->h_last, 0, (int64_t)c.max_batch * d * m->wbytes));
+  CREATE_TRY(cudaMemset(m->err, 0, sizeof(int)));
+
+  if (m->bf16) {
+    bool ok = make_tmap(&m->tm_h, m->h, R, d, 128) && make_tmap(&m->tm_att, m->att, R, NQ, 128) &&
+              make_tmap(&m->tm_u, m->u, R, F, 128) &&
+              make_tmap(&m->tm_hlast, m->h_last, c.max_batch, d, 128) &&
+              make_tmap(&m->tm_wu, m->Wu, V, d, 256);
+    m->tm_wqkv.resize(c.n_layer);
+    m->tm_wo.resize(c.n_layer);
+    m->tm_wfc.resize(c.n_layer);
+    m->tm_wproj.resize(c.n_layer);
+    for (int l = 0; ok && l < c.n_layer; ++l)
+      ok = make_tmap(&m->tm_wqkv[l], m->wqkv[l], NQKV, d, 256) &&
+           make_tmap(&m->tm_wo[l], m->wo[l], d, NQ, 256) &&
+           make_tmap(&m->tm_wfc[l], m->wfc[l], F, d, 256) &&
+           make_tmap(&m->tm_wproj[l], m->wproj[l], d, F, 256);
+    if (!ok) {
+      free_model(m);
+      return NC_ERR_CUDA;
+    }
+  }
+  CREATE_TRY(cudaDeviceSynchronize());
+  *out = m;
+  return NC_OK;
+#undef CREATE_TRY
+}
+
+void nc_model_destroy(nc_model* m) {
+  if (!m) return;
+  cudaDeviceSynchronize();
+  free_model(m);
+}
+
+nc_status nc_kv_reset(nc_model* m, nc_stream_t) {
+  if (!m) return NC_ERR_INVALID_ARG;
+  m->length = 0;
+  m->batch = 0;
+  return NC_OK;
+}
+
+nc_status nc_prefill(nc_model* m, const int32_t* tokens, int32_t B, int32_t T, float* logits,
+                     int32_t last_only, nc_stream_t stream) {
+  if (!m || !tokens || !logits) return NC_ERR_INVALID_ARG;
+  if (B < 1 || B > m->cfg.max_batch || T < 1 || T > m->cfg.max_seq) return NC_ERR_INVALID_ARG;
+  if (m->length != 0) return NC_ERR_STATE;
+  nc_status st = run_call(m, tokens, B, T, 0, logits, last_only != 0, stream);
+  if (st != NC_OK) return st;
+  m->length = T;
+  m->batch = B;
+  return NC_OK;
+}
+
+nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, float* logits,
+                         nc_stream_t stream) {
+  if (!m || !tokens || !logits) return NC_ERR_INVALID_ARG;
+  if (m->length == 0) return NC_ERR_STATE;
+  if (B != m->batch) return NC_ERR_INVALID_ARG;
+  if (m->length >= m->cfg.max_seq) return NC_ERR_CAPACITY;
+  nc_status st = run_call(m, tokens, B, 1, m->length, logits, false, stream);
+  if (st != NC_OK) return st;
+  m->length += 1;
+  return NC_OK;
+}
+
+nc_status nc_sync_status(nc_model* m, nc_stream_t stream) {
+  if (!m) return NC_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return NC_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return NC_ERR_CUDA;
+  int flags = 0;
+  if (cudaMemcpy(&flags, m->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NC_ERR_CUDA;
+  if (flags) cudaMemset(m->err, 0, sizeof(int));
+  if (flags & NC_DEVFLAG_TIMEOUT) return NC_ERR_TIMEOUT;
+  if (flags & NC_DEVFLAG_TOKEN) return NC_ERR_TOKEN;
+  if (flags) return NC_ERR_CUDA;
+  return NC_OK;
+}
+
+nc_status nc_kv_length(const nc_model* m, int32_t* length, int32_t* batch) {
+  if (!m) return NC_ERR_INVALID_ARG;
+  if (length) *length = m->length;
+  if (batch) *batch = m->batch;
+  return NC_OK;
+}
+
+nc_status nc_kv_layout(const nc_model* m, int64_t* total_bytes, int64_t* guard_elems,
+                       int32_t* elem_bytes) {
+  if (!m) return NC_ERR_INVALID_ARG;
+  if (total_bytes) *total_bytes = m->kv_elems * (int64_t)m->wbytes;
+  if (guard_elems) *guard_elems = kGuardElems;
+  if (elem_bytes) *elem_bytes = (int32_t)m->wbytes;
+  return NC_OK;
+}
+
+nc_status nc_kv_read(nc_model* m, void* k_dst, void* v_dst, nc_stream_t stream) {
+  if (!m || !k_dst || !v_dst) return NC_ERR_INVALID_ARG;
+  const size_t bytes = m->kv_elems * m->wbytes;
+  NC_TRY(cudaMemcpyAsync(k_dst, m->k_alloc, bytes, cudaMemcpyDefault, stream));
+  NC_TRY(cudaMemcpyAsync(v_dst, m->v_alloc, bytes, cudaMemcpyDefault, stream));
+  return NC_OK;
+}
+
+int64_t nc_launch_count(const nc_model* m) { return m ? m->launches : -1; }
+
+nc_status nc_gemm_bf16(nc_model* m, const void* A, const void* W, float* C, int32_t M, int32_t N,
+                       int32_t K, nc_stream_t stream) {
+  if (!m || !A || !W || !C || M < 1 || N < 256 || K < 8 || N % 256 || K % 8) return NC_ERR_INVALID_ARG;
+  if (!is_device_ptr(A) || !is_device_ptr(W) || !is_device_ptr(C)) return NC_ERR_INVALID_ARG;
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, A, M, K, 128) || !make_tmap(&tb, W, N, K, 256)) return NC_ERR_INVALID_ARG;
+  GemmArgs a = base_args(m, M, N, K);
+  a.out_f32 = C;
+  a.ldo = N;
+  NC_TRY((launch_gemm_tc<256, EPI_STORE>(m, ta, tb, a, stream)));
+  return NC_OK;
+}
+
+nc_status nc_debug_wait_timeout(nc_model* m, int64_t limit_ns, nc_stream_t stream) {
+  if (!m || limit_ns < 0 || limit_ns > 10000000000ll) return NC_ERR_INVALID_ARG;
+  wait_nothing_kernel<<<1, 32, 0, stream>>>(m->err, (unsigned long long)limit_ns);
+  m->launches++;
+  NC_TRY(cudaGetLastError());
+  return NC_OK;
+}
+
+nc_status nc_profile_begin(nc_model* m) {
+  if (!m) return NC_ERR_INVALID_ARG;
+  m->recs.clear();
+  m->ev_used = 0;
+  m->profiling = true;
+  return NC_OK;
+}
+
+nc_status nc_profile_end(nc_model* m, nc_stream_t stream, double* ms, int64_t* launches) {
+  if (!m || !ms || !launches) return NC_ERR_INVALID_ARG;
+  m->profiling = false;
+  for (int i = 0; i < NC_KCLASS_COUNT; ++i) {
+    ms[i] = 0.0;
+    launches[i] = 0;
+  }
+  NC_TRY(cudaStreamSynchronize(stream));
+  for (const auto& r : m->recs) {
+    float t = 0.f;
+    NC_TRY(cudaEventElapsedTime(&t, r.a, r.b));
+    ms[r.cls] += t;
+    launches[r.cls] += r.launches;
+  }
+  m->recs.clear();
+  m->ev_used = 0;
+  return NC_OK;
+}
+
+nc_status nc_set_wait_limit(nc_model* m, int64_t limit_ns) {
+  if (!m || limit_ns < 1000 || limit_ns > 60000000000ll) return NC_ERR_INVALID_ARG;
+  m->wait_limit_ns = (uint64_t)limit_ns;
+  return NC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,202 @@
+/*
+ * nc.h -- C ABI of the B300-native forward pass of a nanochat-style GPT.
+ *
+ * The model (yelogs.com nanochat story, "technical details and official Q&A";
+ * apidog.com/th "train your own ChatGPT", "how nanochat works" item 1) is a
+ * dense decoder-only transformer: untied token embedding E and unembedding
+ * Wu, parameter-free RMSNorm after the embedding, before attention, before
+ * the MLP and before the unembedding; bias-free QKV projection; RoPE from a
+ * precomputed table (geoz.com.cn NanoChat article, "development tricks");
+ * parameter-free QK-norm; causal multi-query attention (one K/V head shared by
+ * every query head) with scale 1/sqrt(head_dim); output projection and
+ * residual; ReLU^2 MLP and residual; logits = softcap * tanh(z / softcap).
+ * The inference engine runs it as a full-sequence prefill that fills a KV
+ * cache, then one-token decode steps over that cache (szyisi.cn "$100 ...
+ * ChatGPT clone", inference engine paragraph; apidog.com/th item 6).
+ *
+ * Conventions
+ *  - Every pointer argument may be a device pointer or a host pointer (pinned
+ *    or pageable); the library checks with cudaPointerGetAttributes and stages
+ *    host buffers through model-owned device memory on the given stream.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream)
+ *    unless a host buffer forces a synchronous copy.  A model is not
+ *    thread-safe: one host thread drives it.
+ *  - Argument and state errors are returned immediately, with nothing
+ *    enqueued.  Conditions found on the device (a token id outside [0, vocab),
+ *    an expired bounded wait inside a kernel) are recorded in a device error
+ *    word and returned by nc_sync_status().
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef NC_H_
+#define NC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define NC_API __attribute__((visibility("default")))
+#else
+#define NC_API
+#endif
+
+typedef struct CUstream_st* nc_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+  NC_OK = 0,
+  NC_ERR_INVALID_ARG = 1, /* a null pointer, a size out of range, a bad config field */
+  NC_ERR_UNSUPPORTED = 2, /* a config this build has no kernels for */
+  NC_ERR_OOM = 3,         /* device allocation failed */
+  NC_ERR_STATE = 4,       /* prefill on a non-empty cache, decode before prefill */
+  NC_ERR_CAPACITY = 5,    /* the KV cache is full (length == max_seq) */
+  NC_ERR_TOKEN = 6,       /* (device) a token id outside [0, vocab) was seen */
+  NC_ERR_TIMEOUT = 7,     /* (device) a bounded pipeline wait expired */
+  NC_ERR_CUDA = 8         /* a CUDA runtime error */
+} nc_status;
+
+typedef enum { NC_F32 = 0, NC_BF16 = 1 } nc_dtype;
+
+/*
+ * Model shape and capacity.  Shapes of the pages' models: d20 has d_model
+ * 1280, 10 heads of dim 128 (szyisi.cn, "pre-training"); d12/d24 follow the
+ * same depth rule (d_model = 64 * depth, heads of 128, MLP = 4 * d_model);
+ * vocab 65536 = 2**16 (szyisi.cn, tokenizer section).
+ *   n_kv_head must be 1 (multi-query attention).
+ *   NC_BF16: weights, activations and the KV cache in bf16 with fp32
+ *            accumulation and an fp32 residual stream; needs head_dim == 128,
+ *            d_model, d_mlp and n_head*head_dim multiples of 256, vocab a
+ *            multiple of 256.
+ *   NC_F32:  everything fp32 (SIMT kernels); head_dim 64 or 128.
+ *   rms_eps sits inside the square root: x / sqrt(mean(x^2) + eps).
+ *   max_batch / max_seq size the KV cache [n_layer][max_batch][max_seq][head_dim]
+ *   (K and V each) and the activation workspace (max_batch * max_seq rows).
+ */
+typedef struct {
+  int32_t n_layer, d_model, n_head, n_kv_head, head_dim, d_mlp, vocab;
+  float rope_base, softcap, rms_eps;
+  int32_t dtype; /* nc_dtype */
+  int32_t max_batch, max_seq;
+} nc_config;
+
+typedef struct nc_model nc_model;
+
+/*
+ * Create a model on the current CUDA device.
+ *   weights: packed fp32 values, canonical order (PyTorch Linear [out, in]
+ *            row-major, as F.linear takes them: apidog.com/th item 3):
+ *            E[vocab][d]; for each layer Wqkv[(n_head+2)*hd][d] (query heads,
+ *            then the key head, then the value head), Wo[d][n_head*hd],
+ *            Wfc[d_mlp][d], Wproj[d][d_mlp]; then Wu[vocab][d].
+ *            Host or device memory; copied (and rounded to bf16, nearest-even,
+ *            for NC_BF16), so the caller may free it when the call returns.
+ *   out:     receives the model; *out is NULL on failure.
+ * Synchronous.  The model owns its weights, KV cache, RoPE table and workspace.
+ */
+NC_API nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model** out);
+
+/* Free everything the model owns.  NULL is ignored.  Synchronizes the device. */
+NC_API void nc_model_destroy(nc_model* m);
+
+/* Empty the KV cache (length := 0).  Cache contents are left as they are. */
+NC_API nc_status nc_kv_reset(nc_model* m, nc_stream_t stream);
+
+/*
+ * Prefill: run the full forward pass over tokens[B][T] from an empty cache,
+ * write K/V for positions [0, T) of rows [0, B), set the cache length to T.
+ *   tokens:    int32 [B][T], ids in [0, vocab).
+ *   logits:    fp32 [B][T][vocab], or [B][vocab] (position T-1) if last_only.
+ * Errors: NC_ERR_STATE if the cache is not empty; NC_ERR_INVALID_ARG if B is
+ * outside [1, max_batch] or T outside [1, max_seq].
+ */
+NC_API nc_status nc_prefill(nc_model* m, const int32_t* tokens, int32_t B, int32_t T, float* logits,
+                     int32_t last_only, nc_stream_t stream);
+
+/*
+ * Decode step: one new token per row at position p = current length, attending
+ * to cached positions 0..p; appends K/V at p; length := p + 1.
+ *   tokens: int32 [B]; logits: fp32 [B][vocab].
+ * Errors: NC_ERR_STATE before any prefill; NC_ERR_INVALID_ARG if B differs from
+ * the prefill's B; NC_ERR_CAPACITY if length == max_seq.
+ */
+NC_API nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, float* logits,
+                         nc_stream_t stream);
+
+/*
+ * Synchronize `stream`, then report (and clear) the device error word:
+ * NC_ERR_TOKEN, NC_ERR_TIMEOUT, or a pending CUDA error as NC_ERR_CUDA.
+ */
+NC_API nc_status nc_sync_status(nc_model* m, nc_stream_t stream);
+
+/* Current cache length and the prefill batch (0 before the first prefill). */
+NC_API nc_status nc_kv_length(const nc_model* m, int32_t* length, int32_t* batch);
+
+/*
+ * Test hook: copy the whole K and V caches, guard regions included, into
+ * k_dst / v_dst (device or host), each `nc_kv_bytes` bytes.  Layout of each:
+ * [guard][n_layer][max_batch][max_seq][head_dim][guard], elements of
+ * `elem_bytes` (2 for NC_BF16, 4 for NC_F32); guards are `guard_elems`
+ * elements.  At creation the whole buffer holds the sentinel byte 0xFF; a
+ * position is written only when prefill or decode computes it.
+ */
+NC_API nc_status nc_kv_layout(const nc_model* m, int64_t* total_bytes, int64_t* guard_elems,
+                       int32_t* elem_bytes);
+NC_API nc_status nc_kv_read(nc_model* m, void* k_dst, void* v_dst, nc_stream_t stream);
+
+/*
+ * Number of kernels this model has launched since creation (every kernel of
+ * every call, including graph replays).  Used to report launches per step.
+ */
+NC_API int64_t nc_launch_count(const nc_model* m);
+
+/*
+ * Building block, test hook: C[M][N] = A[M][K] * W[N][K]^T with bf16 A and W
+ * (device pointers, row-major, K a multiple of 8, N a multiple of 256) and
+ * fp32 C (device), on the tcgen05 tensor-core GEMM of the prefill path.
+ * Uses the model's error word for timeouts.
+ */
+NC_API nc_status nc_gemm_bf16(nc_model* m, const void* A, const void* W, float* C, int32_t M, int32_t N,
+                       int32_t K, nc_stream_t stream);
+
+/*
+ * Failure-detection hook: launch one CTA that waits, with the library's
+ * bounded wait, on an mbarrier that nothing arrives at, for at most
+ * limit_ns nanoseconds.  nc_sync_status() then returns NC_ERR_TIMEOUT and the
+ * CUDA context stays usable.
+ */
+NC_API nc_status nc_debug_wait_timeout(nc_model* m, int64_t limit_ns, nc_stream_t stream);
+
+/* Upper bound (ns) on every pipeline wait inside the kernels; default 2e9. */
+NC_API nc_status nc_set_wait_limit(nc_model* m, int64_t limit_ns);
+
+/*
+ * Per-kernel timing with CUDA events on the calling stream.  Between
+ * nc_profile_begin and nc_profile_end every kernel the model launches is
+ * bracketed by two events; nc_profile_end synchronizes the stream and returns,
+ * per kernel class, the summed device time (ms) and the number of launches.
+ * Classes (index into the arrays, NC_KCLASS_COUNT entries each):
+ */
+enum {
+  NC_K_EMBED = 0,   /* token embedding + RMSNorm                   */
+  NC_K_QKV = 1,     /* QKV projection + RoPE + QK-norm + cache write */
+  NC_K_ATTN = 2,    /* causal MQA attention (all its kernels)       */
+  NC_K_OPROJ = 3,   /* output projection + residual                 */
+  NC_K_NORM = 4,    /* RMSNorm before the MLP / the next block      */
+  NC_K_FC = 5,      /* MLP up-projection + ReLU^2                    */
+  NC_K_PROJ = 6,    /* MLP down-projection + residual               */
+  NC_K_LMHEAD = 7,  /* unembedding + softcap                        */
+  NC_KCLASS_COUNT = 8
+};
+NC_API nc_status nc_profile_begin(nc_model* m);
+NC_API nc_status nc_profile_end(nc_model* m, nc_stream_t stream, double* ms, int64_t* launches);
+
+/* Static description of a status code. */
+NC_API const char* nc_status_string(nc_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NC_H_ */
