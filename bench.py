@@ -124,16 +124,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def blas_threads():
+    """Threads the oracle's BLAS uses (OpenBLAS defaults to every available core, up to 64)."""
+    try:
+        from threadpoolctl import threadpool_info
+        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except ImportError:
+        env = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+        return int(env) if env else min(len(os.sched_getaffinity(0)), 64)
+
+
 def oracle_tokens_per_s(w, flat, prompt, rows, T):
     """fp64 oracle prefill of `rows` x T tokens; returns (tokens/s, seconds, threads)."""
-    from threadpoolctl import threadpool_info
     from oracle.gpt_oracle import OracleModel
     o = OracleModel(flat, w.shape)
     t0 = time.perf_counter()
     o.prefill(prompt[rows, :T])
     dt = time.perf_counter() - t0
-    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
-    return len(rows) * T / dt, dt, threads
+    return len(rows) * T / dt, dt, blas_threads()
 
 
 def dist_setup():
@@ -171,7 +179,6 @@ def run_reference(args, world, rank):
     flat = nc_inputs.gen_weights(w.shape, w.weight_seed)
     prompt, _ = _tokens(w)
     T = min(512, w.prompt_len)
-    from threadpoolctl import threadpool_info
     from oracle.gpt_oracle import OracleModel
     o = OracleModel(flat, w.shape)
     for _ in range(args.warmup):
@@ -181,7 +188,7 @@ def run_reference(args, world, rank):
         o.prefill(prompt[:1, :T])
     dt = time.perf_counter() - t0
     value = args.steps * T / dt
-    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    threads = blas_threads()
     sample = f"row 0, tokens 0..{T - 1} of {w.name} ({w.batch}x{w.prompt_len}), all-position logits"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

@@ -1,0 +1,402 @@
+// Causal multi-query attention on the tensor cores (bf16 in, fp32 accumulate),
+// flash-style: scores, online softmax and the P.V product stay on chip.
+//
+// Multi-query attention: every query head reads the single K/V head
+// (yelogs.com nanochat story, "technical details and official Q&A"); scale
+// 1/sqrt(head_dim) as in SDPA (apidog.com/th "train your own ChatGPT", "how
+// nanochat works" item 5).
+//
+// Prefill kernel: one CTA = 32 query positions x 2 query heads = 64 rows
+// (4 warps x 16 rows); both heads share every K/V tile loaded into shared
+// memory.  K/V tiles of 64 keys are double-buffered with cp.async; the
+// diagonal tile is masked.  Heavier (later) query blocks are scheduled first.
+//
+// Decode kernel (split over the context): one CTA = one batch row and a
+// chunk of 128 cached keys; the row's n_head query vectors form the 16-row
+// A operand (heads padded to 16), each warp handles 32 keys; partial (max,
+// sum, output) go to a workspace and a combine kernel merges the chunks.
+#pragma once
+
+#include "nc_common.cuh"
+
+namespace nc {
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
+  const int n = pred ? 16 : 0;   // zero-fill when pred is false
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+
+// A [rows][128] bf16 tile in shared memory, rows of 256 B split in 16 chunks
+// of 16 B; chunk c of row r is stored at chunk c ^ (r & 7) to keep ldmatrix
+// conflict-free.
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
+  return base + row * 256 + ((chunk ^ (row & 7)) << 4);
+}
+
+constexpr int ATT_HD = 128;
+
+// Q, O: [B*T][n_head*128] rows m = b*T + t at position pos0 + t; K/V caches
+// [B_max][cache_S][128], keys 0 .. pos0+T-1 valid.
+__global__ void __launch_bounds__(128) attn_prefill_mma_kernel(
+    const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kc,
+    const __nv_bfloat16* __restrict__ Vc, __nv_bfloat16* __restrict__ O, int T, int n_head,
+    int cache_S, int pos0, float scale_log2) {
+  constexpr int BQ = 32, ROWS = 64, BKV = 64;
+  extern __shared__ __align__(128) uint8_t att_smem[];
+  const uint32_t sQ = smem_u32(att_smem);
+  const uint32_t sK0 = sQ + ROWS * 256;                       // 2 stages of K, then 2 of V
+  const uint32_t sV0 = sK0 + 2 * BKV * 256;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qb = gridDim.x - 1 - blockIdx.x;                  // heavy blocks first
+  const int hp = blockIdx.y, b = blockIdx.z;
+  const int q0 = qb * BQ;
+  const int kv_len = pos0 + T;
+  const int ldq = n_head * ATT_HD;
+  const __nv_bfloat16* kbase = Kc + (size_t)b * cache_S * ATT_HD;
+  const __nv_bfloat16* vbase = Vc + (size_t)b * cache_S * ATT_HD;
+
+  // ---- Q tile: row r -> position q0 + r/2, head 2*hp + (r&1)
+  for (int i = tid; i < ROWS * 16; i += 128) {
+    const int r = i >> 4, c = i & 15;
+    const int t = q0 + (r >> 1);
+    const bool ok = t < T;
+    const __nv_bfloat16* src = Q + ((size_t)b * T + (ok ? t : 0)) * ldq + (2 * hp + (r & 1)) * ATT_HD + c * 8;
+    cp_async16(swz(sQ, r, c), src, ok);
+  }
+  const int last_key = min(pos0 + q0 + BQ - 1, kv_len - 1);   // largest key any row needs
+  const int n_blocks = last_key / BKV + 1;
+  auto load_kv = [&](int blk, int stage) {
+    const uint32_t sk = sK0 + stage * BKV * 256, sv = sV0 + stage * BKV * 256;
+    for (int i = tid; i < BKV * 16; i += 128) {
+      const int r = i >> 4, c = i & 15;
+      const int key = blk * BKV + r;
+      const bool ok = key < kv_len;
+      const size_t off = (size_t)(ok ? key : 0) * ATT_HD + c * 8;
+      cp_async16(swz(sk, r, c), kbase + off, ok);
+      cp_async16(swz(sv, r, c), vbase + off, ok);
+    }
+  };
+  load_kv(0, 0);
+  cp_async_commit();
+
+  // per-thread rows within the warp's 16: lane/4 and lane/4 + 8
+  const int r_lo = warp * 16 + (lane >> 2), r_hi = r_lo + 8;
+  const int qpos_lo = pos0 + q0 + (r_lo >> 1), qpos_hi = pos0 + q0 + (r_hi >> 1);
+  float o[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+  uint32_t qf[8][4];
+
+  for (int blk = 0; blk < n_blocks; ++blk) {
+    const int stage = blk & 1;
+    if (blk + 1 < n_blocks) load_kv(blk + 1, stage ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    if (blk == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int chunk = kk * 2 + (lane >> 4);
+        ldsm_x4(swz(sQ, row, chunk), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+      }
+    }
+    const uint32_t sk = sK0 + stage * BKV * 256, sv = sV0 + stage * BKV * 256;
+    // ---- S = Q K^T  (16 x 64 per warp)
+    float s[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+      for (int jp = 0; jp < 4; ++jp) {            // pairs of 8-key tiles
+        const int key = jp * 16 + (lane & 7) + (lane >> 4) * 8;
+        const int chunk = kk * 2 + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(swz(sk, key, chunk), b0, b1, b2, b3);
+        mma_bf16(s[2 * jp], qf[kk], b0, b1);
+        mma_bf16(s[2 * jp + 1], qf[kk], b2, b3);
+      }
+    }
+    // ---- mask (keys beyond the row's position) and online softmax
+    const int kbase_idx = blk * BKV;
+    const bool diag = kbase_idx + BKV - 1 > pos0 + q0;
+    float mx_lo = m_lo, mx_hi = m_hi;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = kbase_idx + j * 8 + (lane & 3) * 2 + e;
+        float a = s[j][e] * scale_log2, c = s[j][2 + e] * scale_log2;
+        if (diag) {
+          if (key > qpos_lo) a = -INFINITY;
+          if (key > qpos_hi) c = -INFINITY;
+        }
+        s[j][e] = a;
+        s[j][2 + e] = c;
+        mx_lo = fmaxf(mx_lo, a);
+        mx_hi = fmaxf(mx_hi, c);
+      }
+    }
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+    const float corr_lo = exp2f(m_lo - mx_lo), corr_hi = exp2f(m_hi - mx_hi);
+    m_lo = mx_lo;
+    m_hi = mx_hi;
+    float sum_lo = 0.f, sum_hi = 0.f;
+    uint32_t pf[4][4];                              // P as A fragments, 4 k-steps of 16 keys
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float p0 = exp2f(s[j][0] - mx_lo), p1 = exp2f(s[j][1] - mx_lo);
+      const float p2 = exp2f(s[j][2] - mx_hi), p3 = exp2f(s[j][3] - mx_hi);
+      sum_lo += p0 + p1;
+      sum_hi += p2 + p3;
+      pf[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
+      pf[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
+    }
+    l_lo = l_lo * corr_lo + sum_lo;
+    l_hi = l_hi * corr_hi + sum_hi;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      o[j][0] *= corr_lo;
+      o[j][1] *= corr_lo;
+      o[j][2] *= corr_hi;
+      o[j][3] *= corr_hi;
+    }
+    // ---- O += P V  (16 x 128 per warp)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+      for (int jp = 0; jp < 8; ++jp) {            // pairs of 8-dim tiles
+        const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int chunk = jp * 2 + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(swz(sv, key, chunk), b0, b1, b2, b3);
+        mma_bf16(o[2 * jp], pf[kk], b0, b1);
+        mma_bf16(o[2 * jp + 1], pf[kk], b2, b3);
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- normalise and store
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+  const float inv_lo = 1.f / l_lo, inv_hi = 1.f / l_hi;
+  const int t_lo = q0 + (r_lo >> 1), t_hi = q0 + (r_hi >> 1);
+  __nv_bfloat16* o_lo = O + ((size_t)b * T + t_lo) * ldq + (2 * hp + (r_lo & 1)) * ATT_HD;
+  __nv_bfloat16* o_hi = O + ((size_t)b * T + t_hi) * ldq + (2 * hp + (r_hi & 1)) * ATT_HD;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int col = j * 8 + (lane & 3) * 2;
+    if (t_lo < T) *reinterpret_cast<uint32_t*>(o_lo + col) = pack_bf16(o[j][0] * inv_lo, o[j][1] * inv_lo);
+    if (t_hi < T) *reinterpret_cast<uint32_t*>(o_hi + col) = pack_bf16(o[j][2] * inv_hi, o[j][3] * inv_hi);
+  }
+}
+
+constexpr size_t ATT_PREFILL_SMEM = (64 + 4 * 64) * 256;     // Q + 2 x (K, V) = 80 KB
+
+// ---------------------------------------------------------------- decode --
+// Q: [B][n_head*128] (one new position per row, at pos = ctx-1); keys 0..ctx-1.
+// Partial results per (row b, chunk c): m, l [B][nchunk][16][2], o [B][nchunk][16][128].
+constexpr int DEC_CHUNK = 128;             // keys per CTA
+constexpr int DEC_KPW = DEC_CHUNK / 4;     // keys per warp
+
+__global__ void __launch_bounds__(128) attn_decode_mma_kernel(
+    const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kc,
+    const __nv_bfloat16* __restrict__ Vc, float* __restrict__ part_o, float* __restrict__ part_ml,
+    int n_head, int cache_S, int ctx, int nchunk, float scale_log2) {
+  extern __shared__ __align__(128) uint8_t att_smem[];
+  const uint32_t sQ = smem_u32(att_smem);                     // 16 rows
+  const uint32_t sK = sQ + 16 * 256;                           // DEC_CHUNK keys
+  const uint32_t sV = sK + DEC_CHUNK * 256;
+  float* red = reinterpret_cast<float*>(att_smem + (16 + 2 * DEC_CHUNK) * 256);  // [4][16][2]
+  float* ored = reinterpret_cast<float*>(att_smem + 16 * 256);  // [4][16][128], aliases K/V
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunk_id = blockIdx.x, b = blockIdx.y;
+  const int k0 = chunk_id * DEC_CHUNK;
+  const int ldq = n_head * ATT_HD;
+  for (int i = tid; i < 16 * 16; i += 128) {
+    const int r = i >> 4, c = i & 15;
+    const bool ok = r < n_head;
+    cp_async16(swz(sQ, r, c), Q + (size_t)b * ldq + (ok ? r : 0) * ATT_HD + c * 8, ok);
+  }
+  const __nv_bfloat16* kb = Kc + (size_t)b * cache_S * ATT_HD;
+  const __nv_bfloat16* vb = Vc + (size_t)b * cache_S * ATT_HD;
+  for (int i = tid; i < DEC_CHUNK * 16; i += 128) {
+    const int r = i >> 4, c = i & 15;
+    const int key = k0 + r;
+    const bool ok = key < ctx;
+    const size_t off = (size_t)(ok ? key : 0) * ATT_HD + c * 8;
+    cp_async16(swz(sK, r, c), kb + off, ok);
+    cp_async16(swz(sV, r, c), vb + off, ok);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+
+  uint32_t qf[8][4];
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+    ldsm_x4(swz(sQ, row, kk * 2 + (lane >> 4)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+  }
+  constexpr int NT = DEC_KPW / 8;                              // 8-key tiles per warp
+  const int wk = warp * DEC_KPW;
+  float s[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+    for (int jp = 0; jp < NT / 2; ++jp) {
+      const int key = wk + jp * 16 + (lane & 7) + (lane >> 4) * 8;
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(swz(sK, key, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
+      mma_bf16(s[2 * jp], qf[kk], b0, b1);
+      mma_bf16(s[2 * jp + 1], qf[kk], b2, b3);
+    }
+  }
+  float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int key = k0 + wk + j * 8 + (lane & 3) * 2 + e;
+      const bool ok = key < ctx;
+      s[j][e] = ok ? s[j][e] * scale_log2 : -INFINITY;
+      s[j][2 + e] = ok ? s[j][2 + e] * scale_log2 : -INFINITY;
+      mx_lo = fmaxf(mx_lo, s[j][e]);
+      mx_hi = fmaxf(mx_hi, s[j][2 + e]);
+    }
+  mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+  mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+  mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+  mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+  // a warp whose keys all lie beyond ctx has max -inf: subtract 0 so exp2 gives 0, not NaN
+  const float ml = mx_lo == -INFINITY ? 0.f : mx_lo, mh = mx_hi == -INFINITY ? 0.f : mx_hi;
+  float sum_lo = 0.f, sum_hi = 0.f;
+  uint32_t pf[NT / 2][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const float p0 = exp2f(s[j][0] - ml), p1 = exp2f(s[j][1] - ml);
+    const float p2 = exp2f(s[j][2] - mh), p3 = exp2f(s[j][3] - mh);
+    sum_lo += p0 + p1;
+    sum_hi += p2 + p3;
+    pf[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
+    pf[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
+  }
+  sum_lo += __shfl_xor_sync(0xffffffffu, sum_lo, 1);
+  sum_lo += __shfl_xor_sync(0xffffffffu, sum_lo, 2);
+  sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, 1);
+  sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, 2);
+  float o[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < NT / 2; ++kk) {
+#pragma unroll
+    for (int jp = 0; jp < 8; ++jp) {
+      const int key = wk + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(swz(sV, key, jp * 2 + (lane >> 4)), b0, b1, b2, b3);
+      mma_bf16(o[2 * jp], pf[kk], b0, b1);
+      mma_bf16(o[2 * jp + 1], pf[kk], b2, b3);
+    }
+  }
+  // ---- merge the 4 warps: per head row, rescale to the CTA max
+  const int rlo = lane >> 2, rhi = rlo + 8;
+  if ((lane & 3) == 0) {
+    red[(warp * 16 + rlo) * 2 + 0] = mx_lo;
+    red[(warp * 16 + rlo) * 2 + 1] = sum_lo;
+    red[(warp * 16 + rhi) * 2 + 0] = mx_hi;
+    red[(warp * 16 + rhi) * 2 + 1] = sum_hi;
+  }
+  __syncthreads();                                             // all warps done with K/V
+  float cm_lo = -INFINITY, cm_hi = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    cm_lo = fmaxf(cm_lo, red[(w * 16 + rlo) * 2]);
+    cm_hi = fmaxf(cm_hi, red[(w * 16 + rhi) * 2]);
+  }
+  const float f_lo = mx_lo == -INFINITY ? 0.f : exp2f(mx_lo - cm_lo);
+  const float f_hi = mx_hi == -INFINITY ? 0.f : exp2f(mx_hi - cm_hi);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int col = j * 8 + (lane & 3) * 2;
+    ored[(warp * 16 + rlo) * 128 + col] = o[j][0] * f_lo;
+    ored[(warp * 16 + rlo) * 128 + col + 1] = o[j][1] * f_lo;
+    ored[(warp * 16 + rhi) * 128 + col] = o[j][2] * f_hi;
+    ored[(warp * 16 + rhi) * 128 + col + 1] = o[j][3] * f_hi;
+  }
+  __syncthreads();
+  // thread = output column; loop over head rows
+  const size_t pbase = ((size_t)b * nchunk + chunk_id) * 16;
+  for (int r = 0; r < n_head; ++r) {
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) acc += ored[(w * 16 + r) * 128 + tid];
+    part_o[(pbase + r) * 128 + tid] = acc;
+  }
+  if (tid < n_head) {
+    float cm = -INFINITY, cl = 0.f;
+    for (int w = 0; w < 4; ++w) cm = fmaxf(cm, red[(w * 16 + tid) * 2]);
+    for (int w = 0; w < 4; ++w) {
+      const float mw = red[(w * 16 + tid) * 2];
+      if (mw != -INFINITY) cl += red[(w * 16 + tid) * 2 + 1] * exp2f(mw - cm);
+    }
+    part_ml[(pbase + tid) * 2 + 0] = cm;
+    part_ml[(pbase + tid) * 2 + 1] = cl;
+  }
+}
+
+constexpr size_t ATT_DECODE_SMEM = (16 + 2 * DEC_CHUNK) * 256 + 4 * 16 * 2 * 4;
+
+// One CTA per (batch row, head): merge the chunks, write bf16 output.
+__global__ void __launch_bounds__(128) attn_decode_combine_kernel(
+    const float* __restrict__ part_o, const float* __restrict__ part_ml,
+    __nv_bfloat16* __restrict__ O, int n_head, int nchunk) {
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  float gm = -INFINITY;
+  for (int c = 0; c < nchunk; ++c) gm = fmaxf(gm, part_ml[(((size_t)b * nchunk + c) * 16 + h) * 2]);
+  float acc = 0.f, l = 0.f;
+  for (int c = 0; c < nchunk; ++c) {
+    const size_t p = ((size_t)b * nchunk + c) * 16 + h;
+    const float mc = part_ml[p * 2];
+    if (mc == -INFINITY) continue;
+    const float f = exp2f(mc - gm);
+    l += part_ml[p * 2 + 1] * f;
+    acc += part_o[p * 128 + tid] * f;
+  }
+  O[((size_t)b * n_head + h) * ATT_HD + tid] = f2bf(acc / l);
+}
+
+}  // namespace nc

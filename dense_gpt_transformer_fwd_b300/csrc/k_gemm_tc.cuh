@@ -14,8 +14,11 @@
 //                 N = BN, K = 16 per instruction; two TMEM accumulators so the
 //                 epilogue of tile i overlaps the main loop of tile i + 1
 //   warps 2..5    epilogue: tcgen05.ld (each warp owns 32 TMEM lanes = 32
-//                 rows), fused math, transpose through shared memory, coalesced
-//                 128-byte row stores
+//                 rows), fused math, then 32-row x 128-byte chunks staged in
+//                 a swizzled shared buffer and written by TMA bulk tensor
+//                 stores (two buffers per warp, so math overlaps the store);
+//                 the residual epilogue TMA-loads the fp32 residual chunk
+//                 into the same buffer, adds, and stores it back.
 // Tiles are visited m-fastest so that CTAs resident at the same time share
 // the W tile (and the whole A panel stays in L2).
 #pragma once
@@ -35,21 +38,14 @@ enum GemmEpi : int {
 
 struct GemmArgs {
   int M, N, K;
-  int ldo;                        // leading dimension of the output (elements)
   // EPI_QKV
-  __nv_bfloat16* q_out;           // [M, n_head * 128]
   __nv_bfloat16* k_cache;         // this layer's K: [B_max][S][128]
   __nv_bfloat16* v_cache;         // this layer's V: [B_max][S][128]
   const float* rope_cos;          // [S][64]
   const float* rope_sin;          // [S][64]
   int n_head, T, pos0, cache_S;
   float eps;
-  // EPI_RESID
-  float* x;
-  // EPI_RELU2
-  __nv_bfloat16* out_bf16;
-  // EPI_LOGITS / EPI_STORE
-  float* out_f32;
+  // EPI_LOGITS
   float softcap;
   // error reporting
   int* err;
@@ -64,8 +60,8 @@ struct TcCfg {
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr int EP_WORDS = 32 * 65;            // per epilogue warp: 32 rows x 65 words
-  static constexpr size_t SMEM = 1024 + STAGES * (size_t)STAGE_BYTES + 4 * EP_WORDS * 4 + 256;
+  static constexpr uint32_t EP_BUF = 4096;             // 32 rows x 128 B
+  static constexpr size_t SMEM = 1024 + STAGES * (size_t)STAGE_BYTES + 4 * 2 * EP_BUF + 256;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -80,20 +76,26 @@ __device__ __forceinline__ float softcap_f(float z, float cap) {
   return cap * (1.0f - __fdividef(2.0f, e + 1.0f));
 }
 
+// Address of 16-byte chunk `cc` (0..7) of row `r` in a 32 x 128 B staging
+// buffer with the 128-byte TMA swizzle (chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t ep_addr(uint32_t buf, int r, int cc) {
+  return buf + r * 128 + ((cc ^ (r & 7)) << 4);
+}
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs args) {
+                   const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   using C = TcCfg<BN>;
   constexpr int BM = C::BM, BK = C::BK, STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * C::A_BYTES;
-  uint32_t* ep_stage = reinterpret_cast<uint32_t*>(sB + STAGES * C::B_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ep_stage + 4 * C::EP_WORDS);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint8_t* sE = sB + STAGES * C::B_BYTES;                       // 4 warps x 2 staging buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 4 * 2 * C::EP_BUF);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, eload[8]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(192, 1)
 
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, TEMPTY = 2 * STAGES + 2,
-            DRAIN = 2 * STAGES + 4;
+            DRAIN = 2 * STAGES + 4, ELOAD = 2 * STAGES + 5;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -117,12 +119,14 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(bar(TEMPTY + a), 128);
     }
     mbar_init(bar(DRAIN), 1);
+    for (int i = 0; i < 8; ++i) mbar_init(bar(ELOAD + i), 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
   tc_fence_before();
@@ -208,9 +212,14 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                         // TMEM lane quarter of this warp
-    uint32_t* st = ep_stage + (warp - 2) * C::EP_WORDS;
+    const int ew = warp - 2;                        // staging slot of this warp
+    const uint32_t buf0 = smem_u32(sE + ew * 2 * C::EP_BUF);
+    const uint32_t eload0 = bar(ELOAD + 2 * ew);
+    uint32_t nload = 0;                             // residual chunk loads issued so far
+    int nstore = 0;                                 // staging buffers used so far
     int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
       const int acc = local & 1;
       if (*abort_flag || !mbar_wait(bar(TFULL + acc), (local >> 1) & 1, limit)) {
         if (!*abort_flag) fail();
@@ -222,74 +231,106 @@ __global__ void __launch_bounds__(192, 1)
       const int my_row = row0 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc * BN;
 
-      if constexpr (EPI == EPI_RELU2) {
+      if constexpr (EPI == EPI_LOGITS || EPI == EPI_STORE) {
+        // 32 fp32 columns per chunk
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          const uint32_t buf = buf0 + (nstore & 1) * C::EP_BUF;
+          float v[32];
+          tmem_ld32(taddr + c, v);
+          if (EPI == EPI_LOGITS) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = softcap_f(v[j], args.softcap);
+          }
+          if (lane == 0) bulk_wait_read<1>();       // this buffer's previous store has read it
+          __syncwarp();
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+            st_shared_v4(ep_addr(buf, lane, cc), v[4 * cc], v[4 * cc + 1], v[4 * cc + 2], v[4 * cc + 3]);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, buf, n0 + c, row0);
+            bulk_commit();
+          }
+          ++nstore;
+        }
+      } else if constexpr (EPI == EPI_RELU2) {
+        // 64 bf16 columns per chunk
 #pragma unroll 1
         for (int c = 0; c < BN; c += 64) {
+          const uint32_t buf = buf0 + (nstore & 1) * C::EP_BUF;
           float v0[32], v1[32];
           tmem_ld32(taddr + c, v0);
           tmem_ld32(taddr + c + 32, v1);
+          uint32_t w[32];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float a0 = fmaxf(v0[2 * j], 0.f), a1 = fmaxf(v0[2 * j + 1], 0.f);
             const float b0 = fmaxf(v1[2 * j], 0.f), b1 = fmaxf(v1[2 * j + 1], 0.f);
-            st[lane * 33 + j] = pack_bf16x2(a0 * a0, a1 * a1);
-            st[lane * 33 + 16 + j] = pack_bf16x2(b0 * b0, b1 * b1);
+            w[j] = pack_bf16x2(a0 * a0, a1 * a1);
+            w[16 + j] = pack_bf16x2(b0 * b0, b1 * b1);
           }
+          if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
-#pragma unroll 4
-          for (int r = 0; r < 32; ++r) {
-            const int m = row0 + r;
-            if (m < args.M)
-              reinterpret_cast<uint32_t*>(args.out_bf16 + (size_t)m * args.ldo + n0 + c)[lane] =
-                  st[r * 33 + lane];
-          }
-          __syncwarp();
-        }
-      } else if constexpr (EPI == EPI_LOGITS || EPI == EPI_STORE) {
-        float* stf = reinterpret_cast<float*>(st);
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float v[32];
-          tmem_ld32(taddr + c, v);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            stf[lane * 33 + j] = (EPI == EPI_LOGITS) ? softcap_f(v[j], args.softcap) : v[j];
+          for (int cc = 0; cc < 8; ++cc)
+            st_shared_v4u(ep_addr(buf, lane, cc), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
+          fence_async_smem();
           __syncwarp();
-#pragma unroll 4
-          for (int r = 0; r < 32; ++r) {
-            const int m = row0 + r;
-            if (m < args.M) args.out_f32[(size_t)m * args.ldo + n0 + c + lane] = stf[r * 33 + lane];
+          if (lane == 0) {
+            tma_store_2d(&tmC, buf, n0 + c, row0);
+            bulk_commit();
           }
-          __syncwarp();
+          ++nstore;
         }
       } else if constexpr (EPI == EPI_RESID) {
-        float* stf = reinterpret_cast<float*>(st);
+        // x chunk (32 rows x 32 fp32) TMA-loaded into the staging buffer,
+        // acc added, stored back.  The load of chunk c+1 is issued before the
+        // math of chunk c.
+        auto issue_load = [&](int c) {
+          const uint32_t buf = buf0 + (nload & 1) * C::EP_BUF;
+          if (lane == 0) {
+            bulk_wait_read<0>();                    // no store still reads this buffer
+            mbar_arrive_expect_tx(eload0 + 8 * (nload & 1), C::EP_BUF);
+            tma_load_2d(buf, &tmC, eload0 + 8 * (nload & 1), n0 + c, row0);
+          }
+          ++nload;
+        };
+        issue_load(0);
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
+          const uint32_t li = nload - 1;            // index of the load of chunk c
+          if (c + 32 < BN) issue_load(c + 32);
+          const uint32_t buf = buf0 + (li & 1) * C::EP_BUF;
           float v[32];
-#pragma unroll 8
-          for (int r = 0; r < 32; ++r) {
-            const int m = row0 + r;
-            stf[r * 33 + lane] = (m < args.M) ? args.x[(size_t)m * args.ldo + n0 + c + lane] : 0.f;
-          }
           tmem_ld32(taddr + c, v);
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) stf[lane * 33 + j] += v[j];
-          __syncwarp();
-#pragma unroll 8
-          for (int r = 0; r < 32; ++r) {
-            const int m = row0 + r;
-            if (m < args.M) args.x[(size_t)m * args.ldo + n0 + c + lane] = stf[r * 33 + lane];
+          if (!mbar_wait(eload0 + 8 * (li & 1), (li >> 1) & 1, limit)) {
+            fail();
+            ok = false;
+            break;
           }
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            const uint32_t a = ep_addr(buf, lane, cc);
+            const float4 x = ld_shared_v4(a);
+            st_shared_v4(a, x.x + v[4 * cc], x.y + v[4 * cc + 1], x.z + v[4 * cc + 2], x.w + v[4 * cc + 3]);
+          }
+          fence_async_smem();
           __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, buf, n0 + c, row0);
+            bulk_commit();
+          }
         }
       } else if constexpr (EPI == EPI_QKV) {
         // BN covers BN/128 whole heads (head_dim 128).  Columns [0, n_head*128)
-        // are query heads, then the key head, then the value head.
+        // are query heads, then the key head, then the value head.  The two
+        // halves of a head (dims 0..63, 64..127) go to the two staging buffers.
         const int b = my_row / args.T;
         const int pos = args.pos0 + (my_row - b * args.T);
         const int pos_c = pos < args.cache_S ? pos : args.cache_S - 1;   // rows >= M only
+        const uint32_t bufA = buf0, bufB = buf0 + C::EP_BUF;
 #pragma unroll 1
         for (int hh = 0; hh < BN / 128; ++hh) {
           const int head = (n0 >> 7) + hh;
@@ -307,6 +348,8 @@ __global__ void __launch_bounds__(192, 1)
             }
             scale = rsqrtf(ss * (1.f / 128.f) + args.eps);
           }
+          if (lane == 0) bulk_wait_read<0>();       // both buffers free
+          __syncwarp();
 #pragma unroll 1
           for (int c = 0; c < 64; c += 32) {
             float a[32], bb[32];
@@ -318,46 +361,62 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
               for (int j4 = 0; j4 < 8; ++j4) {
                 const float4 cs = __ldg(cp + j4), sn = __ldg(sp + j4);
-                const float cc[4] = {cs.x, cs.y, cs.z, cs.w}, ssn[4] = {sn.x, sn.y, sn.z, sn.w};
+                const float cc4[4] = {cs.x, cs.y, cs.z, cs.w}, sn4[4] = {sn.x, sn.y, sn.z, sn.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                   const int j = 4 * j4 + e;
                   const float x0 = a[j] * scale, x1 = bb[j] * scale;
-                  a[j] = x0 * cc[e] - x1 * ssn[e];
-                  bb[j] = x0 * ssn[e] + x1 * cc[e];
+                  a[j] = x0 * cc4[e] - x1 * sn4[e];
+                  bb[j] = x0 * sn4[e] + x1 * cc4[e];
                 }
               }
             }
+            // columns c..c+31 of each half = 16-byte chunks c/8 .. c/8+3
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              st[lane * 65 + (c >> 1) + j] = pack_bf16x2(a[2 * j], a[2 * j + 1]);
-              st[lane * 65 + 32 + (c >> 1) + j] = pack_bf16x2(bb[2 * j], bb[2 * j + 1]);
+            for (int k = 0; k < 4; ++k) {
+              const int cc = (c >> 3) + k;
+              st_shared_v4u(ep_addr(bufA, lane, cc), pack_bf16x2(a[8 * k], a[8 * k + 1]),
+                            pack_bf16x2(a[8 * k + 2], a[8 * k + 3]), pack_bf16x2(a[8 * k + 4], a[8 * k + 5]),
+                            pack_bf16x2(a[8 * k + 6], a[8 * k + 7]));
+              st_shared_v4u(ep_addr(bufB, lane, cc), pack_bf16x2(bb[8 * k], bb[8 * k + 1]),
+                            pack_bf16x2(bb[8 * k + 2], bb[8 * k + 3]), pack_bf16x2(bb[8 * k + 4], bb[8 * k + 5]),
+                            pack_bf16x2(bb[8 * k + 6], bb[8 * k + 7]));
             }
           }
-          __syncwarp();
-#pragma unroll 2
-          for (int r = 0; r < 32; ++r) {
-            const int m = row0 + r;
-            if (m < args.M) {
-              __nv_bfloat16* dst;
-              if (head < args.n_head) {
-                dst = args.q_out + (size_t)m * (args.n_head * 128) + head * 128;
-              } else {
+          if (head < args.n_head) {
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, bufA, head * 128, row0);
+              tma_store_2d(&tmC, bufB, head * 128 + 64, row0);
+              bulk_commit();
+            }
+          } else {
+            // key / value rows go to the cache row (b, pos): 256 B per row,
+            // lane l writes 32-bit words l and l + 32
+            __syncwarp();
+#pragma unroll 4
+            for (int r = 0; r < 32; ++r) {
+              const int m = row0 + r;
+              if (m < args.M) {
                 const int rb = m / args.T;
                 const int rp = args.pos0 + (m - rb * args.T);
-                dst = (is_v ? args.v_cache : args.k_cache) + ((size_t)rb * args.cache_S + rp) * 128;
+                uint32_t* dst = reinterpret_cast<uint32_t*>(
+                    (is_v ? args.v_cache : args.k_cache) + ((size_t)rb * args.cache_S + rp) * 128);
+                const uint32_t off = ((lane >> 2) ^ (r & 7)) * 16 + (lane & 3) * 4;
+                dst[lane] = ld_shared_u32(bufA + r * 128 + off);
+                dst[lane + 32] = ld_shared_u32(bufB + r * 128 + off);
               }
-              uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
-              d32[lane] = st[r * 65 + lane];
-              d32[lane + 32] = st[r * 65 + 32 + lane];
             }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       tc_fence_before();
       mbar_arrive(bar(TEMPTY + acc));
     }
+    if (lane == 0) bulk_wait_all();                 // stores done before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();

@@ -22,6 +22,7 @@
 #include <new>
 #include <vector>
 
+#include "k_attn_mma.cuh"
 #include "k_attn_simt.cuh"
 #include "k_gemm_tc.cuh"
 #include "k_rowops.cuh"
@@ -33,6 +34,8 @@ namespace {
 
 constexpr int64_t kGuardElems = 2048;       // sentinel guard before and after each cache
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+// log2(e) / sqrt(128): attention scale folded into the exp2 of the softmax
+constexpr float kAttnScaleLog2 = 1.4426950408889634f * 0.08838834764831845f;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -48,17 +51,21 @@ bool load_encode() {
   return true;
 }
 
-// 2-D bf16 tensor map over a row-major [rows][cols] matrix, box = 64 columns
-// (128 bytes, one swizzle row) x box_rows rows, 128-byte swizzle, zero fill.
-bool make_tmap(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D tensor map over a row-major [rows][cols] matrix of bf16 or fp32, box =
+// box_cols x box_rows with box_cols * elem = 128 bytes (one swizzle row),
+// 128-byte swizzle, zero fill out of bounds.
+bool make_tmap(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+               bool f32 = false) {
   if (!load_encode()) return false;
-  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (cols * 2) % 16) return false;
+  const uint64_t eb = f32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (cols * eb) % 16) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint64_t strides[1] = {cols * eb};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / eb), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = g_encode(tm, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -128,7 +135,12 @@ struct nc_model {
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_used = 0;
   std::vector<ProfRec> recs;
+  float* part_o = nullptr;             // decode attention partials [max_batch][chunks][16][128]
+  float* part_ml = nullptr;            // [max_batch][chunks][16][2]
+  int max_chunks = 0;
+  // A-operand maps (box 64 x 128), weight maps (box 64 x 256), epilogue maps (box 128 B x 32)
   CUtensorMap tm_h{}, tm_att{}, tm_u{}, tm_hlast{}, tm_wu{};
+  CUtensorMap tm_q_st{}, tm_x_st{}, tm_u_st{};
   std::vector<CUtensorMap> tm_wqkv, tm_wo, tm_wfc, tm_wproj;
 
   void* kc(int l) const { return static_cast<char*>(k_alloc) + (kGuardElems + l * layer_elems) * wbytes; }
@@ -142,7 +154,7 @@ void free_model(nc_model* m) {
   for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
   void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->k_alloc, m->v_alloc, m->x,
                   m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
-                  m->tok_stage, m->logit_stage, m->err};
+                  m->tok_stage, m->logit_stage, m->err, m->part_o, m->part_ml};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete m;
@@ -189,7 +201,7 @@ nc_status validate(const nc_config* c) {
   if (c->n_kv_head != 1) return NC_ERR_UNSUPPORTED;
   if (c->dtype == NC_BF16) {
     if (c->head_dim != 128 || c->d_model % 256 || c->d_mlp % 256 || c->vocab % 256 ||
-        ((c->n_head + 2) * 128) % 256)
+        ((c->n_head + 2) * 128) % 256 || c->n_head > 16)
       return NC_ERR_UNSUPPORTED;
   } else {
     if ((c->head_dim != 64 && c->head_dim != 128) || c->d_model % 32) return NC_ERR_UNSUPPORTED;
@@ -199,7 +211,7 @@ nc_status validate(const nc_config* c) {
 
 template <int BN, int EPI>
 cudaError_t launch_gemm_tc(nc_model* m, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const GemmArgs& a, cudaStream_t s) {
+                           const CUtensorMap& tc, const GemmArgs& a, cudaStream_t s) {
   using C = TcCfg<BN>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -211,7 +223,7 @@ cudaError_t launch_gemm_tc(nc_model* m, const CUtensorMap& ta, const CUtensorMap
   const int tiles = ((a.M + 127) / 128) * (a.N / BN);
   if (tiles == 0) return cudaSuccess;
   const int grid = tiles < m->num_sms ? tiles : m->num_sms;
-  gemm_tc_kernel<BN, EPI><<<grid, 192, C::SMEM, s>>>(ta, tb, a);
+  gemm_tc_kernel<BN, EPI><<<grid, 192, C::SMEM, s>>>(ta, tb, tc, a);
   m->launches++;
   return cudaGetLastError();
 }
@@ -265,7 +277,6 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       KScope ks(m, NC_K_QKV, s);
       if (bf) {
         GemmArgs a = base_args(m, M, NQKV, d);
-        a.q_out = static_cast<bf16*>(m->q);
         a.k_cache = static_cast<bf16*>(m->kc(l));
         a.v_cache = static_cast<bf16*>(m->vc(l));
         a.rope_cos = m->rope_cos;
@@ -274,7 +285,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
         a.T = T;
         a.pos0 = pos0;
         a.cache_S = c.max_seq;
-        NC_TRY((launch_gemm_tc<256, EPI_QKV>(m, m->tm_h, m->tm_wqkv[l], a, s)));
+        NC_TRY((launch_gemm_tc<256, EPI_QKV>(m, m->tm_h, m->tm_wqkv[l], m->tm_q_st, a, s)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_STORE>(m, static_cast<const float*>(m->h),
                                             static_cast<const float*>(m->wqkv[l]), m->c32, M, NQKV,
@@ -289,26 +300,38 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
     }
     {  // causal MQA attention over the cache
       KScope ks(m, NC_K_ATTN, s);
-      if (bf)
-        attn_simt_kernel<bf16, bf16><<<blocks_for_warps((int64_t)M * nh), 256, 0, s>>>(
+      if (bf && pos0 == 0) {
+        attn_prefill_mma_kernel<<<dim3((T + 31) / 32, nh / 2, B), 128, ATT_PREFILL_SMEM, s>>>(
             static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
-            static_cast<const bf16*>(m->vc(l)), static_cast<bf16*>(m->att), M, nh, hd, T, pos0,
-            c.max_seq);
-      else
+            static_cast<const bf16*>(m->vc(l)), static_cast<bf16*>(m->att), T, nh, c.max_seq, pos0,
+            kAttnScaleLog2);
+        m->launches++;
+        NC_TRY(cudaGetLastError());
+      } else if (bf) {
+        const int ctx = pos0 + 1;                     // decode: T == 1
+        const int nchunk = (ctx + DEC_CHUNK - 1) / DEC_CHUNK;
+        attn_decode_mma_kernel<<<dim3(nchunk, B), 128, ATT_DECODE_SMEM, s>>>(
+            static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
+            static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, nh, c.max_seq, ctx, nchunk,
+            kAttnScaleLog2);
+        attn_decode_combine_kernel<<<dim3(nh, B), 128, 0, s>>>(m->part_o, m->part_ml,
+                                                              static_cast<bf16*>(m->att), nh, nchunk);
+        m->launches += 2;
+        NC_TRY(cudaGetLastError());
+      } else {
         attn_simt_kernel<float, float><<<blocks_for_warps((int64_t)M * nh), 256, 0, s>>>(
             static_cast<const float*>(m->q), static_cast<const float*>(m->kc(l)),
             static_cast<const float*>(m->vc(l)), static_cast<float*>(m->att), M, nh, hd, T, pos0,
             c.max_seq);
-      m->launches++;
-      NC_TRY(cudaGetLastError());
+        m->launches++;
+        NC_TRY(cudaGetLastError());
+      }
     }
     {  // x += att Wo^T
       KScope ks(m, NC_K_OPROJ, s);
       if (bf) {
         GemmArgs a = base_args(m, M, d, NQ);
-        a.x = m->x;
-        a.ldo = d;
-        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_att, m->tm_wo[l], a, s)));
+        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_att, m->tm_wo[l], m->tm_x_st, a, s)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->att),
                                             static_cast<const float*>(m->wo[l]), m->x, M, d, NQ, d, s));
@@ -327,9 +350,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       KScope ks(m, NC_K_FC, s);
       if (bf) {
         GemmArgs a = base_args(m, M, F, d);
-        a.out_bf16 = static_cast<bf16*>(m->u);
-        a.ldo = F;
-        NC_TRY((launch_gemm_tc<256, EPI_RELU2>(m, m->tm_h, m->tm_wfc[l], a, s)));
+        NC_TRY((launch_gemm_tc<256, EPI_RELU2>(m, m->tm_h, m->tm_wfc[l], m->tm_u_st, a, s)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RELU2>(m, static_cast<const float*>(m->h),
                                             static_cast<const float*>(m->wfc[l]),
@@ -340,9 +361,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       KScope ks(m, NC_K_PROJ, s);
       if (bf) {
         GemmArgs a = base_args(m, M, d, F);
-        a.x = m->x;
-        a.ldo = d;
-        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_u, m->tm_wproj[l], a, s)));
+        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_u, m->tm_wproj[l], m->tm_x_st, a, s)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->u),
                                             static_cast<const float*>(m->wproj[l]), m->x, M, d, F, d, s));
@@ -367,9 +386,9 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
     KScope ks(m, NC_K_LMHEAD, s);
     if (bf) {
       GemmArgs a = base_args(m, out_rows, V, d);
-      a.out_f32 = logits;
-      a.ldo = V;
-      NC_TRY((launch_gemm_tc<256, EPI_LOGITS>(m, last_only ? m->tm_hlast : m->tm_h, m->tm_wu, a, s)));
+      CUtensorMap tm_out;
+      if (!make_tmap(&tm_out, logits, out_rows, V, 32, true)) return NC_ERR_INVALID_ARG;
+      NC_TRY((launch_gemm_tc<256, EPI_LOGITS>(m, last_only ? m->tm_hlast : m->tm_h, m->tm_wu, tm_out, a, s)));
     } else {
       NC_TRY(launch_simt_gemm<SEPI_LOGITS>(
           m, static_cast<const float*>(last_only ? m->h_last : m->h),
@@ -542,6 +561,15 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   CREATE_TRY(cudaMalloc(&m->h_last, (int64_t)c.max_batch * d * m->wbytes));
   if (!m->bf16) CREATE_TRY(cudaMalloc(&m->c32, R * NQKV * 4));
   CREATE_TRY(cudaMalloc(&m->tok_stage, R * 4));
+  if (m->bf16) {
+    m->max_chunks = (c.max_seq + DEC_CHUNK - 1) / DEC_CHUNK;
+    CREATE_TRY(cudaMalloc(&m->part_o, (int64_t)c.max_batch * m->max_chunks * 16 * 128 * 4));
+    CREATE_TRY(cudaMalloc(&m->part_ml, (int64_t)c.max_batch * m->max_chunks * 16 * 2 * 4));
+    CREATE_TRY(cudaFuncSetAttribute(attn_prefill_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)ATT_PREFILL_SMEM));
+    CREATE_TRY(cudaFuncSetAttribute(attn_decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)ATT_DECODE_SMEM));
+  }
   CREATE_TRY(cudaMalloc(&m->err, sizeof(int)));
   CREATE_TRY(cudaMemset(m->h, 0, R * d * m->wbytes));
   CREATE_TRY(cudaMemset(m->att, 0, R * NQ * m->wbytes));
@@ -553,7 +581,9 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
     bool ok = make_tmap(&m->tm_h, m->h, R, d, 128) && make_tmap(&m->tm_att, m->att, R, NQ, 128) &&
               make_tmap(&m->tm_u, m->u, R, F, 128) &&
               make_tmap(&m->tm_hlast, m->h_last, c.max_batch, d, 128) &&
-              make_tmap(&m->tm_wu, m->Wu, V, d, 256);
+              make_tmap(&m->tm_wu, m->Wu, V, d, 256) &&
+              make_tmap(&m->tm_q_st, m->q, R, NQ, 32) && make_tmap(&m->tm_u_st, m->u, R, F, 32) &&
+              make_tmap(&m->tm_x_st, m->x, R, d, 32, true);
     m->tm_wqkv.resize(c.n_layer);
     m->tm_wo.resize(c.n_layer);
     m->tm_wfc.resize(c.n_layer);
@@ -656,10 +686,10 @@ nc_status nc_gemm_bf16(nc_model* m, const void* A, const void* W, float* C, int3
   if (!is_device_ptr(A) || !is_device_ptr(W) || !is_device_ptr(C)) return NC_ERR_INVALID_ARG;
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, A, M, K, 128) || !make_tmap(&tb, W, N, K, 256)) return NC_ERR_INVALID_ARG;
+  CUtensorMap tc;
+  if (!make_tmap(&tc, C, M, N, 32, true)) return NC_ERR_INVALID_ARG;
   GemmArgs a = base_args(m, M, N, K);
-  a.out_f32 = C;
-  a.ldo = N;
-  NC_TRY((launch_gemm_tc<256, EPI_STORE>(m, ta, tb, a, stream)));
+  NC_TRY((launch_gemm_tc<256, EPI_STORE>(m, ta, tb, tc, a, stream)));
   return NC_OK;
 }
 
