@@ -313,6 +313,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-decode", action="store_true", help="skip the d12 decode measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (smaller cases for profiling)")
+    ap.add_argument("--seq", type=int, default=None, help="override the workload's prompt length")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
@@ -328,6 +331,10 @@ def main():
 
     peaks, peak_src = load_peaks()
     w = nc_inputs.WORKLOADS[args.config]
+    if args.batch or args.seq:
+        from dataclasses import replace
+        w = replace(w, name=f"{w.name}[batch={args.batch or w.batch},seq={args.seq or w.prompt_len}]",
+                    batch=args.batch or w.batch, prompt_len=args.seq or w.prompt_len)
     flat = nc_inputs.gen_weights(w.shape, w.weight_seed)
     prompt, nxt = _tokens(w)
     line = {"metric": METRIC, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
