@@ -19,6 +19,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -29,6 +30,14 @@
 #include "nc_common.cuh"
 
 using namespace nc;
+
+// Fixed scratch for nc_decode_step_noalloc: the split-context decode
+// attention's partial results, per (batch row, 128-key chunk, head slot of
+// 16) a 128-float output plus (max, sum).  Sized for B * chunks <= 2560
+// (21.3 MB); every GPU that loads this library holds it until exit.
+constexpr int64_t kNoAllocMaxRowChunks = 2560;
+constexpr int64_t kNoAllocFloats = kNoAllocMaxRowChunks * 16 * (128 + 2);
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
 
 namespace {
 
@@ -437,6 +446,26 @@ __global__ void wait_nothing_kernel(int* err, unsigned long long limit_ns) {
   if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, limit_ns)) atomicOr(err, NC_DEVFLAG_TIMEOUT);
 }
 
+// Device address of g_noalloc_scratch for `device` (which must be current).
+// Host code only sees a stand-in for the array's name, so the address is
+// looked up once per device with cudaGetSymbolAddress and cached.
+constexpr int kMaxDevices = 64;
+float* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+nc_status noalloc_scratch(int device, float** out) {
+  if (device < 0 || device >= kMaxDevices) return NC_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[device]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return NC_ERR_CUDA;
+    g_noalloc_ptr[device] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[device];
+  return NC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -452,6 +481,7 @@ const char* nc_status_string(nc_status s) {
     case NC_ERR_TOKEN: return "token id out of range";
     case NC_ERR_TIMEOUT: return "device wait timed out";
     case NC_ERR_CUDA: return "CUDA error";
+    case NC_ERR_SCRATCH_LIMIT: return "batch x context exceeds the fixed no-allocation scratch";
   }
   return "unknown status";
 }
@@ -636,6 +666,35 @@ nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, float* l
   if (B != m->batch) return NC_ERR_INVALID_ARG;
   if (m->length >= m->cfg.max_seq) return NC_ERR_CAPACITY;
   nc_status st = run_call(m, tokens, B, 1, m->length, logits, false, stream);
+  if (st != NC_OK) return st;
+  m->length += 1;
+  return NC_OK;
+}
+
+nc_status nc_decode_step_noalloc(nc_model* m, const int32_t* tokens, int32_t B, float* logits,
+                                 nc_stream_t stream) {
+  if (!m || !tokens || !logits) return NC_ERR_INVALID_ARG;
+  if (!m->bf16) return NC_ERR_UNSUPPORTED;
+  if (m->length == 0) return NC_ERR_STATE;
+  if (B != m->batch) return NC_ERR_INVALID_ARG;
+  if (m->length >= m->cfg.max_seq) return NC_ERR_CAPACITY;
+  if (!is_device_ptr(tokens) || !is_device_ptr(logits)) return NC_ERR_INVALID_ARG;
+  const int64_t nchunk = (m->length + 1 + DEC_CHUNK - 1) / DEC_CHUNK;
+  if ((int64_t)B * nchunk > kNoAllocMaxRowChunks) return NC_ERR_SCRATCH_LIMIT;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != m->device) return NC_ERR_INVALID_ARG;
+  float* scratch = nullptr;
+  nc_status st = noalloc_scratch(dev, &scratch);
+  if (st != NC_OK) return st;
+  // the decode attention reads its partial buffers from the model: point them
+  // at the fixed scratch for this call only
+  float* const keep_o = m->part_o;
+  float* const keep_ml = m->part_ml;
+  m->part_o = scratch;
+  m->part_ml = scratch + (int64_t)B * nchunk * 16 * 128;
+  st = forward(m, tokens, B, 1, m->length, logits, false, stream);
+  m->part_o = keep_o;
+  m->part_ml = keep_ml;
   if (st != NC_OK) return st;
   m->length += 1;
   return NC_OK;

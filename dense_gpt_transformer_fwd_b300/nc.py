@@ -20,7 +20,7 @@ NC_F32, NC_BF16 = 0, 1
 KCLASSES = ("embed", "qkv", "attn", "oproj", "norm", "fc", "proj", "lm_head")
 STATUS = {0: "NC_OK", 1: "NC_ERR_INVALID_ARG", 2: "NC_ERR_UNSUPPORTED", 3: "NC_ERR_OOM",
           4: "NC_ERR_STATE", 5: "NC_ERR_CAPACITY", 6: "NC_ERR_TOKEN", 7: "NC_ERR_TIMEOUT",
-          8: "NC_ERR_CUDA"}
+          8: "NC_ERR_CUDA", 9: "NC_ERR_SCRATCH_LIMIT"}
 
 
 class NcError(RuntimeError):
@@ -63,6 +63,7 @@ def lib() -> ctypes.CDLL:
         "nc_kv_reset": ([P, P], S),
         "nc_prefill": ([P, P, I32, I32, P, I32, P], S),
         "nc_decode_step": ([P, P, I32, P, P], S),
+        "nc_decode_step_noalloc": ([P, P, I32, P, P], S),
         "nc_sync_status": ([P, P], S),
         "nc_kv_length": ([P, ctypes.POINTER(I32), ctypes.POINTER(I32)], S),
         "nc_kv_layout": ([P, ctypes.POINTER(I64), ctypes.POINTER(I64), ctypes.POINTER(I32)], S),
@@ -174,6 +175,14 @@ class Model:
             out = self._out(tokens, B)
         _check(self._L.nc_decode_step(self._h, _ptr(tokens), B, _ptr(out), _stream(stream)),
                "nc_decode_step")
+        return out.view(B, self.cfg.vocab)
+
+    def decode_step_noalloc(self, tokens, out, stream=None):
+        """nc_decode_step_noalloc: device tokens [B] int32 and a caller-owned
+        device logits buffer [B, V] fp32; allocates nothing."""
+        B = tokens.numel()
+        _check(self._L.nc_decode_step_noalloc(self._h, _ptr(tokens), B, _ptr(out), _stream(stream)),
+               "nc_decode_step_noalloc")
         return out.view(B, self.cfg.vocab)
 
     def kv_reset(self, stream=None):
