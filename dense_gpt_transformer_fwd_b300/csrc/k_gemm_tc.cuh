@@ -7,18 +7,19 @@
 // QK norm, ReLU^2, logit softcap; apidog.com/th "train your own ChatGPT",
 // "how nanochat works" item 3: F.linear with the weight in the compute dtype).
 //
-// Roles inside one CTA (192 threads, one CTA per SM):
+// Roles inside one CTA (320 threads, one CTA per SM):
 //   warp 0        TMA producer: A and W tiles (128 B swizzle) into a ring of
 //                 STAGES shared-memory slots, completion on mbarriers
 //   warp 1        TMEM owner + MMA issuer: tcgen05.mma kind::f16, M = 128,
 //                 N = BN, K = 16 per instruction; two TMEM accumulators so the
 //                 epilogue of tile i overlaps the main loop of tile i + 1
-//   warps 2..5    epilogue: tcgen05.ld (each warp owns 32 TMEM lanes = 32
-//                 rows), fused math, then 32-row x 128-byte chunks staged in
-//                 a swizzled shared buffer and written by TMA bulk tensor
-//                 stores (two buffers per warp, so math overlaps the store);
-//                 the residual epilogue TMA-loads the fp32 residual chunk
-//                 into the same buffer, adds, and stores it back.
+//   warps 2..9    epilogue, two warps per TMEM lane quarter (a warp may only
+//                 read the 32 TMEM lanes of its quarter, warp % 4), each
+//                 owning half of the tile's columns: tcgen05.ld, fused math,
+//                 then 32-row x 128-byte chunks staged in a swizzled shared
+//                 buffer and written by TMA bulk tensor stores.  The residual
+//                 epilogue uses the TMA reduce-add store, so x += acc happens
+//                 in L2 without reading x into the SM.
 // Tiles are visited m-fastest so that CTAs resident at the same time share
 // the W tile (and the whole A panel stays in L2).
 #pragma once
@@ -52,16 +53,25 @@ struct GemmArgs {
   unsigned long long wait_limit_ns;
 };
 
-template <int BN>
+template <int BN, int EPI>
 struct TcCfg {
   static constexpr int BM = 128, BK = 64;
-  static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  // the QKV epilogue stages both halves of a head (RoPE pairs dims j, j+64)
+  static constexpr int EP_BUFS = EPI == EPI_QKV ? 2 : 1;
+  static constexpr uint32_t EP_BUF = 4096;             // 32 rows x 128 B
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr size_t EP_TOTAL = (size_t)EPI_WARPS * EP_BUFS * EP_BUF;
+  static constexpr size_t SMEM_CAP = 232448 - 1024 - 256;
+  static constexpr int STAGES_FIT = (int)((SMEM_CAP - EP_TOTAL) / STAGE_BYTES);
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr uint32_t EP_BUF = 4096;             // 32 rows x 128 B
-  static constexpr size_t SMEM = 1024 + STAGES * (size_t)STAGE_BYTES + 4 * 2 * EP_BUF + 256;
+  static constexpr size_t SMEM = 1024 + STAGES * (size_t)STAGE_BYTES + EP_TOTAL + 256;
+  static_assert(STAGES >= 2, "shared memory too small for the pipeline");
+  static_assert(SMEM <= 232448, "shared memory over the sm_103a per-block limit");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -69,11 +79,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&t);
 }
 
-// softcap without a libm call: cap * tanh(y), tanh(y) = 1 - 2 / (exp(2y) + 1);
-// saturates correctly to +-cap when exp overflows to inf or underflows to 0.
-__device__ __forceinline__ float softcap_f(float z, float cap) {
-  const float e = __expf(2.0f * z / cap);
-  return cap * (1.0f - __fdividef(2.0f, e + 1.0f));
+// softcap = cap * tanh(z / cap) with the single-instruction hardware tanh
+// (PTX tanh.approx.f32, one MUFU op; relative error about 2^-11, i.e. at
+// most ~7e-3 absolute at the cap of 15).  Saturates to +-cap for large |z|.
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float softcap_f(float z, float inv_cap, float cap) {
+  return cap * tanh_approx(z * inv_cap);
 }
 
 // Address of 16-byte chunk `cc` (0..7) of row `r` in a 32 x 128 B staging
@@ -82,20 +97,29 @@ __device__ __forceinline__ uint32_t ep_addr(uint32_t buf, int r, int cc) {
   return buf + r * 128 + ((cc ^ (r & 7)) << 4);
 }
 
+// shared -> global tensor reduce-add (x += staged tile, performed in L2)
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, uint32_t src, int c0, int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 template <int BN, int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, EPI>;
   constexpr int BM = C::BM, BK = C::BK, STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * C::A_BYTES;
-  uint8_t* sE = sB + STAGES * C::B_BYTES;                       // 4 warps x 2 staging buffers
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 4 * 2 * C::EP_BUF);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, eload[8]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 13);
+  uint8_t* sE = sB + STAGES * C::B_BYTES;                       // epilogue staging buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + C::EP_TOTAL);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -107,7 +131,7 @@ __global__ void __launch_bounds__(192, 1)
 
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, TEMPTY = 2 * STAGES + 2,
-            DRAIN = 2 * STAGES + 4, ELOAD = 2 * STAGES + 5;
+            DRAIN = 2 * STAGES + 4;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -116,10 +140,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar(TFULL + a), 1);
-      mbar_init(bar(TEMPTY + a), 128);
+      mbar_init(bar(TEMPTY + a), 32 * C::EPI_WARPS);
     }
     mbar_init(bar(DRAIN), 1);
-    for (int i = 0; i < 8; ++i) mbar_init(bar(ELOAD + i), 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -211,15 +234,14 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    const int e = warp - 2;                         // 0..7
     const int q = warp & 3;                         // TMEM lane quarter of this warp
-    const int ew = warp - 2;                        // staging slot of this warp
-    const uint32_t buf0 = smem_u32(sE + ew * 2 * C::EP_BUF);
-    const uint32_t eload0 = bar(ELOAD + 2 * ew);
-    uint32_t nload = 0;                             // residual chunk loads issued so far
-    int nstore = 0;                                 // staging buffers used so far
+    constexpr int HALF = BN / 2;                    // columns owned by this warp
+    const int ch0 = (e >> 2) * HALF;                // first owned column in the tile
+    const uint32_t buf0 = smem_u32(sE + e * C::EP_BUFS * C::EP_BUF);
+    const float inv_cap = 1.0f / args.softcap;
     int local = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
       const int acc = local & 1;
       if (*abort_flag || !mbar_wait(bar(TFULL + acc), (local >> 1) & 1, limit)) {
         if (!*abort_flag) fail();
@@ -229,37 +251,37 @@ __global__ void __launch_bounds__(192, 1)
       const int m0 = (tile % num_m) * BM, n0 = (tile / num_m) * BN;
       const int row0 = m0 + 32 * q;                 // first row of this warp
       const int my_row = row0 + lane;
-      const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc * BN;
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc * BN + ch0;
 
-      if constexpr (EPI == EPI_LOGITS || EPI == EPI_STORE) {
+      if constexpr (EPI == EPI_LOGITS || EPI == EPI_STORE || EPI == EPI_RESID) {
         // 32 fp32 columns per chunk
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          const uint32_t buf = buf0 + (nstore & 1) * C::EP_BUF;
+        for (int c = 0; c < HALF; c += 32) {
           float v[32];
           tmem_ld32(taddr + c, v);
-          if (EPI == EPI_LOGITS) {
+          if constexpr (EPI == EPI_LOGITS) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = softcap_f(v[j], args.softcap);
+            for (int j = 0; j < 32; ++j) v[j] = softcap_f(v[j], inv_cap, args.softcap);
           }
-          if (lane == 0) bulk_wait_read<1>();       // this buffer's previous store has read it
+          if (lane == 0) bulk_wait_read<0>();       // the previous store has read the buffer
           __syncwarp();
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc)
-            st_shared_v4(ep_addr(buf, lane, cc), v[4 * cc], v[4 * cc + 1], v[4 * cc + 2], v[4 * cc + 3]);
+            st_shared_v4(ep_addr(buf0, lane, cc), v[4 * cc], v[4 * cc + 1], v[4 * cc + 2], v[4 * cc + 3]);
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmC, buf, n0 + c, row0);
+            if constexpr (EPI == EPI_RESID)
+              tma_reduce_add_2d(&tmC, buf0, n0 + ch0 + c, row0);
+            else
+              tma_store_2d(&tmC, buf0, n0 + ch0 + c, row0);
             bulk_commit();
           }
-          ++nstore;
         }
       } else if constexpr (EPI == EPI_RELU2) {
         // 64 bf16 columns per chunk
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 64) {
-          const uint32_t buf = buf0 + (nstore & 1) * C::EP_BUF;
+        for (int c = 0; c < HALF; c += 64) {
           float v0[32], v1[32];
           tmem_ld32(taddr + c, v0);
           tmem_ld32(taddr + c + 32, v1);
@@ -271,69 +293,30 @@ __global__ void __launch_bounds__(192, 1)
             w[j] = pack_bf16x2(a0 * a0, a1 * a1);
             w[16 + j] = pack_bf16x2(b0 * b0, b1 * b1);
           }
-          if (lane == 0) bulk_wait_read<1>();
+          if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc)
-            st_shared_v4u(ep_addr(buf, lane, cc), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
+            st_shared_v4u(ep_addr(buf0, lane, cc), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmC, buf, n0 + c, row0);
-            bulk_commit();
-          }
-          ++nstore;
-        }
-      } else if constexpr (EPI == EPI_RESID) {
-        // x chunk (32 rows x 32 fp32) TMA-loaded into the staging buffer,
-        // acc added, stored back.  The load of chunk c+1 is issued before the
-        // math of chunk c.
-        auto issue_load = [&](int c) {
-          const uint32_t buf = buf0 + (nload & 1) * C::EP_BUF;
-          if (lane == 0) {
-            bulk_wait_read<0>();                    // no store still reads this buffer
-            mbar_arrive_expect_tx(eload0 + 8 * (nload & 1), C::EP_BUF);
-            tma_load_2d(buf, &tmC, eload0 + 8 * (nload & 1), n0 + c, row0);
-          }
-          ++nload;
-        };
-        issue_load(0);
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          const uint32_t li = nload - 1;            // index of the load of chunk c
-          if (c + 32 < BN) issue_load(c + 32);
-          const uint32_t buf = buf0 + (li & 1) * C::EP_BUF;
-          float v[32];
-          tmem_ld32(taddr + c, v);
-          if (!mbar_wait(eload0 + 8 * (li & 1), (li >> 1) & 1, limit)) {
-            fail();
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            const uint32_t a = ep_addr(buf, lane, cc);
-            const float4 x = ld_shared_v4(a);
-            st_shared_v4(a, x.x + v[4 * cc], x.y + v[4 * cc + 1], x.z + v[4 * cc + 2], x.w + v[4 * cc + 3]);
-          }
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmC, buf, n0 + c, row0);
+            tma_store_2d(&tmC, buf0, n0 + ch0 + c, row0);
             bulk_commit();
           }
         }
       } else if constexpr (EPI == EPI_QKV) {
-        // BN covers BN/128 whole heads (head_dim 128).  Columns [0, n_head*128)
-        // are query heads, then the key head, then the value head.  The two
-        // halves of a head (dims 0..63, 64..127) go to the two staging buffers.
+        // BN covers BN/128 whole heads (head_dim 128); each warp owns HALF/128
+        // heads.  Columns [0, n_head*128) are query heads, then the key head,
+        // then the value head.  The two halves of a head (dims 0..63, 64..127)
+        // go to the warp's two staging buffers.
         const int b = my_row / args.T;
         const int pos = args.pos0 + (my_row - b * args.T);
         const int pos_c = pos < args.cache_S ? pos : args.cache_S - 1;   // rows >= M only
         const uint32_t bufA = buf0, bufB = buf0 + C::EP_BUF;
 #pragma unroll 1
-        for (int hh = 0; hh < BN / 128; ++hh) {
-          const int head = (n0 >> 7) + hh;
+        for (int hh = 0; hh < HALF / 128; ++hh) {
+          const int head = ((n0 + ch0) >> 7) + hh;
           const bool is_v = head == args.n_head + 1;
           const uint32_t hbase = taddr + hh * 128;
           float scale = 1.f;
@@ -363,11 +346,11 @@ __global__ void __launch_bounds__(192, 1)
                 const float4 cs = __ldg(cp + j4), sn = __ldg(sp + j4);
                 const float cc4[4] = {cs.x, cs.y, cs.z, cs.w}, sn4[4] = {sn.x, sn.y, sn.z, sn.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int j = 4 * j4 + e;
+                for (int k = 0; k < 4; ++k) {
+                  const int j = 4 * j4 + k;
                   const float x0 = a[j] * scale, x1 = bb[j] * scale;
-                  a[j] = x0 * cc4[e] - x1 * sn4[e];
-                  bb[j] = x0 * sn4[e] + x1 * cc4[e];
+                  a[j] = x0 * cc4[k] - x1 * sn4[k];
+                  bb[j] = x0 * sn4[k] + x1 * cc4[k];
                 }
               }
             }

@@ -221,7 +221,7 @@ nc_status validate(const nc_config* c) {
 template <int BN, int EPI>
 cudaError_t launch_gemm_tc(nc_model* m, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const GemmArgs& a, cudaStream_t s) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, EPI>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
@@ -232,7 +232,7 @@ cudaError_t launch_gemm_tc(nc_model* m, const CUtensorMap& ta, const CUtensorMap
   const int tiles = ((a.M + 127) / 128) * (a.N / BN);
   if (tiles == 0) return cudaSuccess;
   const int grid = tiles < m->num_sms ? tiles : m->num_sms;
-  gemm_tc_kernel<BN, EPI><<<grid, 192, C::SMEM, s>>>(ta, tb, tc, a);
+  gemm_tc_kernel<BN, EPI><<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tc, a);
   m->launches++;
   return cudaGetLastError();
 }
