@@ -1,15 +1,10 @@
-// Causal multi-query attention on the tensor cores (bf16 in, fp32 accumulate),
-// flash-style: scores, online softmax and the P.V product stay on chip.
+// Causal multi-query attention for the decode step on the tensor cores (bf16
+// in, fp32 accumulate, mma.sync): scores, softmax and P.V stay on chip.
 //
 // Multi-query attention: every query head reads the single K/V head
 // (yelogs.com nanochat story, "technical details and official Q&A"); scale
 // 1/sqrt(head_dim) as in SDPA (apidog.com/th "train your own ChatGPT", "how
 // nanochat works" item 5).
-//
-// Prefill kernel: one CTA = 32 query positions x 2 query heads = 64 rows
-// (4 warps x 16 rows); both heads share every K/V tile loaded into shared
-// memory.  K/V tiles of 64 keys are double-buffered with cp.async; the
-// diagonal tile is masked.  Heavier (later) query blocks are scheduled first.
 //
 // Decode kernel (split over the context): one CTA = one batch row and a
 // chunk of 128 cached keys; the row's n_head query vectors form the 16-row
@@ -57,172 +52,6 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
 }
 
 constexpr int ATT_HD = 128;
-
-// Q, O: [B*T][n_head*128] rows m = b*T + t at position pos0 + t; K/V caches
-// [B_max][cache_S][128], keys 0 .. pos0+T-1 valid.
-__global__ void __launch_bounds__(128) attn_prefill_mma_kernel(
-    const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kc,
-    const __nv_bfloat16* __restrict__ Vc, __nv_bfloat16* __restrict__ O, int T, int n_head,
-    int cache_S, int pos0, float scale_log2) {
-  constexpr int BQ = 32, ROWS = 64, BKV = 64;
-  extern __shared__ __align__(128) uint8_t att_smem[];
-  const uint32_t sQ = smem_u32(att_smem);
-  const uint32_t sK0 = sQ + ROWS * 256;                       // 2 stages of K, then 2 of V
-  const uint32_t sV0 = sK0 + 2 * BKV * 256;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qb = gridDim.x - 1 - blockIdx.x;                  // heavy blocks first
-  const int hp = blockIdx.y, b = blockIdx.z;
-  const int q0 = qb * BQ;
-  const int kv_len = pos0 + T;
-  const int ldq = n_head * ATT_HD;
-  const __nv_bfloat16* kbase = Kc + (size_t)b * cache_S * ATT_HD;
-  const __nv_bfloat16* vbase = Vc + (size_t)b * cache_S * ATT_HD;
-
-  // ---- Q tile: row r -> position q0 + r/2, head 2*hp + (r&1)
-  for (int i = tid; i < ROWS * 16; i += 128) {
-    const int r = i >> 4, c = i & 15;
-    const int t = q0 + (r >> 1);
-    const bool ok = t < T;
-    const __nv_bfloat16* src = Q + ((size_t)b * T + (ok ? t : 0)) * ldq + (2 * hp + (r & 1)) * ATT_HD + c * 8;
-    cp_async16(swz(sQ, r, c), src, ok);
-  }
-  const int last_key = min(pos0 + q0 + BQ - 1, kv_len - 1);   // largest key any row needs
-  const int n_blocks = last_key / BKV + 1;
-  auto load_kv = [&](int blk, int stage) {
-    const uint32_t sk = sK0 + stage * BKV * 256, sv = sV0 + stage * BKV * 256;
-    for (int i = tid; i < BKV * 16; i += 128) {
-      const int r = i >> 4, c = i & 15;
-      const int key = blk * BKV + r;
-      const bool ok = key < kv_len;
-      const size_t off = (size_t)(ok ? key : 0) * ATT_HD + c * 8;
-      cp_async16(swz(sk, r, c), kbase + off, ok);
-      cp_async16(swz(sv, r, c), vbase + off, ok);
-    }
-  };
-  load_kv(0, 0);
-  cp_async_commit();
-
-  // per-thread rows within the warp's 16: lane/4 and lane/4 + 8
-  const int r_lo = warp * 16 + (lane >> 2), r_hi = r_lo + 8;
-  const int qpos_lo = pos0 + q0 + (r_lo >> 1), qpos_hi = pos0 + q0 + (r_hi >> 1);
-  float o[16][4];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
-  uint32_t qf[8][4];
-
-  for (int blk = 0; blk < n_blocks; ++blk) {
-    const int stage = blk & 1;
-    if (blk + 1 < n_blocks) load_kv(blk + 1, stage ^ 1);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    if (blk == 0) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int chunk = kk * 2 + (lane >> 4);
-        ldsm_x4(swz(sQ, row, chunk), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-      }
-    }
-    const uint32_t sk = sK0 + stage * BKV * 256, sv = sV0 + stage * BKV * 256;
-    // ---- S = Q K^T  (16 x 64 per warp)
-    float s[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int jp = 0; jp < 4; ++jp) {            // pairs of 8-key tiles
-        const int key = jp * 16 + (lane & 7) + (lane >> 4) * 8;
-        const int chunk = kk * 2 + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(swz(sk, key, chunk), b0, b1, b2, b3);
-        mma_bf16(s[2 * jp], qf[kk], b0, b1);
-        mma_bf16(s[2 * jp + 1], qf[kk], b2, b3);
-      }
-    }
-    // ---- mask (keys beyond the row's position) and online softmax
-    const int kbase_idx = blk * BKV;
-    const bool diag = kbase_idx + BKV - 1 > pos0 + q0;
-    float mx_lo = m_lo, mx_hi = m_hi;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = kbase_idx + j * 8 + (lane & 3) * 2 + e;
-        float a = s[j][e] * scale_log2, c = s[j][2 + e] * scale_log2;
-        if (diag) {
-          if (key > qpos_lo) a = -INFINITY;
-          if (key > qpos_hi) c = -INFINITY;
-        }
-        s[j][e] = a;
-        s[j][2 + e] = c;
-        mx_lo = fmaxf(mx_lo, a);
-        mx_hi = fmaxf(mx_hi, c);
-      }
-    }
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-    const float corr_lo = exp2f(m_lo - mx_lo), corr_hi = exp2f(m_hi - mx_hi);
-    m_lo = mx_lo;
-    m_hi = mx_hi;
-    float sum_lo = 0.f, sum_hi = 0.f;
-    uint32_t pf[4][4];                              // P as A fragments, 4 k-steps of 16 keys
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float p0 = exp2f(s[j][0] - mx_lo), p1 = exp2f(s[j][1] - mx_lo);
-      const float p2 = exp2f(s[j][2] - mx_hi), p3 = exp2f(s[j][3] - mx_hi);
-      sum_lo += p0 + p1;
-      sum_hi += p2 + p3;
-      pf[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
-      pf[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
-    }
-    l_lo = l_lo * corr_lo + sum_lo;
-    l_hi = l_hi * corr_hi + sum_hi;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      o[j][0] *= corr_lo;
-      o[j][1] *= corr_lo;
-      o[j][2] *= corr_hi;
-      o[j][3] *= corr_hi;
-    }
-    // ---- O += P V  (16 x 128 per warp)
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-      for (int jp = 0; jp < 8; ++jp) {            // pairs of 8-dim tiles
-        const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int chunk = jp * 2 + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(swz(sv, key, chunk), b0, b1, b2, b3);
-        mma_bf16(o[2 * jp], pf[kk], b0, b1);
-        mma_bf16(o[2 * jp + 1], pf[kk], b2, b3);
-      }
-    }
-    __syncthreads();
-  }
-
-  // ---- normalise and store
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  const float inv_lo = 1.f / l_lo, inv_hi = 1.f / l_hi;
-  const int t_lo = q0 + (r_lo >> 1), t_hi = q0 + (r_hi >> 1);
-  __nv_bfloat16* o_lo = O + ((size_t)b * T + t_lo) * ldq + (2 * hp + (r_lo & 1)) * ATT_HD;
-  __nv_bfloat16* o_hi = O + ((size_t)b * T + t_hi) * ldq + (2 * hp + (r_hi & 1)) * ATT_HD;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int col = j * 8 + (lane & 3) * 2;
-    if (t_lo < T) *reinterpret_cast<uint32_t*>(o_lo + col) = pack_bf16(o[j][0] * inv_lo, o[j][1] * inv_lo);
-    if (t_hi < T) *reinterpret_cast<uint32_t*>(o_hi + col) = pack_bf16(o[j][2] * inv_hi, o[j][3] * inv_hi);
-  }
-}
-
-constexpr size_t ATT_PREFILL_SMEM = (64 + 4 * 64) * 256;     // Q + 2 x (K, V) = 80 KB
 
 // ---------------------------------------------------------------- decode --
 // Q: [B][n_head*128] (one new position per row, at pos = ctx-1); keys 0..ctx-1.

@@ -1,0 +1,361 @@
+// Causal multi-query attention for the prefill on the 5th-generation tensor
+// cores (sm_103a): flash-style, scores S and output O accumulate in TMEM,
+// operands are fed by TMA, the online softmax runs one thread per row.
+//
+// Multi-query attention: every query head reads the single K/V head
+// (yelogs.com nanochat story, "technical details and official Q&A"); scale
+// 1/sqrt(head_dim) as in SDPA (apidog.com/th "train your own ChatGPT", "how
+// nanochat works" item 5); query t attends to keys 0..t.
+//
+// One CTA = one batch row, one tile of 128 query positions and TWO query
+// heads (tiles "A" and "B"), which share every K and V tile it loads.  Per
+// 128-key block j:
+//   S_t   = Q_t K_j^T          tcgen05.mma M=128 N=128 K=128   (TMEM, fp32)
+//   P_t   = exp2(S_t * c - m)  softmax threads, bf16, into shared memory
+//   O_t  += P_t V_j            tcgen05.mma M=128 N=128 K=128   (TMEM, fp32)
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// The running max m is only raised when a block's max exceeds it by more
+// than 2^8 (in the exp2 domain); O and the running sum are then rescaled by
+// the same thread (it owns that TMEM lane).  The final O / l is exact either
+// way, since numerator and denominator share the reference m.
+//
+// Operands (all K-major bf16 tiles with the 128-byte swizzle, boxes of 64
+// columns x 128 rows): Q from the query buffer viewed as [B][T][n_head*128];
+// K from this layer's cache [B_max][S][128]; V from a transposed copy
+// V^T [B_max][128][S_vt] that the QKV epilogue writes during the prefill, so
+// that P V is again an A * B^T product with B = V^T.  O is staged in the P
+// buffer and written by a TMA store into the attention output
+// [B][T][n_head*128]; the tensor maps clip rows t >= T.
+//
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA
+// issuer, warps 2..5 softmax of tile A, warps 6..9 softmax of tile B (warp w
+// reads TMEM lanes 32*(w%4) .. +31, i.e. rows of its quarter).
+// Every mbarrier wait is bounded; on expiry the kernel records
+// NC_DEVFLAG_TIMEOUT, lets its copies and MMAs drain, frees TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+#include "nc_common.cuh"
+
+namespace nc {
+
+struct AttnTcArgs {
+  int B, T, n_head, n_qt;          // n_qt = ceil(T / 128)
+  float scale_log2;                // log2(e) / sqrt(head_dim)
+  int* err;
+  unsigned long long wait_limit_ns;
+};
+
+constexpr int ATC_THREADS = 320;
+constexpr uint32_t ATC_HALF = 16384;                 // 128 rows x 128 B
+constexpr uint32_t ATC_TILE = 2 * ATC_HALF;          // 128 rows x 128 bf16
+constexpr uint32_t ATC_OFF_Q = 0;                    // 2 tiles
+constexpr uint32_t ATC_OFF_K = 2 * ATC_TILE;         // 2 stages
+constexpr uint32_t ATC_OFF_V = 4 * ATC_TILE;         // 1 stage
+constexpr uint32_t ATC_OFF_P = 5 * ATC_TILE;         // 2 tiles
+constexpr uint32_t ATC_OFF_BAR = 7 * ATC_TILE;
+constexpr size_t ATC_SMEM = 1024 + 7 * (size_t)ATC_TILE + 256;
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int c0,
+                                            int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// 32 lanes x 32 consecutive fp32 columns, registers -> TMEM
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+      "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+      "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+      "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16_2(float lo, float hi) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+// byte address of bf16 element (row r, column c) of a 128 x 128 tile stored
+// as two K-major 128-byte-swizzled halves (columns 0..63, 64..127)
+__device__ __forceinline__ uint32_t atc_addr(uint32_t tile, int r, int c) {
+  return tile + (c >> 6) * ATC_HALF + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2;
+}
+
+__global__ void __launch_bounds__(ATC_THREADS, 1)
+    attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,   // q   [B][T][NQ]
+                           const __grid_constant__ CUtensorMap tmK,   // K   [B_max][S][128]
+                           const __grid_constant__ CUtensorMap tmVt,  // V^T [B_max][128][S_vt]
+                           const __grid_constant__ CUtensorMap tmO,   // att [B][T][NQ]
+                           const AttnTcArgs args) {
+  extern __shared__ uint8_t atc_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(atc_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s0 = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ATC_OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  // barrier indices
+  const int QFULL = 0, KFULL = 1, KFREE = 3, VFULL = 5, VFREE = 6, SFULL = 7, SFREE = 9,
+            PFULL = 11, PVDONE = 13, DRAIN = 15;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pairs = args.n_head >> 1;
+  // heavy query tiles first: item -> (query tile, batch row, head pair)
+  const int per_qt = args.B * pairs;
+  const int qt = args.n_qt - 1 - (int)(blockIdx.x / per_qt);
+  const int rest = (int)(blockIdx.x % per_qt);
+  const int b = rest / pairs, hp = rest % pairs;
+  const int q0 = qt * 128;
+  const int nb = qt + 1;                             // key blocks 0 .. qt
+  const uint64_t limit = args.wait_limit_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(QFULL), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(KFULL + i), 1);
+      mbar_init(bar(KFREE + i), 1);
+      mbar_init(bar(SFULL + i), 1);
+      mbar_init(bar(SFREE + i), 128);
+      mbar_init(bar(PFULL + i), 128);
+      mbar_init(bar(PVDONE + i), 1);
+    }
+    mbar_init(bar(VFULL), 1);
+    mbar_init(bar(VFREE), 1);
+    mbar_init(bar(DRAIN), 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmVt);
+    tma_prefetch_desc(&tmO);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto fail = [&]() {
+    atomicOr(args.err, NC_DEVFLAG_TIMEOUT);
+    *abort_flag = 1;
+  };
+  auto wait = [&](int i, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait(bar(i), parity, limit)) return true;
+    fail();
+    return false;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = true;
+      int kin[2] = {-1, -1}, vin = -1;               // parity of loads in flight
+      mbar_arrive_expect_tx(bar(QFULL), 2 * ATC_TILE);
+      for (int t = 0; t < 2; ++t)
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(s0 + ATC_OFF_Q + t * ATC_TILE + h * ATC_HALF, &tmQ, bar(QFULL),
+                      (2 * hp + t) * 128 + 64 * h, q0, b);
+      for (int j = 0; ok && j < nb; ++j) {
+        const int ks = j & 1;
+        if (!wait(KFREE + ks, ((j >> 1) & 1) ^ 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(KFULL + ks), ATC_TILE);
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(s0 + ATC_OFF_K + ks * ATC_TILE + h * ATC_HALF, &tmK, bar(KFULL + ks), 64 * h,
+                      j * 128, b);
+        kin[ks] = (j >> 1) & 1;
+        if (!wait(VFREE, (j & 1) ^ 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(VFULL), ATC_TILE);
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(s0 + ATC_OFF_V + h * ATC_HALF, &tmVt, bar(VFULL), j * 128 + 64 * h, 0, b);
+        vin = j & 1;
+      }
+      if (!ok) {
+        // let every copy still in flight land before the CTA exits
+        mbar_wait(bar(QFULL), 0, limit);
+        for (int s = 0; s < 2; ++s)
+          if (kin[s] >= 0) mbar_wait(bar(KFULL + s), (uint32_t)kin[s], limit);
+        if (vin >= 0) mbar_wait(bar(VFULL), (uint32_t)vin, limit);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+      bool ok = wait(QFULL, 0), any = false;
+      for (int j = 0; ok && j < nb; ++j) {
+        const int ks = j & 1;
+        if (!wait(KFULL + ks, (j >> 1) & 1)) { ok = false; break; }
+        for (int t = 0; ok && t < 2; ++t) {
+          if (j > 0 && !wait(SFREE + t, (j - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qa = s0 + ATC_OFF_Q + t * ATC_TILE, ka = s0 + ATC_OFF_K + ks * ATC_TILE;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * ATC_HALF + (kk & 3) * 32;
+            tc_mma_f16(tmem_base + t * 128, smem_desc_sw128(qa + off), smem_desc_sw128(ka + off), idesc,
+                       kk != 0);
+          }
+          any = true;
+          tc_commit(bar(SFULL + t));
+        }
+        if (!ok) break;
+        tc_commit(bar(KFREE + ks));
+        if (!wait(VFULL, j & 1)) { ok = false; break; }
+        for (int t = 0; ok && t < 2; ++t) {
+          if (!wait(PFULL + t, j & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t pa = s0 + ATC_OFF_P + t * ATC_TILE, va = s0 + ATC_OFF_V;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * ATC_HALF + (kk & 3) * 32;
+            tc_mma_f16(tmem_base + 256 + t * 128, smem_desc_sw128(pa + off), smem_desc_sw128(va + off),
+                       idesc, (j | kk) != 0);
+          }
+          tc_commit(bar(PVDONE + t));
+        }
+        if (!ok) break;
+        tc_commit(bar(VFREE));
+      }
+      if (!ok && any) {
+        // every issued MMA must finish before TMEM is released
+        tc_commit(bar(DRAIN));
+        mbar_wait(bar(DRAIN), 0, limit);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int t = (warp - 2) >> 2;                  // tile: 0 = head 2hp, 1 = head 2hp+1
+    const int qd = warp & 3;                        // TMEM lane quarter
+    const int r = 32 * qd + lane;                   // row of the tile = query q0 + r
+    const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
+    const uint32_t tS = tmem_base + lane_off + t * 128;
+    const uint32_t tO = tmem_base + lane_off + 256 + t * 128;
+    const uint32_t pbuf = s0 + ATC_OFF_P + t * ATC_TILE;
+    const float sl2 = args.scale_log2;
+    float m = -INFINITY;                            // reference max (raw score units)
+    float l = 0.f;                                  // running sum of exp2((s - m) * sl2)
+    bool ok = true;
+    for (int j = 0; ok && j < nb; ++j) {
+      if (!wait(SFULL + t, j & 1)) { ok = false; break; }
+      tc_fence_after();
+      const bool diag = j == qt;
+      // pass 1: block max over the row's unmasked keys
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 128; c += 32) {
+        float v[32];
+        tmem_ld32(tS + c, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (!(diag && c + i > r)) mx = fmaxf(mx, v[i]);
+      }
+      bool rescale = false;
+      float factor = 1.f;
+      if (mx > m && (m == -INFINITY || (mx - m) * sl2 > 8.f)) {
+        factor = ex2_approx((m - mx) * sl2);        // 0 when m = -inf
+        l *= factor;
+        m = mx;
+        rescale = j > 0;
+      }
+      // P_t of the previous block must have been consumed (and O_t written)
+      if (j > 0 && !wait(PVDONE + t, (j - 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      const float mb = m * sl2;
+      // pass 2: P = exp2(s * sl2 - m * sl2) in bf16, row sum in fp32
+#pragma unroll 1
+      for (int c = 0; c < 128; c += 32) {
+        float v[32];
+        tmem_ld32(tS + c, v);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float p0 = ex2_approx(fmaf(v[i], sl2, -mb));
+          float p1 = ex2_approx(fmaf(v[i + 1], sl2, -mb));
+          if (diag && c + i > r) p0 = 0.f;
+          if (diag && c + i + 1 > r) p1 = 0.f;
+          l += p0 + p1;
+          w[i >> 1] = pack_bf16_2(p0, p1);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          st_shared_v4u(atc_addr(pbuf, r, c + 8 * k), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(SFREE + t));                  // S_t may be overwritten
+      if (rescale) {
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          float v[32];
+          tmem_ld32(tO + c, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= factor;
+          tmem_st32(tO + c, v);
+        }
+        tmem_wait_st();
+      }
+      fence_async_smem();                           // P visible to the tensor core
+      tc_fence_before();
+      mbar_arrive(bar(PFULL + t));
+    }
+    // ---- epilogue: O / l -> bf16 -> P buffer -> TMA store
+    if (ok && !wait(PVDONE + t, (nb - 1) & 1)) ok = false;
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+#pragma unroll 1
+      for (int c = 0; c < 128; c += 32) {
+        float v[32];
+        tmem_ld32(tO + c, v);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) w[i >> 1] = pack_bf16_2(v[i] * inv, v[i + 1] * inv);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          st_shared_v4u(atc_addr(pbuf, r, c + 8 * k), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+      }
+      fence_async_smem();
+    }
+    // every thread of the tile reaches this barrier exactly once
+    named_bar_sync(1 + t, 128);
+    if (threadIdx.x == 64 + 128 * t) {
+      if (ok && !*abort_flag) {
+        const int head = 2 * hp + t;
+        tma_store_3d(&tmO, pbuf, head * 128, q0, b);
+        tma_store_3d(&tmO, pbuf + ATC_HALF, head * 128 + 64, q0, b);
+        bulk_commit();
+      }
+      bulk_wait_all();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+}  // namespace nc

@@ -1,0 +1,269 @@
+// Decode-step projections: C[b, n] = sum_k A[b, k] W[n, k] for a handful of
+// rows b (the batch, B <= 128) on the 5th-generation tensor cores.
+//
+// With one new token per row the weight matrix is read once per step and
+// each weight is used B times, so these products are bound by HBM bandwidth,
+// not by the tensor core.  The operands are swapped relative to the prefill
+// GEMM: the MMA's 128-row operand is a tile of 128 weight rows, its N operand
+// is the batch (padded to a multiple of 16), so the accumulator in TMEM is
+// D[n][b] (lane = weight row).  To keep every SM streaming weights, K is
+// split across CTAs: grid = (N / 128) x splits, each CTA owns one weight tile
+// and K / splits of its columns, with all of its loads in flight at once.
+// Each CTA writes its fp32 partial D to a workspace; the last CTA of a tile
+// to finish (a counter per tile) sums the partials in split order, which
+// keeps the result deterministic, and applies the fused epilogue:
+//   EPI_QKV    (the tile is one head) QK-norm + RoPE at the row's position;
+//              q -> Q, k and v -> the KV cache row (b, pos)
+//   EPI_RESID  x[b, n] += sum                      (fp32 residual stream)
+//   EPI_RELU2  u[b, n] = bf16(relu(sum)^2)         (MLP hidden)
+//   EPI_LOGITS logits[b, n] = cap * tanh(sum/cap)  (fp32; used with 1 split)
+//
+// Bias-free projections, QK norm, RoPE, ReLU^2 and the logit softcap follow
+// the nanochat pages (yelogs.com story, "technical details and official Q&A";
+// geoz.com.cn "development tricks").
+//
+// 128 threads: warp 0 lane 0 issues the TMA loads, warp 1 lane 0 the MMAs,
+// then all four warps (warp w reads TMEM lanes 32w..32w+31) run the
+// epilogue.  Every mbarrier wait is bounded.
+#pragma once
+
+#include <cuda.h>
+#include "k_gemm_tc.cuh"
+#include "nc_common.cuh"
+
+namespace nc {
+
+struct SkinnyArgs {
+  int B, N, K;                    // rows, weight rows, reduction length
+  int splits, kb_per;             // K split into `splits` ranges of kb_per 64-wide blocks
+  float* part;                    // [splits][B][N] fp32 partials (splits > 1)
+  int* counters;                  // [N / 128], zero between launches
+  // epilogue outputs
+  float* x;                       // EPI_RESID: [B][N] fp32, += ; EPI_LOGITS: [B][N] fp32 out
+  __nv_bfloat16* out_bf;          // EPI_RELU2: [B][N]; EPI_QKV: Q [B][n_head*128]
+  __nv_bfloat16* k_cache;         // EPI_QKV: this layer's K [B_max][S][128]
+  __nv_bfloat16* v_cache;
+  const float* rope_cos;          // [S][64]
+  const float* rope_sin;
+  const int* pos_dev;             // EPI_QKV: position of the new token (device)
+  int n_head, cache_S;
+  float eps, softcap;
+  int* err;
+  unsigned long long wait_limit_ns;
+};
+
+template <int NB>
+struct SkCfg {
+  static constexpr uint32_t W_BYTES = 128 * 64 * 2;      // 16 KB
+  static constexpr uint32_t A_BYTES = NB * 64 * 2;
+  static constexpr uint32_t STAGE_BYTES = W_BYTES + A_BYTES;
+  static constexpr int STAGES = (int)(98304 / STAGE_BYTES) < 2 ? 2 : (int)(98304 / STAGE_BYTES);
+  static constexpr uint32_t TMEM_COLS = NB < 32 ? 32 : NB;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+};
+
+template <int NB, int EPI>
+__global__ void __launch_bounds__(128)
+    gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                       const SkinnyArgs args) {
+  using C = SkCfg<NB>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t sk_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sk_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sW = smem;
+  uint8_t* sA = smem + STAGES * C::W_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + STAGES * C::A_BYTES);
+  // bars: full[STAGES], empty[STAGES], done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);   // [0] abort, [1] last CTA
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int FULL = 0, EMPTY = STAGES, DONE = 2 * STAGES;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x, split = blockIdx.y;
+  const int n0 = tile * 128;
+  const int kb0 = split * args.kb_per;
+  const int nkb = args.kb_per;
+  const uint64_t limit = args.wait_limit_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(FULL + s), 1);
+      mbar_init(bar(EMPTY + s), 1);
+    }
+    mbar_init(bar(DONE), 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmA);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  auto fail = [&]() {
+    atomicOr(args.err, NC_DEVFLAG_TIMEOUT);
+    flags[0] = 1;
+  };
+
+  bool mma_ok = true;
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    int issued[STAGES];
+    for (int s = 0; s < STAGES; ++s) issued[s] = -1;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int kb = 0; kb < nkb; ++kb) {
+      if (flags[0] || !mbar_wait(bar(EMPTY + stage), phase ^ 1, limit)) {
+        if (!flags[0]) fail();
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(bar(FULL + stage), C::STAGE_BYTES);
+      tma_load_2d(smem_u32(sW + stage * C::W_BYTES), &tmW, bar(FULL + stage), (kb0 + kb) * 64, n0);
+      tma_load_2d(smem_u32(sA + stage * C::A_BYTES), &tmA, bar(FULL + stage), (kb0 + kb) * 64, 0);
+      issued[stage] = (int)phase;
+      if (++stage == STAGES) { stage = 0; phase ^= 1; }
+    }
+    if (!ok)
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s] >= 0) mbar_wait(bar(FULL + s), (uint32_t)issued[s], limit);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(128, NB);
+    uint32_t stage = 0, phase = 0;
+    bool any = false;
+    for (int kb = 0; kb < nkb; ++kb) {
+      if (flags[0] || !mbar_wait(bar(FULL + stage), phase, limit)) {
+        if (!flags[0]) fail();
+        mma_ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t w0 = smem_u32(sW + stage * C::W_BYTES), a0 = smem_u32(sA + stage * C::A_BYTES);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        tc_mma_f16(tmem_base, smem_desc_sw128(w0 + k * 32), smem_desc_sw128(a0 + k * 32), idesc,
+                   (kb | k) != 0);
+      any = true;
+      tc_commit(bar(EMPTY + stage));
+      if (++stage == STAGES) { stage = 0; phase ^= 1; }
+    }
+    // completion of every issued MMA (also the drain on the abort path)
+    if (any) tc_commit(bar(DONE));
+    else mbar_arrive(bar(DONE));
+  }
+  __syncwarp();
+
+  // ------------------------------------------------------------- epilogue
+  const bool done_ok = mbar_wait(bar(DONE), 0, limit);
+  if (!done_ok && threadIdx.x == 0) fail();
+  tc_fence_after();
+  const int row = 32 * warp + lane;                  // weight row n0 + row
+  const uint32_t taddr = tmem_base + ((uint32_t)(32 * warp) << 16);
+  const bool ok = done_ok && !flags[0];
+  __syncthreads();
+  const bool run = ok && !flags[0];
+
+  if (EPI == EPI_LOGITS && args.splits == 1) {
+    if (run) {
+      const float inv_cap = 1.f / args.softcap;
+#pragma unroll 1
+      for (int c = 0; c < NB; c += 32) {
+        float v[32];
+        tmem_ld32(taddr + c, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c + j < args.B) args.x[(size_t)(c + j) * args.N + n0 + row] = softcap_f(v[j], inv_cap, args.softcap);
+      }
+    }
+  } else {
+    // partial D -> workspace [split][b][n]
+    if (run) {
+#pragma unroll 1
+      for (int c = 0; c < NB; c += 32) {
+        float v[32];
+        tmem_ld32(taddr + c, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c + j < args.B) args.part[((size_t)split * args.B + c + j) * args.N + n0 + row] = v[j];
+      }
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0 && run) {
+      const int prev = atomicAdd(&args.counters[tile], 1);
+      flags[1] = prev == args.splits - 1;
+    }
+    __syncthreads();
+    if (run && flags[1]) {
+      __threadfence();
+      if (threadIdx.x == 0) args.counters[tile] = 0;   // ready for the next launch
+      const float* part = args.part;
+      const size_t plane = (size_t)args.B * args.N;
+      if constexpr (EPI == EPI_RESID || EPI == EPI_RELU2 || EPI == EPI_LOGITS) {
+        // thread = column n0 + row, loop over batch rows: coalesced across lanes
+        for (int b = 0; b < args.B; ++b) {
+          const size_t o = (size_t)b * args.N + n0 + row;
+          float s = 0.f;
+          for (int sp = 0; sp < args.splits; ++sp) s += __ldcg(part + sp * plane + o);
+          if constexpr (EPI == EPI_RESID) {
+            args.x[o] += s;
+          } else if constexpr (EPI == EPI_RELU2) {
+            const float r = fmaxf(s, 0.f);
+            args.out_bf[o] = f2bf(r * r);
+          } else {
+            args.x[o] = softcap_f(s, 1.f / args.softcap, args.softcap);
+          }
+        }
+      } else if constexpr (EPI == EPI_QKV) {
+        // one warp per batch row; lane holds dims lane + 32 i (i = 0..3) so
+        // both members of a RoPE pair (j, j + 64) sit in the same lane
+        const int head = tile;
+        const bool is_v = head == args.n_head + 1;
+        const int pos = *args.pos_dev;
+        for (int b = warp; b < args.B; b += 4) {
+          float v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const size_t o = (size_t)b * args.N + n0 + lane + 32 * i;
+            float s = 0.f;
+            for (int sp = 0; sp < args.splits; ++sp) s += __ldcg(part + sp * plane + o);
+            v[i] = s;
+          }
+          if (!is_v) {
+            float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+            ss = warp_sum(ss);
+            const float r = rsqrtf(ss * (1.f / 128.f) + args.eps);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int j = lane + 32 * i;
+              const float cs = args.rope_cos[(size_t)pos * 64 + j], sn = args.rope_sin[(size_t)pos * 64 + j];
+              const float x0 = v[i] * r, x1 = v[i + 2] * r;
+              v[i] = x0 * cs - x1 * sn;
+              v[i + 2] = x0 * sn + x1 * cs;
+            }
+          }
+          __nv_bfloat16* dst;
+          if (head < args.n_head)
+            dst = args.out_bf + (size_t)b * args.n_head * 128 + head * 128;
+          else
+            dst = (is_v ? args.v_cache : args.k_cache) + ((size_t)b * args.cache_S + pos) * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = f2bf(v[i]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+}  // namespace nc

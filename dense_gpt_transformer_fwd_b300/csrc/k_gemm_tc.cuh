@@ -45,6 +45,8 @@ struct GemmArgs {
   const float* rope_cos;          // [S][64]
   const float* rope_sin;          // [S][64]
   int n_head, T, pos0, cache_S;
+  __nv_bfloat16* vt;              // optional V^T [B_max][128][vt_S] for the prefill attention
+  int vt_S;
   float eps;
   // EPI_LOGITS
   float softcap;
@@ -352,6 +354,16 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
                   a[j] = x0 * cc4[k] - x1 * sn4[k];
                   bb[j] = x0 * sn4[k] + x1 * cc4[k];
                 }
+              }
+            }
+            if (is_v && args.vt != nullptr && my_row < args.M) {
+              // transposed copy V^T[b][dim][pos]: lanes (consecutive positions)
+              // write consecutive addresses for each dim
+              __nv_bfloat16* vt = args.vt + (size_t)b * 128 * args.vt_S + pos;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                vt[(size_t)(c + j) * args.vt_S] = f2bf(a[j]);
+                vt[(size_t)(64 + c + j) * args.vt_S] = f2bf(bb[j]);
               }
             }
             // columns c..c+31 of each half = 16-byte chunks c/8 .. c/8+3

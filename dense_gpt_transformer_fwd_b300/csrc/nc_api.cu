@@ -25,6 +25,7 @@
 
 #include "k_attn_mma.cuh"
 #include "k_attn_simt.cuh"
+#include "k_attn_tc.cuh"
 #include "k_gemm_tc.cuh"
 #include "k_rowops.cuh"
 #include "nc_common.cuh"
@@ -74,6 +75,22 @@ bool make_tmap(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, u
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(tm, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D bf16 tensor map, dims/box innermost first, 128-byte swizzle (box[0] =
+// 64 elements = one swizzle row), zero fill out of bounds.
+bool make_tmap3(CUtensorMap* tm, const void* ptr, const uint64_t dims[3], const uint64_t strides_b[2],
+                const uint32_t box[3]) {
+  if (!load_encode()) return false;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || strides_b[0] % 16 || strides_b[1] % 16) return false;
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {strides_b[0], strides_b[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), d, st, bx, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -144,6 +161,10 @@ struct nc_model {
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_used = 0;
   std::vector<ProfRec> recs;
+  void* vt = nullptr;                  // prefill V^T [max_batch][128][vt_S] (bf16)
+  int vt_S = 0;
+  CUtensorMap tm_vt{};                 // 3-D map over vt, box 64 keys x 128 dims
+  std::vector<CUtensorMap> tm_kc;      // per layer 3-D map over the K cache, box 64 x 128 keys
   float* part_o = nullptr;             // decode attention partials [max_batch][chunks][16][128]
   float* part_ml = nullptr;            // [max_batch][chunks][16][2]
   int max_chunks = 0;
@@ -163,7 +184,7 @@ void free_model(nc_model* m) {
   for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
   void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->k_alloc, m->v_alloc, m->x,
                   m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
-                  m->tok_stage, m->logit_stage, m->err, m->part_o, m->part_ml};
+                  m->tok_stage, m->logit_stage, m->err, m->part_o, m->part_ml, m->vt};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete m;
@@ -210,7 +231,7 @@ nc_status validate(const nc_config* c) {
   if (c->n_kv_head != 1) return NC_ERR_UNSUPPORTED;
   if (c->dtype == NC_BF16) {
     if (c->head_dim != 128 || c->d_model % 256 || c->d_mlp % 256 || c->vocab % 256 ||
-        ((c->n_head + 2) * 128) % 256 || c->n_head > 16)
+        ((c->n_head + 2) * 128) % 256 || c->n_head > 16 || c->n_head % 2)
       return NC_ERR_UNSUPPORTED;
   } else {
     if ((c->head_dim != 64 && c->head_dim != 128) || c->d_model % 32) return NC_ERR_UNSUPPORTED;
@@ -270,6 +291,14 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
   const bool bf = m->bf16;
   using bf16 = __nv_bfloat16;
 
+  CUtensorMap tm_qa[2];  // q and att viewed as [B][T][n_head*128], box 64 x 128 rows
+  if (bf && pos0 == 0 && T > 1) {
+    const uint64_t dims[3] = {(uint64_t)NQ, (uint64_t)T, (uint64_t)B};
+    const uint64_t strides[2] = {(uint64_t)NQ * 2, (uint64_t)T * NQ * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    if (!make_tmap3(&tm_qa[0], m->q, dims, strides, box) || !make_tmap3(&tm_qa[1], m->att, dims, strides, box))
+      return NC_ERR_CUDA;
+  }
   {  // x = rms(E[tok]); h = rms(x)
     KScope ks(m, NC_K_EMBED, s);
     if (bf)
@@ -294,6 +323,10 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
         a.T = T;
         a.pos0 = pos0;
         a.cache_S = c.max_seq;
+        if (pos0 == 0 && T > 1) {
+          a.vt = static_cast<bf16*>(m->vt);
+          a.vt_S = m->vt_S;
+        }
         NC_TRY((launch_gemm_tc<256, EPI_QKV>(m, m->tm_h, m->tm_wqkv[l], m->tm_q_st, a, s)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_STORE>(m, static_cast<const float*>(m->h),
@@ -309,11 +342,17 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
     }
     {  // causal MQA attention over the cache
       KScope ks(m, NC_K_ATTN, s);
-      if (bf && pos0 == 0) {
-        attn_prefill_mma_kernel<<<dim3((T + 31) / 32, nh / 2, B), 128, ATT_PREFILL_SMEM, s>>>(
-            static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
-            static_cast<const bf16*>(m->vc(l)), static_cast<bf16*>(m->att), T, nh, c.max_seq, pos0,
-            kAttnScaleLog2);
+      if (bf && pos0 == 0 && T > 1) {
+        AttnTcArgs aa;
+        aa.B = B;
+        aa.T = T;
+        aa.n_head = nh;
+        aa.n_qt = (T + 127) / 128;
+        aa.scale_log2 = kAttnScaleLog2;
+        aa.err = m->err;
+        aa.wait_limit_ns = m->wait_limit_ns;
+        attn_prefill_tc_kernel<<<aa.n_qt * B * (nh / 2), ATC_THREADS, ATC_SMEM, s>>>(
+            tm_qa[0], m->tm_kc[l], m->tm_vt, tm_qa[1], aa);
         m->launches++;
         NC_TRY(cudaGetLastError());
       } else if (bf) {
@@ -595,8 +634,11 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
     m->max_chunks = (c.max_seq + DEC_CHUNK - 1) / DEC_CHUNK;
     CREATE_TRY(cudaMalloc(&m->part_o, (int64_t)c.max_batch * m->max_chunks * 16 * 128 * 4));
     CREATE_TRY(cudaMalloc(&m->part_ml, (int64_t)c.max_batch * m->max_chunks * 16 * 2 * 4));
-    CREATE_TRY(cudaFuncSetAttribute(attn_prefill_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)ATT_PREFILL_SMEM));
+    CREATE_TRY(cudaFuncSetAttribute(attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)ATC_SMEM));
+    m->vt_S = (c.max_seq + 127) / 128 * 128;
+    CREATE_TRY(cudaMalloc(&m->vt, (int64_t)c.max_batch * 128 * m->vt_S * 2));
+    CREATE_TRY(cudaMemset(m->vt, 0, (int64_t)c.max_batch * 128 * m->vt_S * 2));
     CREATE_TRY(cudaFuncSetAttribute(attn_decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)ATT_DECODE_SMEM));
   }
@@ -618,6 +660,19 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
     m->tm_wo.resize(c.n_layer);
     m->tm_wfc.resize(c.n_layer);
     m->tm_wproj.resize(c.n_layer);
+    {
+      const uint64_t dims[3] = {(uint64_t)m->vt_S, 128, (uint64_t)c.max_batch};
+      const uint64_t strides[2] = {(uint64_t)m->vt_S * 2, (uint64_t)m->vt_S * 256};
+      const uint32_t box[3] = {64, 128, 1};
+      ok = ok && make_tmap3(&m->tm_vt, m->vt, dims, strides, box);
+    }
+    m->tm_kc.resize(c.n_layer);
+    for (int l = 0; ok && l < c.n_layer; ++l) {
+      const uint64_t dims[3] = {128, (uint64_t)c.max_seq, (uint64_t)c.max_batch};
+      const uint64_t strides[2] = {256, (uint64_t)c.max_seq * 256};
+      const uint32_t box[3] = {64, 128, 1};
+      ok = make_tmap3(&m->tm_kc[l], m->kc(l), dims, strides, box);
+    }
     for (int l = 0; ok && l < c.n_layer; ++l)
       ok = make_tmap(&m->tm_wqkv[l], m->wqkv[l], NQKV, d, 256) &&
            make_tmap(&m->tm_wo[l], m->wo[l], d, NQ, 256) &&
