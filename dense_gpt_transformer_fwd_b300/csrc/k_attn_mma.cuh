@@ -62,7 +62,12 @@ constexpr int DEC_KPW = DEC_CHUNK / 4;     // keys per warp
 __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kc,
     const __nv_bfloat16* __restrict__ Vc, float* __restrict__ part_o, float* __restrict__ part_ml,
-    int n_head, int cache_S, int ctx, int nchunk, float scale_log2) {
+    int n_head, int cache_S, int ctx, const int* __restrict__ pos_dev, float scale_log2) {
+  // with pos_dev the context is read on the device (the step is graph-replayable);
+  // chunks beyond it exit
+  if (pos_dev) ctx = *pos_dev + 1;
+  const int nchunk = (ctx + DEC_CHUNK - 1) / DEC_CHUNK;
+  if ((int)blockIdx.x >= nchunk) return;
   extern __shared__ __align__(128) uint8_t att_smem[];
   const uint32_t sQ = smem_u32(att_smem);                     // 16 rows
   const uint32_t sK = sQ + 16 * 256;                           // DEC_CHUNK keys
@@ -212,7 +217,9 @@ constexpr size_t ATT_DECODE_SMEM = (16 + 2 * DEC_CHUNK) * 256 + 4 * 16 * 2 * 4;
 // One CTA per (batch row, head): merge the chunks, write bf16 output.
 __global__ void __launch_bounds__(128) attn_decode_combine_kernel(
     const float* __restrict__ part_o, const float* __restrict__ part_ml,
-    __nv_bfloat16* __restrict__ O, int n_head, int nchunk) {
+    __nv_bfloat16* __restrict__ O, int n_head, int ctx, const int* __restrict__ pos_dev) {
+  if (pos_dev) ctx = *pos_dev + 1;
+  const int nchunk = (ctx + DEC_CHUNK - 1) / DEC_CHUNK;
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   float gm = -INFINITY;
   for (int c = 0; c < nchunk; ++c) gm = fmaxf(gm, part_ml[(((size_t)b * nchunk + c) * 16 + h) * 2]);

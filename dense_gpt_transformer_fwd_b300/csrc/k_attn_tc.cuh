@@ -203,42 +203,54 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
+    // order: S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...  so that
+    // the softmax of one head overlaps the tensor-core work of the other
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
-      bool ok = wait(QFULL, 0), any = false;
-      for (int j = 0; ok && j < nb; ++j) {
-        const int ks = j & 1;
-        if (!wait(KFULL + ks, (j >> 1) & 1)) { ok = false; break; }
-        for (int t = 0; ok && t < 2; ++t) {
-          if (j > 0 && !wait(SFREE + t, (j - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t qa = s0 + ATC_OFF_Q + t * ATC_TILE, ka = s0 + ATC_OFF_K + ks * ATC_TILE;
+      auto issue_s = [&](int t, int ks) {
+        const uint32_t qa = s0 + ATC_OFF_Q + t * ATC_TILE, ka = s0 + ATC_OFF_K + ks * ATC_TILE;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * ATC_HALF + (kk & 3) * 32;
-            tc_mma_f16(tmem_base + t * 128, smem_desc_sw128(qa + off), smem_desc_sw128(ka + off), idesc,
-                       kk != 0);
-          }
-          any = true;
-          tc_commit(bar(SFULL + t));
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * ATC_HALF + (kk & 3) * 32;
+          tc_mma_f16(tmem_base + t * 128, smem_desc_sw128(qa + off), smem_desc_sw128(ka + off), idesc, kk != 0);
         }
-        if (!ok) break;
-        tc_commit(bar(KFREE + ks));
+        tc_commit(bar(SFULL + t));
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t pa = s0 + ATC_OFF_P + t * ATC_TILE, va = s0 + ATC_OFF_V;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * ATC_HALF + (kk & 3) * 32;
+          tc_mma_f16(tmem_base + 256 + t * 128, smem_desc_sw128(pa + off), smem_desc_sw128(va + off), idesc,
+                     (j | kk) != 0);
+        }
+        tc_commit(bar(PVDONE + t));
+      };
+      bool ok = wait(QFULL, 0) && wait(KFULL + 0, 0), any = false;
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+        tc_commit(bar(KFREE + 0));
+        any = true;
+      }
+      for (int j = 0; ok && j < nb; ++j) {
+        const bool more = j + 1 < nb;
+        const int ks1 = (j + 1) & 1;
         if (!wait(VFULL, j & 1)) { ok = false; break; }
         for (int t = 0; ok && t < 2; ++t) {
           if (!wait(PFULL + t, j & 1)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t pa = s0 + ATC_OFF_P + t * ATC_TILE, va = s0 + ATC_OFF_V;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * ATC_HALF + (kk & 3) * 32;
-            tc_mma_f16(tmem_base + 256 + t * 128, smem_desc_sw128(pa + off), smem_desc_sw128(va + off),
-                       idesc, (j | kk) != 0);
+          issue_pv(t, j);
+          if (t == 1) tc_commit(bar(VFREE));
+          if (more) {
+            if (t == 0 && !wait(KFULL + ks1, ((j + 1) >> 1) & 1)) { ok = false; break; }
+            if (!wait(SFREE + t, j & 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(t, ks1);
+            if (t == 1) tc_commit(bar(KFREE + ks1));
           }
-          tc_commit(bar(PVDONE + t));
         }
-        if (!ok) break;
-        tc_commit(bar(VFREE));
       }
       if (!ok && any) {
         // every issued MMA must finish before TMEM is released
@@ -262,17 +274,18 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     for (int j = 0; ok && j < nb; ++j) {
       if (!wait(SFULL + t, j & 1)) { ok = false; break; }
       tc_fence_after();
-      const bool diag = j == qt;
-      // pass 1: block max over the row's unmasked keys
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 128; c += 32) {
-        float v[32];
-        tmem_ld32(tS + c, v);
+      float v[128];
+      tmem_ld128(tS, v);                            // the whole row of S_t
+      tc_fence_before();
+      mbar_arrive(bar(SFREE + t));                  // S_t may be overwritten
+      if (j == qt) {                                // diagonal block: keys c > r are in the future
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (!(diag && c + i > r)) mx = fmaxf(mx, v[i]);
+        for (int c = 0; c < 128; ++c)
+          if (c > r) v[c] = -INFINITY;
       }
+      float mx = v[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, v[c]);
       bool rescale = false;
       float factor = 1.f;
       if (mx > m && (m == -INFINITY || (mx - m) * sl2 > 8.f)) {
@@ -281,39 +294,29 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
         m = mx;
         rescale = j > 0;
       }
+      const float mb = m * sl2;
+      uint32_t w[64];
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float p0 = ex2_approx(fmaf(v[c], sl2, -mb));
+        const float p1 = ex2_approx(fmaf(v[c + 1], sl2, -mb));
+        l += p0 + p1;
+        w[c >> 1] = pack_bf16_2(p0, p1);
+      }
       // P_t of the previous block must have been consumed (and O_t written)
       if (j > 0 && !wait(PVDONE + t, (j - 1) & 1)) { ok = false; break; }
       tc_fence_after();
-      const float mb = m * sl2;
-      // pass 2: P = exp2(s * sl2 - m * sl2) in bf16, row sum in fp32
-#pragma unroll 1
-      for (int c = 0; c < 128; c += 32) {
-        float v[32];
-        tmem_ld32(tS + c, v);
-        uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float p0 = ex2_approx(fmaf(v[i], sl2, -mb));
-          float p1 = ex2_approx(fmaf(v[i + 1], sl2, -mb));
-          if (diag && c + i > r) p0 = 0.f;
-          if (diag && c + i + 1 > r) p1 = 0.f;
-          l += p0 + p1;
-          w[i >> 1] = pack_bf16_2(p0, p1);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          st_shared_v4u(atc_addr(pbuf, r, c + 8 * k), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(SFREE + t));                  // S_t may be overwritten
+      for (int k = 0; k < 16; ++k)
+        st_shared_v4u(atc_addr(pbuf, r, 8 * k), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
       if (rescale) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
-          float v[32];
-          tmem_ld32(tO + c, v);
+          float o[32];
+          tmem_ld32(tO + c, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= factor;
-          tmem_st32(tO + c, v);
+          for (int i = 0; i < 32; ++i) o[i] *= factor;
+          tmem_st32(tO + c, o);
         }
         tmem_wait_st();
       }
@@ -326,17 +329,14 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;
-#pragma unroll 1
-      for (int c = 0; c < 128; c += 32) {
-        float v[32];
-        tmem_ld32(tO + c, v);
-        uint32_t w[16];
+      float v[128];
+      tmem_ld128(tO, v);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) w[i >> 1] = pack_bf16_2(v[i] * inv, v[i + 1] * inv);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          st_shared_v4u(atc_addr(pbuf, r, c + 8 * k), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-      }
+      for (int k = 0; k < 16; ++k)
+        st_shared_v4u(atc_addr(pbuf, r, 8 * k), pack_bf16_2(v[8 * k] * inv, v[8 * k + 1] * inv),
+                      pack_bf16_2(v[8 * k + 2] * inv, v[8 * k + 3] * inv),
+                      pack_bf16_2(v[8 * k + 4] * inv, v[8 * k + 5] * inv),
+                      pack_bf16_2(v[8 * k + 6] * inv, v[8 * k + 7] * inv));
       fence_async_smem();
     }
     // every thread of the tile reaches this barrier exactly once

@@ -8,10 +8,12 @@
 // is the batch (padded to a multiple of 16), so the accumulator in TMEM is
 // D[n][b] (lane = weight row).  To keep every SM streaming weights, K is
 // split across CTAs: grid = (N / 128) x splits, each CTA owns one weight tile
-// and K / splits of its columns, with all of its loads in flight at once.
-// Each CTA writes its fp32 partial D to a workspace; the last CTA of a tile
-// to finish (a counter per tile) sums the partials in split order, which
-// keeps the result deterministic, and applies the fused epilogue:
+// and K / splits of its columns, with its loads in flight at once.  The
+// splits of one tile form a thread-block cluster: each CTA parks its fp32
+// partial D in its own shared memory, and after a cluster barrier CTA r sums
+// the partials of every CTA (distributed shared memory, in rank order, so
+// the result is deterministic) for the batch rows b = r (mod splits) and
+// applies the fused epilogue:
 //   EPI_QKV    (the tile is one head) QK-norm + RoPE at the row's position;
 //              q -> Q, k and v -> the KV cache row (b, pos)
 //   EPI_RESID  x[b, n] += sum                      (fp32 residual stream)
@@ -36,8 +38,7 @@ namespace nc {
 struct SkinnyArgs {
   int B, N, K;                    // rows, weight rows, reduction length
   int splits, kb_per;             // K split into `splits` ranges of kb_per 64-wide blocks
-  float* part;                    // [splits][B][N] fp32 partials (splits > 1)
-  int* counters;                  // [N / 128], zero between launches
+                                  // (the cluster size along grid y)
   // epilogue outputs
   float* x;                       // EPI_RESID: [B][N] fp32, += ; EPI_LOGITS: [B][N] fp32 out
   __nv_bfloat16* out_bf;          // EPI_RELU2: [B][N]; EPI_QKV: Q [B][n_head*128]
@@ -60,7 +61,26 @@ struct SkCfg {
   static constexpr int STAGES = (int)(98304 / STAGE_BYTES) < 2 ? 2 : (int)(98304 / STAGE_BYTES);
   static constexpr uint32_t TMEM_COLS = NB < 32 ? 32 : NB;
   static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+  static_assert((size_t)STAGES * STAGE_BYTES >= (size_t)NB * 128 * 4, "partial tile must fit the ring");
 };
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// all threads of all CTAs of the cluster; release/acquire orders the shared
+// memory writes before the barrier with the remote reads after it
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
 
 template <int NB, int EPI>
 __global__ void __launch_bounds__(128)
@@ -75,7 +95,7 @@ __global__ void __launch_bounds__(128)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sA + STAGES * C::A_BYTES);
   // bars: full[STAGES], empty[STAGES], done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
-  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);   // [0] abort, [1] last CTA
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);   // [0] abort
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int FULL = 0, EMPTY = STAGES, DONE = 2 * STAGES;
 
@@ -93,7 +113,6 @@ __global__ void __launch_bounds__(128)
     }
     mbar_init(bar(DONE), 1);
     flags[0] = 0;
-    flags[1] = 0;
     mbar_fence_init();
   }
   if (warp == 0 && lane == 0) {
@@ -165,13 +184,12 @@ __global__ void __launch_bounds__(128)
   tc_fence_after();
   const int row = 32 * warp + lane;                  // weight row n0 + row
   const uint32_t taddr = tmem_base + ((uint32_t)(32 * warp) << 16);
-  const bool ok = done_ok && !flags[0];
   __syncthreads();
-  const bool run = ok && !flags[0];
+  const bool run = done_ok && !flags[0];
+  const float inv_cap = 1.f / args.softcap;
 
-  if (EPI == EPI_LOGITS && args.splits == 1) {
+  if (args.splits == 1 && EPI == EPI_LOGITS) {
     if (run) {
-      const float inv_cap = 1.f / args.softcap;
 #pragma unroll 1
       for (int c = 0; c < NB; c += 32) {
         float v[32];
@@ -182,7 +200,9 @@ __global__ void __launch_bounds__(128)
       }
     }
   } else {
-    // partial D -> workspace [split][b][n]
+    // this CTA's partial D[n][b] -> own shared memory as P[b][n] (the ring is
+    // free: every load has landed and every MMA has read it)
+    const uint32_t psm = smem_u32(smem);
     if (run) {
 #pragma unroll 1
       for (int c = 0; c < NB; c += 32) {
@@ -190,50 +210,27 @@ __global__ void __launch_bounds__(128)
         tmem_ld32(taddr + c, v);
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (c + j < args.B) args.part[((size_t)split * args.B + c + j) * args.N + n0 + row] = v[j];
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(psm + ((c + j) * 128 + row) * 4), "f"(v[j]) : "memory");
       }
     }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0 && run) {
-      const int prev = atomicAdd(&args.counters[tile], 1);
-      flags[1] = prev == args.splits - 1;
-    }
-    __syncthreads();
-    if (run && flags[1]) {
-      __threadfence();
-      if (threadIdx.x == 0) args.counters[tile] = 0;   // ready for the next launch
-      const float* part = args.part;
-      const size_t plane = (size_t)args.B * args.N;
-      if constexpr (EPI == EPI_RESID || EPI == EPI_RELU2 || EPI == EPI_LOGITS) {
-        // thread = column n0 + row, loop over batch rows: coalesced across lanes
-        for (int b = 0; b < args.B; ++b) {
-          const size_t o = (size_t)b * args.N + n0 + row;
-          float s = 0.f;
-          for (int sp = 0; sp < args.splits; ++sp) s += __ldcg(part + sp * plane + o);
-          if constexpr (EPI == EPI_RESID) {
-            args.x[o] += s;
-          } else if constexpr (EPI == EPI_RELU2) {
-            const float r = fmaxf(s, 0.f);
-            args.out_bf[o] = f2bf(r * r);
-          } else {
-            args.x[o] = softcap_f(s, 1.f / args.softcap, args.softcap);
-          }
-        }
-      } else if constexpr (EPI == EPI_QKV) {
+    cluster_sync_all();                              // every CTA of the tile reaches it once
+    const int S = args.splits;
+    const int rank = (int)cluster_ctarank();
+    if (run) {
+      if constexpr (EPI == EPI_QKV) {
         // one warp per batch row; lane holds dims lane + 32 i (i = 0..3) so
         // both members of a RoPE pair (j, j + 64) sit in the same lane
         const int head = tile;
         const bool is_v = head == args.n_head + 1;
         const int pos = *args.pos_dev;
-        for (int b = warp; b < args.B; b += 4) {
+        for (int b = rank + S * warp; b < args.B; b += 4 * S) {
           float v[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const size_t o = (size_t)b * args.N + n0 + lane + 32 * i;
-            float s = 0.f;
-            for (int sp = 0; sp < args.splits; ++sp) s += __ldcg(part + sp * plane + o);
-            v[i] = s;
+            const uint32_t a = psm + (b * 128 + lane + 32 * i) * 4;
+            float sum = 0.f;
+            for (int q = 0; q < S; ++q) sum += ld_dsmem_f32(a, (uint32_t)q);
+            v[i] = sum;
           }
           if (!is_v) {
             float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
@@ -256,8 +253,25 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = f2bf(v[i]);
         }
+      } else {
+        // rows b = rank, rank + S, ...; thread = column n0 + row (coalesced)
+        for (int b = rank; b < args.B; b += S) {
+          const uint32_t a = psm + (b * 128 + row) * 4;
+          float sum = 0.f;
+          for (int q = 0; q < S; ++q) sum += ld_dsmem_f32(a, (uint32_t)q);
+          const size_t o = (size_t)b * args.N + n0 + row;
+          if constexpr (EPI == EPI_RESID) {
+            args.x[o] += sum;
+          } else if constexpr (EPI == EPI_RELU2) {
+            const float r = fmaxf(sum, 0.f);
+            args.out_bf[o] = f2bf(r * r);
+          } else {
+            args.x[o] = softcap_f(sum, inv_cap, args.softcap);
+          }
+        }
       }
     }
+    cluster_sync_all();                              // remote reads done before any CTA exits
   }
 
   tc_fence_before();

@@ -19,8 +19,10 @@ namespace nc {
 template <typename TW, typename TA>
 __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tok, const TW* __restrict__ E,
                                      float* __restrict__ x, TA* __restrict__ h, int M, int d,
-                                     int vocab, float eps, int* err) {
+                                     int vocab, float eps, int* err, int* len_set, int len_val) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  // the prefill records the cache length on the device for the decode steps
+  if (len_set && blockIdx.x == 0 && threadIdx.x == 0) *len_set = len_val;
   if (warp >= M) return;
   int t = tok[warp];
   if (t < 0 || t >= vocab) {
@@ -51,8 +53,11 @@ __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tok, const TW* 
 // (stride 1, offset 0 for all rows; stride T, offset T-1 for the last position of each row).
 template <typename TA>
 __global__ void rmsnorm_kernel(const float* __restrict__ x, TA* __restrict__ h, int rows, int d,
-                               int stride, int offset, float eps) {
+                               int stride, int offset, float eps, int* len_inc) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  // the final norm of a decode step advances the device-side cache length;
+  // every kernel of the step that reads it has finished (stream order)
+  if (len_inc && blockIdx.x == 0 && threadIdx.x == 0) *len_inc += 1;
   if (warp >= rows) return;
   const float* xr = x + ((size_t)warp * stride + offset) * d;
   float ss = 0.f;

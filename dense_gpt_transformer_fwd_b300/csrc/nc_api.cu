@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -26,6 +27,7 @@
 #include "k_attn_mma.cuh"
 #include "k_attn_simt.cuh"
 #include "k_attn_tc.cuh"
+#include "k_gemm_skinny.cuh"
 #include "k_gemm_tc.cuh"
 #include "k_rowops.cuh"
 #include "nc_common.cuh"
@@ -161,6 +163,19 @@ struct nc_model {
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_used = 0;
   std::vector<ProfRec> recs;
+  int* d_len = nullptr;                // device copy of the cache length (decode reads it)
+  // decode-step skinny GEMMs (bf16, B <= sk_nb)
+  int sk_nb = 0;                       // padded batch of the MMA N operand: 32, 64 or 128 (0 = off)
+  int sk_splits[4] = {1, 1, 1, 1};     // K splits of QKV, O-proj, FC, PROJ
+  std::vector<CUtensorMap> tm_w128;    // per layer Wqkv, Wo, Wfc, Wproj, box 64 x 128 rows
+  CUtensorMap tm_wu128{}, tm_h_nb{}, tm_att_nb{}, tm_u_nb{};
+  // captured decode step
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t g_exec = nullptr;
+  int g_B = 0;
+  const void* g_tok = nullptr;
+  const void* g_logits = nullptr;
+  int64_t g_launches = 0;
   void* vt = nullptr;                  // prefill V^T [max_batch][128][vt_S] (bf16)
   int vt_S = 0;
   CUtensorMap tm_vt{};                 // 3-D map over vt, box 64 keys x 128 dims
@@ -182,9 +197,12 @@ namespace {
 void free_model(nc_model* m) {
   if (!m) return;
   for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
+  if (m->g_exec) cudaGraphExecDestroy(m->g_exec);
+  if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
   void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->k_alloc, m->v_alloc, m->x,
                   m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
-                  m->tok_stage, m->logit_stage, m->err, m->part_o, m->part_ml, m->vt};
+                  m->tok_stage, m->logit_stage, m->err, m->part_o, m->part_ml, m->vt,
+                  m->d_len};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete m;
@@ -258,6 +276,22 @@ cudaError_t launch_gemm_tc(nc_model* m, const CUtensorMap& ta, const CUtensorMap
   return cudaGetLastError();
 }
 
+// K split for a decode-step GEMM with `tiles` weight tiles and `kb` 64-wide
+// K blocks: the divisor of kb, at most the portable cluster size 8, that puts
+// the CTA count closest to one per SM.
+int choose_splits(int tiles, int kb, int sms) {
+  int best = 1, best_gap = 1 << 30;
+  for (int sp = 1; sp <= kb && sp <= 8; ++sp) {
+    if (kb % sp) continue;
+    const int gap = std::abs(tiles * sp - sms);
+    if (gap < best_gap) {
+      best = sp;
+      best_gap = gap;
+    }
+  }
+  return best;
+}
+
 GemmArgs base_args(nc_model* m, int M, int N, int K) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -301,12 +335,15 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
   }
   {  // x = rms(E[tok]); h = rms(x)
     KScope ks(m, NC_K_EMBED, s);
+    int* len_set = pos0 == 0 ? m->d_len : nullptr;   // prefill: device length := T
     if (bf)
       embed_rmsnorm_kernel<bf16, bf16><<<blocks_for_warps(M), 256, 0, s>>>(
-          tok, static_cast<const bf16*>(m->E), m->x, static_cast<bf16*>(m->h), M, d, V, eps, m->err);
+          tok, static_cast<const bf16*>(m->E), m->x, static_cast<bf16*>(m->h), M, d, V, eps, m->err,
+          len_set, T);
     else
       embed_rmsnorm_kernel<float, float><<<blocks_for_warps(M), 256, 0, s>>>(
-          tok, static_cast<const float*>(m->E), m->x, static_cast<float*>(m->h), M, d, V, eps, m->err);
+          tok, static_cast<const float*>(m->E), m->x, static_cast<float*>(m->h), M, d, V, eps, m->err,
+          len_set, T);
     m->launches++;
     NC_TRY(cudaGetLastError());
   }
@@ -360,10 +397,10 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
         const int nchunk = (ctx + DEC_CHUNK - 1) / DEC_CHUNK;
         attn_decode_mma_kernel<<<dim3(nchunk, B), 128, ATT_DECODE_SMEM, s>>>(
             static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
-            static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, nh, c.max_seq, ctx, nchunk,
+            static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, nh, c.max_seq, ctx, nullptr,
             kAttnScaleLog2);
         attn_decode_combine_kernel<<<dim3(nh, B), 128, 0, s>>>(m->part_o, m->part_ml,
-                                                              static_cast<bf16*>(m->att), nh, nchunk);
+                                                              static_cast<bf16*>(m->att), nh, ctx, nullptr);
         m->launches += 2;
         NC_TRY(cudaGetLastError());
       } else {
@@ -388,9 +425,11 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
     {  // h = rms(x)
       KScope ks(m, NC_K_NORM, s);
       if (bf)
-        rmsnorm_kernel<bf16><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<bf16*>(m->h), M, d, 1, 0, eps);
+        rmsnorm_kernel<bf16><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<bf16*>(m->h), M, d, 1, 0,
+                                                                 eps, nullptr);
       else
-        rmsnorm_kernel<float><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<float*>(m->h), M, d, 1, 0, eps);
+        rmsnorm_kernel<float><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<float*>(m->h), M, d, 1, 0,
+                                                                  eps, nullptr);
       m->launches++;
       NC_TRY(cudaGetLastError());
     }
@@ -420,12 +459,14 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       const bool final_last = last_only && l == c.n_layer - 1;
       const int rows = final_last ? B : M;
       void* dst = final_last ? m->h_last : m->h;
+      // a decode step (pos0 > 0) advances the device-side length in its final norm
+      int* len_inc = (pos0 > 0 && l == c.n_layer - 1) ? m->d_len : nullptr;
       if (bf)
         rmsnorm_kernel<bf16><<<blocks_for_warps(rows), 256, 0, s>>>(
-            m->x, static_cast<bf16*>(dst), rows, d, final_last ? T : 1, final_last ? T - 1 : 0, eps);
+            m->x, static_cast<bf16*>(dst), rows, d, final_last ? T : 1, final_last ? T - 1 : 0, eps, len_inc);
       else
         rmsnorm_kernel<float><<<blocks_for_warps(rows), 256, 0, s>>>(
-            m->x, static_cast<float*>(dst), rows, d, final_last ? T : 1, final_last ? T - 1 : 0, eps);
+            m->x, static_cast<float*>(dst), rows, d, final_last ? T : 1, final_last ? T - 1 : 0, eps, len_inc);
       m->launches++;
       NC_TRY(cudaGetLastError());
     }
@@ -443,6 +484,193 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
           static_cast<const float*>(m->Wu), logits, out_rows, V, d, V, s));
     }
   }
+  return NC_OK;
+}
+
+template <int NB, int EPI>
+cudaError_t launch_skinny(nc_model* m, const CUtensorMap& tw, const CUtensorMap& ta, SkinnyArgs a, int tiles,
+                          cudaStream_t s) {
+  using C = SkCfg<NB>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles, a.splits, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = a.splits;   // the K splits of one tile form a cluster
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<NB, EPI>, tw, ta, a);
+  m->launches++;
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+SkinnyArgs skinny_args(nc_model* m, int B, int N, int K, int splits) {
+  SkinnyArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.B = B;
+  a.N = N;
+  a.K = K;
+  a.splits = splits;
+  a.kb_per = K / 64 / splits;
+  a.eps = m->cfg.rms_eps;
+  a.softcap = m->cfg.softcap;
+  a.err = m->err;
+  a.wait_limit_ns = m->wait_limit_ns;
+  return a;
+}
+
+// One decode step of the bf16 model for B <= NB rows on the skinny GEMMs.
+// Every kernel takes the position from the device-side length, so the
+// sequence is the same at every step and can be replayed as a CUDA graph.
+template <int NB>
+nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logits, cudaStream_t s) {
+  const nc_config& c = m->cfg;
+  const int d = c.d_model, nh = c.n_head, F = c.d_mlp, V = c.vocab;
+  const int NQKV = (nh + 2) * 128, NQ = nh * 128;
+  const float eps = c.rms_eps;
+  using bf16 = __nv_bfloat16;
+  {
+    KScope ks(m, NC_K_EMBED, s);
+    embed_rmsnorm_kernel<bf16, bf16><<<blocks_for_warps(B), 256, 0, s>>>(
+        tok, static_cast<const bf16*>(m->E), m->x, static_cast<bf16*>(m->h), B, d, V, eps, m->err, nullptr, 0);
+    m->launches++;
+    NC_TRY(cudaGetLastError());
+  }
+  for (int l = 0; l < c.n_layer; ++l) {
+    {
+      KScope ks(m, NC_K_QKV, s);
+      SkinnyArgs a = skinny_args(m, B, NQKV, d, m->sk_splits[0]);
+      a.out_bf = static_cast<bf16*>(m->q);
+      a.k_cache = static_cast<bf16*>(m->kc(l));
+      a.v_cache = static_cast<bf16*>(m->vc(l));
+      a.rope_cos = m->rope_cos;
+      a.rope_sin = m->rope_sin;
+      a.pos_dev = m->d_len;
+      a.n_head = nh;
+      a.cache_S = c.max_seq;
+      NC_TRY((launch_skinny<NB, EPI_QKV>(m, m->tm_w128[4 * l + 0], m->tm_h_nb, a, NQKV / 128, s)));
+    }
+    {
+      KScope ks(m, NC_K_ATTN, s);
+      attn_decode_mma_kernel<<<dim3(m->max_chunks, B), 128, ATT_DECODE_SMEM, s>>>(
+          static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
+          static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, nh, c.max_seq, 0, m->d_len,
+          kAttnScaleLog2);
+      attn_decode_combine_kernel<<<dim3(nh, B), 128, 0, s>>>(m->part_o, m->part_ml,
+                                                            static_cast<bf16*>(m->att), nh, 0, m->d_len);
+      m->launches += 2;
+      NC_TRY(cudaGetLastError());
+    }
+    {
+      KScope ks(m, NC_K_OPROJ, s);
+      SkinnyArgs a = skinny_args(m, B, d, NQ, m->sk_splits[1]);
+      a.x = m->x;
+      NC_TRY((launch_skinny<NB, EPI_RESID>(m, m->tm_w128[4 * l + 1], m->tm_att_nb, a, d / 128, s)));
+    }
+    {
+      KScope ks(m, NC_K_NORM, s);
+      rmsnorm_kernel<bf16><<<blocks_for_warps(B), 256, 0, s>>>(m->x, static_cast<bf16*>(m->h), B, d, 1, 0,
+                                                               eps, nullptr);
+      m->launches++;
+      NC_TRY(cudaGetLastError());
+    }
+    {
+      KScope ks(m, NC_K_FC, s);
+      SkinnyArgs a = skinny_args(m, B, F, d, m->sk_splits[2]);
+      a.out_bf = static_cast<bf16*>(m->u);
+      NC_TRY((launch_skinny<NB, EPI_RELU2>(m, m->tm_w128[4 * l + 2], m->tm_h_nb, a, F / 128, s)));
+    }
+    {
+      KScope ks(m, NC_K_PROJ, s);
+      SkinnyArgs a = skinny_args(m, B, d, F, m->sk_splits[3]);
+      a.x = m->x;
+      NC_TRY((launch_skinny<NB, EPI_RESID>(m, m->tm_w128[4 * l + 3], m->tm_u_nb, a, d / 128, s)));
+    }
+    {
+      KScope ks(m, NC_K_NORM, s);
+      int* len_inc = l == c.n_layer - 1 ? m->d_len : nullptr;
+      rmsnorm_kernel<bf16><<<blocks_for_warps(B), 256, 0, s>>>(m->x, static_cast<bf16*>(m->h), B, d, 1, 0,
+                                                               eps, len_inc);
+      m->launches++;
+      NC_TRY(cudaGetLastError());
+    }
+  }
+  {
+    KScope ks(m, NC_K_LMHEAD, s);
+    SkinnyArgs a = skinny_args(m, B, V, d, 1);
+    a.x = logits;
+    NC_TRY((launch_skinny<NB, EPI_LOGITS>(m, m->tm_wu128, m->tm_h_nb, a, V / 128, s)));
+  }
+  return NC_OK;
+}
+
+bool decode_on_skinny(const nc_model* m, int B) { return m->bf16 && m->sk_nb > 0 && B <= m->sk_nb; }
+
+nc_status forward_decode(nc_model* m, const int32_t* tok, int B, float* logits, cudaStream_t s) {
+  if (!decode_on_skinny(m, B)) return forward(m, tok, B, 1, m->length, logits, false, s);
+  switch (m->sk_nb) {
+    case 32: return forward_decode_nb<32>(m, tok, B, logits, s);
+    case 64: return forward_decode_nb<64>(m, tok, B, logits, s);
+    default: return forward_decode_nb<128>(m, tok, B, logits, s);
+  }
+}
+
+// Decode step through a CUDA graph of the whole step.  The first step with a
+// given (B, logit buffer) runs eagerly; the second captures the
+// step on a model-owned stream; every step is then one graph launch on the
+// caller's stream.  Profiling runs the step eagerly.
+nc_status decode_graph(nc_model* m, const int32_t* tok, int B, float* logits, cudaStream_t s) {
+  if (!decode_on_skinny(m, B) || m->profiling) return forward_decode(m, tok, B, logits, s);
+  // the graph reads the tokens from the model's staging buffer
+  if (tok != m->tok_stage) {
+    NC_TRY(cudaMemcpyAsync(m->tok_stage, tok, (size_t)B * 4, cudaMemcpyDeviceToDevice, s));
+    tok = m->tok_stage;
+  }
+  const bool same = m->g_B == B && m->g_tok == tok && m->g_logits == logits;
+  if (!same) {
+    if (m->g_exec) {
+      cudaGraphExecDestroy(m->g_exec);
+      m->g_exec = nullptr;
+    }
+    m->g_B = B;
+    m->g_tok = tok;
+    m->g_logits = logits;
+    return forward_decode(m, tok, B, logits, s);
+  }
+  if (!m->g_exec) {
+    if (!m->cap_stream) NC_TRY(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
+    const int64_t l0 = m->launches;
+    NC_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+    nc_status st = forward_decode(m, tok, B, logits, m->cap_stream);
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamEndCapture(m->cap_stream, &g);
+    m->g_launches = m->launches - l0;
+    m->launches = l0;
+    if (st != NC_OK) {
+      if (g) cudaGraphDestroy(g);
+      return st;
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+    e = cudaGraphInstantiate(&m->g_exec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) {
+      m->g_exec = nullptr;
+      return from_cuda(e);
+    }
+  }
+  NC_TRY(cudaGraphLaunch(m->g_exec, s));
+  m->launches += m->g_launches;
   return NC_OK;
 }
 
@@ -469,7 +697,8 @@ nc_status run_call(nc_model* m, const int32_t* tokens, int B, int T, int pos0, f
     }
     out_dev = m->logit_stage;
   }
-  nc_status st = forward(m, tok_dev, B, T, pos0, out_dev, last_only, s);
+  nc_status st = pos0 > 0 ? decode_graph(m, tok_dev, B, out_dev, s)
+                          : forward(m, tok_dev, B, T, pos0, out_dev, last_only, s);
   if (st != NC_OK) return st;
   if (host_out) NC_TRY(cudaMemcpyAsync(logits, out_dev, out_bytes, cudaMemcpyDeviceToHost, s));
   return NC_OK;
@@ -643,6 +872,15 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
                                     (int)ATT_DECODE_SMEM));
   }
   CREATE_TRY(cudaMalloc(&m->err, sizeof(int)));
+  CREATE_TRY(cudaMalloc(&m->d_len, sizeof(int)));
+  CREATE_TRY(cudaMemset(m->d_len, 0, sizeof(int)));
+  if (m->bf16) {
+    // decode-step skinny GEMMs: batch padded to 32, 64 or 128 columns
+    m->sk_nb = c.max_batch <= 32 ? 32 : (c.max_batch <= 64 ? 64 : 128);
+    const int64_t Ns[4] = {NQKV, d, F, d}, Ks[4] = {d, NQ, d, F};
+    for (int g = 0; g < 4; ++g)
+      m->sk_splits[g] = choose_splits((int)(Ns[g] / 128), (int)(Ks[g] / 64), m->num_sms);
+  }
   CREATE_TRY(cudaMemset(m->h, 0, R * d * m->wbytes));
   CREATE_TRY(cudaMemset(m->att, 0, R * NQ * m->wbytes));
   CREATE_TRY(cudaMemset(m->u, 0, R * F * m->wbytes));
@@ -666,6 +904,14 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
       const uint32_t box[3] = {64, 128, 1};
       ok = ok && make_tmap3(&m->tm_vt, m->vt, dims, strides, box);
     }
+    ok = ok && make_tmap(&m->tm_wu128, m->Wu, V, d, 128) && make_tmap(&m->tm_h_nb, m->h, R, d, m->sk_nb) &&
+         make_tmap(&m->tm_att_nb, m->att, R, NQ, m->sk_nb) && make_tmap(&m->tm_u_nb, m->u, R, F, m->sk_nb);
+    m->tm_w128.resize(4 * c.n_layer);
+    for (int l = 0; ok && l < c.n_layer; ++l)
+      ok = make_tmap(&m->tm_w128[4 * l + 0], m->wqkv[l], NQKV, d, 128) &&
+           make_tmap(&m->tm_w128[4 * l + 1], m->wo[l], d, NQ, 128) &&
+           make_tmap(&m->tm_w128[4 * l + 2], m->wfc[l], F, d, 128) &&
+           make_tmap(&m->tm_w128[4 * l + 3], m->wproj[l], d, F, 128);
     m->tm_kc.resize(c.n_layer);
     for (int l = 0; ok && l < c.n_layer; ++l) {
       const uint64_t dims[3] = {128, (uint64_t)c.max_seq, (uint64_t)c.max_batch};
@@ -747,7 +993,7 @@ nc_status nc_decode_step_noalloc(nc_model* m, const int32_t* tokens, int32_t B, 
   float* const keep_ml = m->part_ml;
   m->part_o = scratch;
   m->part_ml = scratch + (int64_t)B * nchunk * 16 * 128;
-  st = forward(m, tokens, B, 1, m->length, logits, false, stream);
+  st = forward_decode(m, tokens, B, logits, stream);
   m->part_o = keep_o;
   m->part_ml = keep_ml;
   if (st != NC_OK) return st;
