@@ -9,7 +9,8 @@
 // Decode kernel (split over the context): one CTA = one batch row and a
 // chunk of 128 cached keys; the row's n_head query vectors form the 16-row
 // A operand (heads padded to 16), each warp handles 32 keys; partial (max,
-// sum, output) go to a workspace and a combine kernel merges the chunks.
+// sum, output) go to a workspace, and the last CTA of the row to finish
+// (a per-row counter) merges the chunks into the bf16 output.
 #pragma once
 
 #include "nc_common.cuh"
@@ -62,9 +63,12 @@ constexpr int DEC_KPW = DEC_CHUNK / 4;     // keys per warp
 __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kc,
     const __nv_bfloat16* __restrict__ Vc, float* __restrict__ part_o, float* __restrict__ part_ml,
-    int n_head, int cache_S, int ctx, const int* __restrict__ pos_dev, float scale_log2) {
+    __nv_bfloat16* __restrict__ O, int* __restrict__ counters, int n_head, int cache_S, int ctx,
+    const int* __restrict__ pos_dev, float scale_log2) {
+  pdl_trigger();
   // with pos_dev the context is read on the device (the step is graph-replayable);
-  // chunks beyond it exit
+  // the length only changes at the end of a step, so it may be read before
+  // waiting for the previous kernel.  Chunks beyond the context exit.
   if (pos_dev) ctx = *pos_dev + 1;
   const int nchunk = (ctx + DEC_CHUNK - 1) / DEC_CHUNK;
   if ((int)blockIdx.x >= nchunk) return;
@@ -78,16 +82,28 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
   const int chunk_id = blockIdx.x, b = blockIdx.y;
   const int k0 = chunk_id * DEC_CHUNK;
   const int ldq = n_head * ATT_HD;
+  const __nv_bfloat16* kb = Kc + (size_t)b * cache_S * ATT_HD;
+  const __nv_bfloat16* vb = Vc + (size_t)b * cache_S * ATT_HD;
+  // keys before the newest were written by earlier calls: stream them now
+  for (int i = tid; i < DEC_CHUNK * 16; i += 128) {
+    const int r = i >> 4, c = i & 15;
+    const int key = k0 + r;
+    if (key >= ctx - 1) continue;
+    const size_t off = (size_t)key * ATT_HD + c * 8;
+    cp_async16(swz(sK, r, c), kb + off, true);
+    cp_async16(swz(sV, r, c), vb + off, true);
+  }
+  cp_async_commit();
+  pdl_wait();                                                  // q and the newest K/V row
   for (int i = tid; i < 16 * 16; i += 128) {
     const int r = i >> 4, c = i & 15;
     const bool ok = r < n_head;
     cp_async16(swz(sQ, r, c), Q + (size_t)b * ldq + (ok ? r : 0) * ATT_HD + c * 8, ok);
   }
-  const __nv_bfloat16* kb = Kc + (size_t)b * cache_S * ATT_HD;
-  const __nv_bfloat16* vb = Vc + (size_t)b * cache_S * ATT_HD;
   for (int i = tid; i < DEC_CHUNK * 16; i += 128) {
     const int r = i >> 4, c = i & 15;
     const int key = k0 + r;
+    if (key < ctx - 1) continue;
     const bool ok = key < ctx;
     const size_t off = (size_t)(ok ? key : 0) * ATT_HD + c * 8;
     cp_async16(swz(sK, r, c), kb + off, ok);
@@ -210,29 +226,59 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
     part_ml[(pbase + tid) * 2 + 0] = cm;
     part_ml[(pbase + tid) * 2 + 1] = cl;
   }
+
+  // ---- the last chunk CTA of row b to finish merges every chunk (chunk
+  // order fixed, so the result does not depend on which CTA is last)
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&counters[b], 1) == nchunk - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid == 0) counters[b] = 0;                               // ready for the next call
+  float* wts = ored;                                           // [nchunk][16] merge weights
+  float* inv_l = red;                                          // [16]
+  __syncthreads();                                             // ored / red no longer read
+  const size_t rb = (size_t)b * nchunk * 16;
+  if (tid < n_head) {
+    float gm = -INFINITY;
+    for (int c = 0; c < nchunk; ++c) gm = fmaxf(gm, __ldcg(part_ml + (rb + c * 16 + tid) * 2));
+    float l = 0.f;
+    for (int c = 0; c < nchunk; ++c) {
+      const float mc = __ldcg(part_ml + (rb + c * 16 + tid) * 2);
+      const float f = mc == -INFINITY ? 0.f : exp2f(mc - gm);
+      wts[c * 16 + tid] = f;
+      l += __ldcg(part_ml + (rb + c * 16 + tid) * 2 + 1) * f;
+    }
+    inv_l[tid] = 1.f / l;
+  }
+  __syncthreads();
+  // thread = output column; all chunks of two heads requested at once
+  for (int h0 = 0; h0 < n_head; h0 += 2) {
+    float acc[2] = {0.f, 0.f};
+    for (int c0 = 0; c0 < nchunk; c0 += 8) {
+      float o8[2][8];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + i, h = h0 + hh;
+          o8[hh][i] = (c < nchunk && h < n_head) ? __ldcg(part_o + (rb + c * 16 + h) * 128 + tid) : 0.f;
+        }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (c0 + i < nchunk && h0 + hh < n_head) acc[hh] += o8[hh][i] * wts[(c0 + i) * 16 + h0 + hh];
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+      if (h0 + hh < n_head)
+        O[((size_t)b * n_head + h0 + hh) * ATT_HD + tid] = f2bf(acc[hh] * inv_l[h0 + hh]);
+  }
 }
 
 constexpr size_t ATT_DECODE_SMEM = (16 + 2 * DEC_CHUNK) * 256 + 4 * 16 * 2 * 4;
-
-// One CTA per (batch row, head): merge the chunks, write bf16 output.
-__global__ void __launch_bounds__(128) attn_decode_combine_kernel(
-    const float* __restrict__ part_o, const float* __restrict__ part_ml,
-    __nv_bfloat16* __restrict__ O, int n_head, int ctx, const int* __restrict__ pos_dev) {
-  if (pos_dev) ctx = *pos_dev + 1;
-  const int nchunk = (ctx + DEC_CHUNK - 1) / DEC_CHUNK;
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  float gm = -INFINITY;
-  for (int c = 0; c < nchunk; ++c) gm = fmaxf(gm, part_ml[(((size_t)b * nchunk + c) * 16 + h) * 2]);
-  float acc = 0.f, l = 0.f;
-  for (int c = 0; c < nchunk; ++c) {
-    const size_t p = ((size_t)b * nchunk + c) * 16 + h;
-    const float mc = part_ml[p * 2];
-    if (mc == -INFINITY) continue;
-    const float f = exp2f(mc - gm);
-    l += part_ml[p * 2 + 1] * f;
-    acc += part_o[p * 128 + tid] * f;
-  }
-  O[((size_t)b * n_head + h) * ATT_HD + tid] = f2bf(acc / l);
-}
 
 }  // namespace nc

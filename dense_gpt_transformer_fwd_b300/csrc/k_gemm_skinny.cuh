@@ -26,7 +26,9 @@
 //
 // 128 threads: warp 0 lane 0 issues the TMA loads, warp 1 lane 0 the MMAs,
 // then all four warps (warp w reads TMEM lanes 32w..32w+31) run the
-// epilogue.  Every mbarrier wait is bounded.
+// epilogue.  Every mbarrier wait is bounded.  Launched as a programmatic
+// dependent of the previous kernel, the CTA streams its first weight blocks
+// into shared memory before it waits for that kernel's results.
 #pragma once
 
 #include <cuda.h>
@@ -129,14 +131,25 @@ __global__ void __launch_bounds__(128)
     flags[0] = 1;
   };
 
-  bool mma_ok = true;
+  pdl_trigger();
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
+    // weights do not depend on the previous kernel: the first `pre` weight
+    // blocks are requested before waiting for it, their activation blocks after
     int issued[STAGES];
     for (int s = 0; s < STAGES; ++s) issued[s] = -1;
-    uint32_t stage = 0, phase = 0;
+    const int pre = nkb < STAGES ? nkb : STAGES;
+    for (int kb = 0; kb < pre; ++kb) {
+      mbar_arrive_expect_tx(bar(FULL + kb), C::STAGE_BYTES);
+      tma_load_2d(smem_u32(sW + kb * C::W_BYTES), &tmW, bar(FULL + kb), (kb0 + kb) * 64, n0);
+      issued[kb] = 0;
+    }
+    pdl_wait();
+    for (int kb = 0; kb < pre; ++kb)
+      tma_load_2d(smem_u32(sA + kb * C::A_BYTES), &tmA, bar(FULL + kb), (kb0 + kb) * 64, 0);
+    uint32_t stage = pre == STAGES ? 0 : pre, phase = pre == STAGES ? 1 : 0;
     bool ok = true;
-    for (int kb = 0; kb < nkb; ++kb) {
+    for (int kb = pre; kb < nkb; ++kb) {
       if (flags[0] || !mbar_wait(bar(EMPTY + stage), phase ^ 1, limit)) {
         if (!flags[0]) fail();
         ok = false;
@@ -159,7 +172,6 @@ __global__ void __launch_bounds__(128)
     for (int kb = 0; kb < nkb; ++kb) {
       if (flags[0] || !mbar_wait(bar(FULL + stage), phase, limit)) {
         if (!flags[0]) fail();
-        mma_ok = false;
         break;
       }
       tc_fence_after();
@@ -179,6 +191,7 @@ __global__ void __launch_bounds__(128)
   __syncwarp();
 
   // ------------------------------------------------------------- epilogue
+  pdl_wait();                                        // x / positions of the previous kernels
   const bool done_ok = mbar_wait(bar(DONE), 0, limit);
   if (!done_ok && threadIdx.x == 0) fail();
   tc_fence_after();
@@ -224,12 +237,19 @@ __global__ void __launch_bounds__(128)
         const bool is_v = head == args.n_head + 1;
         const int pos = *args.pos_dev;
         for (int b = rank + S * warp; b < args.B; b += 4 * S) {
+          // every partial requested before any is summed (rank order kept)
+          float part[4][8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              part[i][q] = q < S ? ld_dsmem_f32(psm + (b * 128 + lane + 32 * i) * 4, (uint32_t)q) : 0.f;
           float v[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const uint32_t a = psm + (b * 128 + lane + 32 * i) * 4;
             float sum = 0.f;
-            for (int q = 0; q < S; ++q) sum += ld_dsmem_f32(a, (uint32_t)q);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sum += part[i][q];
             v[i] = sum;
           }
           if (!is_v) {
@@ -254,19 +274,35 @@ __global__ void __launch_bounds__(128)
           for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = f2bf(v[i]);
         }
       } else {
-        // rows b = rank, rank + S, ...; thread = column n0 + row (coalesced)
-        for (int b = rank; b < args.B; b += S) {
-          const uint32_t a = psm + (b * 128 + row) * 4;
-          float sum = 0.f;
-          for (int q = 0; q < S; ++q) sum += ld_dsmem_f32(a, (uint32_t)q);
-          const size_t o = (size_t)b * args.N + n0 + row;
-          if constexpr (EPI == EPI_RESID) {
-            args.x[o] += sum;
-          } else if constexpr (EPI == EPI_RELU2) {
-            const float r = fmaxf(sum, 0.f);
-            args.out_bf[o] = f2bf(r * r);
-          } else {
-            args.x[o] = softcap_f(sum, inv_cap, args.softcap);
+        // rows b = rank, rank + S, ...; thread = column n0 + row (coalesced);
+        // four rows at a time with every load issued before the sums
+        for (int b0 = rank; b0 < args.B; b0 += 4 * S) {
+          float part[4][8], xo[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int b = b0 + i * S;
+            const bool in = b < args.B;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              part[i][q] = (in && q < S) ? ld_dsmem_f32(psm + (b * 128 + row) * 4, (uint32_t)q) : 0.f;
+            if constexpr (EPI == EPI_RESID) xo[i] = in ? args.x[(size_t)b * args.N + n0 + row] : 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int b = b0 + i * S;
+            if (b >= args.B) break;
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sum += part[i][q];
+            const size_t o = (size_t)b * args.N + n0 + row;
+            if constexpr (EPI == EPI_RESID) {
+              args.x[o] = xo[i] + sum;
+            } else if constexpr (EPI == EPI_RELU2) {
+              const float r = fmaxf(sum, 0.f);
+              args.out_bf[o] = f2bf(r * r);
+            } else {
+              args.x[o] = softcap_f(sum, inv_cap, args.softcap);
+            }
           }
         }
       }

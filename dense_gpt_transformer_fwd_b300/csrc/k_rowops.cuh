@@ -21,6 +21,8 @@ __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tok, const TW* 
                                      float* __restrict__ x, TA* __restrict__ h, int M, int d,
                                      int vocab, float eps, int* err, int* len_set, int len_val) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
   // the prefill records the cache length on the device for the decode steps
   if (len_set && blockIdx.x == 0 && threadIdx.x == 0) *len_set = len_val;
   if (warp >= M) return;
@@ -55,6 +57,8 @@ template <typename TA>
 __global__ void rmsnorm_kernel(const float* __restrict__ x, TA* __restrict__ h, int rows, int d,
                                int stride, int offset, float eps, int* len_inc) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
   // the final norm of a decode step advances the device-side cache length;
   // every kernel of the step that reads it has finished (stream order)
   if (len_inc && blockIdx.x == 0 && threadIdx.x == 0) *len_inc += 1;

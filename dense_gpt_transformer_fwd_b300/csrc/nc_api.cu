@@ -22,6 +22,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "k_attn_mma.cuh"
@@ -164,6 +165,7 @@ struct nc_model {
   size_t ev_used = 0;
   std::vector<ProfRec> recs;
   int* d_len = nullptr;                // device copy of the cache length (decode reads it)
+  int* att_counters = nullptr;         // decode attention: chunks finished per batch row
   // decode-step skinny GEMMs (bf16, B <= sk_nb)
   int sk_nb = 0;                       // padded batch of the MMA N operand: 32, 64 or 128 (0 = off)
   int sk_splits[4] = {1, 1, 1, 1};     // K splits of QKV, O-proj, FC, PROJ
@@ -202,7 +204,7 @@ void free_model(nc_model* m) {
   void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->k_alloc, m->v_alloc, m->x,
                   m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
                   m->tok_stage, m->logit_stage, m->err, m->part_o, m->part_ml, m->vt,
-                  m->d_len};
+                  m->d_len, m->att_counters};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete m;
@@ -255,6 +257,25 @@ nc_status validate(const nc_config* c) {
     if ((c->head_dim != 64 && c->head_dim != 128) || c->d_model % 32) return NC_ERR_UNSUPPORTED;
   }
   return NC_OK;
+}
+
+// Launch with programmatic stream serialization when `pdl` is set: the
+// kernel may start while the previous kernel in the stream is running and
+// waits for it with griddepcontrol.wait (every kernel of the library does).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(bool pdl, void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
 }
 
 template <int BN, int EPI>
@@ -397,11 +418,9 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
         const int nchunk = (ctx + DEC_CHUNK - 1) / DEC_CHUNK;
         attn_decode_mma_kernel<<<dim3(nchunk, B), 128, ATT_DECODE_SMEM, s>>>(
             static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
-            static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, nh, c.max_seq, ctx, nullptr,
-            kAttnScaleLog2);
-        attn_decode_combine_kernel<<<dim3(nh, B), 128, 0, s>>>(m->part_o, m->part_ml,
-                                                              static_cast<bf16*>(m->att), nh, ctx, nullptr);
-        m->launches += 2;
+            static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, static_cast<bf16*>(m->att),
+            m->att_counters, nh, c.max_seq, ctx, nullptr, kAttnScaleLog2);
+        m->launches++;
         NC_TRY(cudaGetLastError());
       } else {
         attn_simt_kernel<float, float><<<blocks_for_warps((int64_t)M * nh), 256, 0, s>>>(
@@ -503,13 +522,15 @@ cudaError_t launch_skinny(nc_model* m, const CUtensorMap& tw, const CUtensorMap&
   cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = a.splits;   // the K splits of one tile form a cluster
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<NB, EPI>, tw, ta, a);
   m->launches++;
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -563,14 +584,12 @@ nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logit
     }
     {
       KScope ks(m, NC_K_ATTN, s);
-      attn_decode_mma_kernel<<<dim3(m->max_chunks, B), 128, ATT_DECODE_SMEM, s>>>(
-          static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
-          static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, nh, c.max_seq, 0, m->d_len,
-          kAttnScaleLog2);
-      attn_decode_combine_kernel<<<dim3(nh, B), 128, 0, s>>>(m->part_o, m->part_ml,
-                                                            static_cast<bf16*>(m->att), nh, 0, m->d_len);
-      m->launches += 2;
-      NC_TRY(cudaGetLastError());
+      NC_TRY(launch_k(true, attn_decode_mma_kernel, dim3(m->max_chunks, B), dim3(128), ATT_DECODE_SMEM, s,
+                      static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
+                      static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, static_cast<bf16*>(m->att),
+                      m->att_counters, nh, (int)c.max_seq, 0, static_cast<const int*>(m->d_len),
+                      kAttnScaleLog2));
+      m->launches++;
     }
     {
       KScope ks(m, NC_K_OPROJ, s);
@@ -580,10 +599,9 @@ nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logit
     }
     {
       KScope ks(m, NC_K_NORM, s);
-      rmsnorm_kernel<bf16><<<blocks_for_warps(B), 256, 0, s>>>(m->x, static_cast<bf16*>(m->h), B, d, 1, 0,
-                                                               eps, nullptr);
+      NC_TRY(launch_k(true, rmsnorm_kernel<bf16>, dim3(blocks_for_warps(B)), dim3(256), 0, s,
+                      static_cast<const float*>(m->x), static_cast<bf16*>(m->h), B, d, 1, 0, eps, (int*)nullptr));
       m->launches++;
-      NC_TRY(cudaGetLastError());
     }
     {
       KScope ks(m, NC_K_FC, s);
@@ -600,10 +618,9 @@ nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logit
     {
       KScope ks(m, NC_K_NORM, s);
       int* len_inc = l == c.n_layer - 1 ? m->d_len : nullptr;
-      rmsnorm_kernel<bf16><<<blocks_for_warps(B), 256, 0, s>>>(m->x, static_cast<bf16*>(m->h), B, d, 1, 0,
-                                                               eps, len_inc);
+      NC_TRY(launch_k(true, rmsnorm_kernel<bf16>, dim3(blocks_for_warps(B)), dim3(256), 0, s,
+                      static_cast<const float*>(m->x), static_cast<bf16*>(m->h), B, d, 1, 0, eps, len_inc));
       m->launches++;
-      NC_TRY(cudaGetLastError());
     }
   }
   {
@@ -874,6 +891,8 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   CREATE_TRY(cudaMalloc(&m->err, sizeof(int)));
   CREATE_TRY(cudaMalloc(&m->d_len, sizeof(int)));
   CREATE_TRY(cudaMemset(m->d_len, 0, sizeof(int)));
+  CREATE_TRY(cudaMalloc(&m->att_counters, c.max_batch * sizeof(int)));
+  CREATE_TRY(cudaMemset(m->att_counters, 0, c.max_batch * sizeof(int)));
   if (m->bf16) {
     // decode-step skinny GEMMs: batch padded to 32, 64 or 128 columns
     m->sk_nb = c.max_batch <= 32 ? 32 : (c.max_batch <= 64 ? 64 : 128);
