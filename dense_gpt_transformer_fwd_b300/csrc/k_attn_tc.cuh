@@ -35,6 +35,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <type_traits>
 #include "nc_common.cuh"
 
 namespace nc {
@@ -74,6 +75,20 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// 2^x on the FMA pipe, for x <= 127: x = j + f with j = floor(x), f in [0, 1);
+// 2^f from a degree-3 polynomial fitted here to 2^f on [0, 1) (reweighted
+// least squares on Chebyshev nodes, max relative error 8.6e-5, far below the
+// bf16 rounding of P); 2^j is added to the exponent field.  Inputs below
+// -126 are clamped there (2^-126, negligible against the row maximum's 1).
+// Used for a share of the softmax exponentials so that the MUFU unit, which
+// evaluates ex2.approx, is not the only pipe doing that work.
+__device__ __forceinline__ float exp2_poly(float x) {
+  x = fmaxf(x, -126.f);
+  const float j = floorf(x);
+  const float f = x - j;
+  const float p = fmaf(f, fmaf(f, fmaf(f, 0.0770670473575592f, 0.22764497995376587f), 0.6951168179512024f), 1.0f);
+  return __int_as_float(__float_as_int(p) + ((int)j << 23));
 }
 // 32 lanes x 32 consecutive fp32 columns, registers -> TMEM
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
@@ -283,9 +298,16 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
         for (int c = 0; c < 128; ++c)
           if (c > r) v[c] = -INFINITY;
       }
-      float mx = v[0];
+      // row max as a tree (8 independent chains) to keep the latency short
+      float mk[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, v[c]);
+      for (int i = 0; i < 8; ++i) mk[i] = v[i];
+#pragma unroll
+      for (int c = 8; c < 128; c += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mk[i] = fmaxf(mk[i], v[c + i]);
+      const float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
+                             fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
       bool rescale = false;
       float factor = 1.f;
       if (mx > m && (m == -INFINITY || (mx - m) * sl2 > 8.f)) {
@@ -295,20 +317,33 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
         rescale = j > 0;
       }
       const float mb = m * sl2;
-      uint32_t w[64];
-#pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        const float p0 = ex2_approx(fmaf(v[c], sl2, -mb));
-        const float p1 = ex2_approx(fmaf(v[c + 1], sl2, -mb));
-        l += p0 + p1;
-        w[c >> 1] = pack_bf16_2(p0, p1);
-      }
       // P_t of the previous block must have been consumed (and O_t written)
       if (j > 0 && !wait(PVDONE + t, (j - 1) & 1)) { ok = false; break; }
       tc_fence_after();
+      // P = exp2(s * sl2 - m * sl2) in bf16, 8 columns (one 16-byte chunk) at
+      // a time straight into shared memory; row sum in 8 partial sums
+      float lk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // off the diagonal one exponential in four runs on the FMA pipe (the
+      // diagonal block has masked -inf entries: MUFU only)
+      auto emit = [&](auto split_pipes) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        st_shared_v4u(atc_addr(pbuf, r, 8 * k), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+        for (int c = 0; c < 128; c += 8) {
+          float p[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float x = fmaf(v[c + i], sl2, -mb);
+            p[i] = (decltype(split_pipes)::value && (i & 3) == 3) ? exp2_poly(x) : ex2_approx(x);
+            lk[i] += p[i];
+          }
+          st_shared_v4u(atc_addr(pbuf, r, c), pack_bf16_2(p[0], p[1]), pack_bf16_2(p[2], p[3]),
+                        pack_bf16_2(p[4], p[5]), pack_bf16_2(p[6], p[7]));
+        }
+      };
+      if (j == qt)
+        emit(std::false_type{});
+      else
+        emit(std::true_type{});
+      l += ((lk[0] + lk[1]) + (lk[2] + lk[3])) + ((lk[4] + lk[5]) + (lk[6] + lk[7]));
       if (rescale) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {

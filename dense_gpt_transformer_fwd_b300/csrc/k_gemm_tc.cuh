@@ -108,7 +108,37 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, uint32_t src
       : "memory");
 }
 
-template <int BN, int EPI>
+// TMA load of one box, written at the same shared-memory offset of every CTA
+// in `mask` within the cluster; each destination CTA's mbarrier (same offset)
+// receives the completed bytes
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
+      : "memory");
+}
+// arrive on the mbarrier at the same offset in every CTA of `mask` once all
+// previously issued tcgen05.mma of this thread have completed
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          bar),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void cluster_barrier_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// tmB's box is BN/2 rows x 64 columns.
+// MC = true: launched as clusters of two CTAs along M that work on the same
+// weight tile at the same time; each CTA loads half of every W box (BN/2 rows,
+// tmB's box) and multicasts it to both, so each CTA reads a third less from
+// L2 per MMA.  A stage of either CTA is refilled only after both CTAs' MMAs
+// have released it (the MMA commit arrives on both CTAs' empty barrier).
+template <int BN, int EPI, bool MC = false>
 __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
@@ -127,7 +157,14 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_m = (args.M + BM - 1) / BM;
   const int num_n = args.N / BN;
-  const int num_tiles = num_m * num_n;
+  // work units: tiles, or (MC) pairs of vertically adjacent tiles, m fastest
+  const int num_m2 = (num_m + 1) / 2;
+  const int rank = MC ? (int)(blockIdx.x & 1) : 0;
+  const int unit0 = MC ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ustride = MC ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int num_units = MC ? num_m2 * num_n : num_m * num_n;
+  auto unit_m0 = [&](int u) { return MC ? ((u % num_m2) * 2 + rank) * BM : (u % num_m) * BM; };
+  auto unit_n0 = [&](int u) { return MC ? (u / num_m2) * BN : (u / num_m) * BN; };
   const int KB = (args.K + BK - 1) / BK;
   const uint64_t limit = args.wait_limit_ns;
 
@@ -138,7 +175,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar(FULL + s), 1);
-      mbar_init(bar(EMPTY + s), 1);
+      mbar_init(bar(EMPTY + s), MC ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar(TFULL + a), 1);
@@ -156,6 +193,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
+  if constexpr (MC) cluster_barrier_all();        // the peer's barriers are initialised
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -171,8 +209,8 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
       int issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = -1;   // parity of an outstanding load
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m0 = (tile % num_m) * BM, n0 = (tile / num_m) * BN;
+      for (int u = unit0; ok && u < num_units; u += ustride) {
+        const int m0 = unit_m0(u), n0 = unit_n0(u);
         for (int kb = 0; kb < KB; ++kb) {
           if (*abort_flag || !mbar_wait(bar(EMPTY + stage), phase ^ 1, limit)) {
             if (!*abort_flag) fail();
@@ -181,7 +219,15 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
           }
           mbar_arrive_expect_tx(bar(FULL + stage), C::STAGE_BYTES);
           tma_load_2d(smem_u32(sA + stage * C::A_BYTES), &tmA, bar(FULL + stage), kb * BK, m0);
-          tma_load_2d(smem_u32(sB + stage * C::B_BYTES), &tmB, bar(FULL + stage), kb * BK, n0);
+          // W boxes are BN/2 rows; the two halves sit back to back in the stage
+          if constexpr (MC) {
+            tma_load_2d_mc(smem_u32(sB + stage * C::B_BYTES + rank * (C::B_BYTES / 2)), &tmB, bar(FULL + stage),
+                           kb * BK, n0 + rank * (BN / 2), (uint16_t)0x3);
+          } else {
+            tma_load_2d(smem_u32(sB + stage * C::B_BYTES), &tmB, bar(FULL + stage), kb * BK, n0);
+            tma_load_2d(smem_u32(sB + stage * C::B_BYTES + C::B_BYTES / 2), &tmB, bar(FULL + stage), kb * BK,
+                        n0 + BN / 2);
+          }
           issued[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -199,7 +245,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true, any = false;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+      for (int u = unit0; ok && u < num_units; u += ustride, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (*abort_flag || !mbar_wait(bar(TEMPTY + acc), acc_phase ^ 1, limit)) {
@@ -223,7 +269,10 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
             tc_mma_f16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
                        (kb | k) != 0);
           any = true;
-          tc_commit(bar(EMPTY + stage));
+          if constexpr (MC)
+            tc_commit_mc(bar(EMPTY + stage), (uint16_t)0x3);
+          else
+            tc_commit(bar(EMPTY + stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (ok) tc_commit(bar(TFULL + acc));
@@ -243,14 +292,14 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
     const uint32_t buf0 = smem_u32(sE + e * C::EP_BUFS * C::EP_BUF);
     const float inv_cap = 1.0f / args.softcap;
     int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int u = unit0; u < num_units; u += ustride, ++local) {
       const int acc = local & 1;
       if (*abort_flag || !mbar_wait(bar(TFULL + acc), (local >> 1) & 1, limit)) {
         if (!*abort_flag) fail();
         break;
       }
       tc_fence_after();
-      const int m0 = (tile % num_m) * BM, n0 = (tile / num_m) * BN;
+      const int m0 = unit_m0(u), n0 = unit_n0(u);
       const int row0 = m0 + 32 * q;                 // first row of this warp
       const int my_row = row0 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc * BN + ch0;
@@ -416,6 +465,8 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // (MC) no CTA leaves while its peer may still signal its barriers
+  if constexpr (MC) cluster_barrier_all();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }

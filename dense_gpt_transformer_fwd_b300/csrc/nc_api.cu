@@ -108,8 +108,12 @@ bool is_device_ptr(const void* p) {
   return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
+// last CUDA error this thread turned into NC_ERR_CUDA / NC_ERR_OOM
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
 nc_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return NC_OK;
+  g_last_cuda_error = e;
   return e == cudaErrorMemoryAllocation ? NC_ERR_OOM : NC_ERR_CUDA;
 }
 
@@ -185,10 +189,9 @@ struct nc_model {
   float* part_o = nullptr;             // decode attention partials [max_batch][chunks][16][128]
   float* part_ml = nullptr;            // [max_batch][chunks][16][2]
   int max_chunks = 0;
-  // A-operand maps (box 64 x 128), weight maps (box 64 x 256), epilogue maps (box 128 B x 32)
-  CUtensorMap tm_h{}, tm_att{}, tm_u{}, tm_hlast{}, tm_wu{};
+  // A-operand maps (box 64 x 128), epilogue maps (box 128 B x 32); weight maps below
+  CUtensorMap tm_h{}, tm_att{}, tm_u{}, tm_hlast{};
   CUtensorMap tm_q_st{}, tm_x_st{}, tm_u_st{};
-  std::vector<CUtensorMap> tm_wqkv, tm_wo, tm_wfc, tm_wproj;
 
   void* kc(int l) const { return static_cast<char*>(k_alloc) + (kGuardElems + l * layer_elems) * wbytes; }
   void* vc(int l) const { return static_cast<char*>(v_alloc) + (kGuardElems + l * layer_elems) * wbytes; }
@@ -278,21 +281,47 @@ cudaError_t launch_k(bool pdl, void (*k)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
 }
 
+// Prefill GEMM; tb is a weight map with a box of BN/2 rows.  With `mc` (and
+// at least two M tiles) it runs as clusters of two CTAs that share each
+// weight tile through TMA multicast.
 template <int BN, int EPI>
 cudaError_t launch_gemm_tc(nc_model* m, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const CUtensorMap& tc, const GemmArgs& a, cudaStream_t s) {
+                           const CUtensorMap& tc, const GemmArgs& a, cudaStream_t s, bool mc = false) {
   using C = TcCfg<BN, EPI>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int tiles = ((a.M + 127) / 128) * (a.N / BN);
-  if (tiles == 0) return cudaSuccess;
+  const int num_m = (a.M + 127) / 128, num_n = a.N / BN;
+  if (num_m * num_n == 0) return cudaSuccess;
+  if (mc && num_m >= 2) {
+    const int units = ((num_m + 1) / 2) * num_n;
+    const int pairs = units < m->num_sms / 2 ? units : m->num_sms / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, true>, ta, tb, tc, a);
+    m->launches++;
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+  const int tiles = num_m * num_n;
   const int grid = tiles < m->num_sms ? tiles : m->num_sms;
-  gemm_tc_kernel<BN, EPI><<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tc, a);
+  gemm_tc_kernel<BN, EPI, false><<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tc, a);
   m->launches++;
   return cudaGetLastError();
 }
@@ -385,7 +414,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
           a.vt = static_cast<bf16*>(m->vt);
           a.vt_S = m->vt_S;
         }
-        NC_TRY((launch_gemm_tc<256, EPI_QKV>(m, m->tm_h, m->tm_wqkv[l], m->tm_q_st, a, s)));
+        NC_TRY((launch_gemm_tc<256, EPI_QKV>(m, m->tm_h, m->tm_w128[4 * l + 0], m->tm_q_st, a, s, true)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_STORE>(m, static_cast<const float*>(m->h),
                                             static_cast<const float*>(m->wqkv[l]), m->c32, M, NQKV,
@@ -435,7 +464,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       KScope ks(m, NC_K_OPROJ, s);
       if (bf) {
         GemmArgs a = base_args(m, M, d, NQ);
-        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_att, m->tm_wo[l], m->tm_x_st, a, s)));
+        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_att, m->tm_w128[4 * l + 1], m->tm_x_st, a, s, true)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->att),
                                             static_cast<const float*>(m->wo[l]), m->x, M, d, NQ, d, s));
@@ -456,7 +485,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       KScope ks(m, NC_K_FC, s);
       if (bf) {
         GemmArgs a = base_args(m, M, F, d);
-        NC_TRY((launch_gemm_tc<256, EPI_RELU2>(m, m->tm_h, m->tm_wfc[l], m->tm_u_st, a, s)));
+        NC_TRY((launch_gemm_tc<256, EPI_RELU2>(m, m->tm_h, m->tm_w128[4 * l + 2], m->tm_u_st, a, s, true)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RELU2>(m, static_cast<const float*>(m->h),
                                             static_cast<const float*>(m->wfc[l]),
@@ -467,7 +496,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       KScope ks(m, NC_K_PROJ, s);
       if (bf) {
         GemmArgs a = base_args(m, M, d, F);
-        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_u, m->tm_wproj[l], m->tm_x_st, a, s)));
+        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_u, m->tm_w128[4 * l + 3], m->tm_x_st, a, s, true)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->u),
                                             static_cast<const float*>(m->wproj[l]), m->x, M, d, F, d, s));
@@ -496,7 +525,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       GemmArgs a = base_args(m, out_rows, V, d);
       CUtensorMap tm_out;
       if (!make_tmap(&tm_out, logits, out_rows, V, 32, true)) return NC_ERR_INVALID_ARG;
-      NC_TRY((launch_gemm_tc<256, EPI_LOGITS>(m, last_only ? m->tm_hlast : m->tm_h, m->tm_wu, tm_out, a, s)));
+      NC_TRY((launch_gemm_tc<256, EPI_LOGITS>(m, last_only ? m->tm_hlast : m->tm_h, m->tm_wu128, tm_out, a, s, true)));
     } else {
       NC_TRY(launch_simt_gemm<SEPI_LOGITS>(
           m, static_cast<const float*>(last_only ? m->h_last : m->h),
@@ -755,6 +784,10 @@ nc_status noalloc_scratch(int device, float** out) {
 
 extern "C" {
 
+const char* nc_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
+}
+
 const char* nc_status_string(nc_status s) {
   switch (s) {
     case NC_OK: return "ok";
@@ -910,13 +943,8 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
     bool ok = make_tmap(&m->tm_h, m->h, R, d, 128) && make_tmap(&m->tm_att, m->att, R, NQ, 128) &&
               make_tmap(&m->tm_u, m->u, R, F, 128) &&
               make_tmap(&m->tm_hlast, m->h_last, c.max_batch, d, 128) &&
-              make_tmap(&m->tm_wu, m->Wu, V, d, 256) &&
               make_tmap(&m->tm_q_st, m->q, R, NQ, 32) && make_tmap(&m->tm_u_st, m->u, R, F, 32) &&
               make_tmap(&m->tm_x_st, m->x, R, d, 32, true);
-    m->tm_wqkv.resize(c.n_layer);
-    m->tm_wo.resize(c.n_layer);
-    m->tm_wfc.resize(c.n_layer);
-    m->tm_wproj.resize(c.n_layer);
     {
       const uint64_t dims[3] = {(uint64_t)m->vt_S, 128, (uint64_t)c.max_batch};
       const uint64_t strides[2] = {(uint64_t)m->vt_S * 2, (uint64_t)m->vt_S * 256};
@@ -938,11 +966,6 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
       const uint32_t box[3] = {64, 128, 1};
       ok = make_tmap3(&m->tm_kc[l], m->kc(l), dims, strides, box);
     }
-    for (int l = 0; ok && l < c.n_layer; ++l)
-      ok = make_tmap(&m->tm_wqkv[l], m->wqkv[l], NQKV, d, 256) &&
-           make_tmap(&m->tm_wo[l], m->wo[l], d, NQ, 256) &&
-           make_tmap(&m->tm_wfc[l], m->wfc[l], F, d, 256) &&
-           make_tmap(&m->tm_wproj[l], m->wproj[l], d, F, 256);
     if (!ok) {
       free_model(m);
       return NC_ERR_CUDA;
@@ -1063,12 +1086,14 @@ nc_status nc_gemm_bf16(nc_model* m, const void* A, const void* W, float* C, int3
                        int32_t K, nc_stream_t stream) {
   if (!m || !A || !W || !C || M < 1 || N < 256 || K < 8 || N % 256 || K % 8) return NC_ERR_INVALID_ARG;
   if (!is_device_ptr(A) || !is_device_ptr(W) || !is_device_ptr(C)) return NC_ERR_INVALID_ARG;
+  // M > 128 runs the two-CTA multicast path (the one the prefill uses)
+  const bool mc = M > 128;
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, A, M, K, 128) || !make_tmap(&tb, W, N, K, 256)) return NC_ERR_INVALID_ARG;
+  if (!make_tmap(&ta, A, M, K, 128) || !make_tmap(&tb, W, N, K, 128)) return NC_ERR_INVALID_ARG;
   CUtensorMap tc;
   if (!make_tmap(&tc, C, M, N, 32, true)) return NC_ERR_INVALID_ARG;
   GemmArgs a = base_args(m, M, N, K);
-  NC_TRY((launch_gemm_tc<256, EPI_STORE>(m, ta, tb, tc, a, stream)));
+  NC_TRY((launch_gemm_tc<256, EPI_STORE>(m, ta, tb, tc, a, stream, mc)));
   return NC_OK;
 }
 

@@ -24,10 +24,10 @@ STATUS = {0: "NC_OK", 1: "NC_ERR_INVALID_ARG", 2: "NC_ERR_UNSUPPORTED", 3: "NC_E
 
 
 class NcError(RuntimeError):
-    def __init__(self, code: int, what: str):
+    def __init__(self, code: int, what: str, detail: str = ""):
         self.code = code
         self.name = STATUS.get(code, str(code))
-        super().__init__(f"{what}: {self.name}")
+        super().__init__(f"{what}: {self.name}" + (f" ({detail})" if detail else ""))
 
 
 class NcConfig(ctypes.Structure):
@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
         "nc_profile_begin": ([P], S),
         "nc_profile_end": ([P, P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)], S),
         "nc_status_string": ([S], ctypes.c_char_p),
+        "nc_last_cuda_error": ([], ctypes.c_char_p),
     }
     for name, (argt, rest) in sig.items():
         f = getattr(L, name)
@@ -86,7 +87,10 @@ def lib() -> ctypes.CDLL:
 
 def _check(code: int, what: str):
     if code != 0:
-        raise NcError(code, what)
+        detail = ""
+        if STATUS.get(code) in ("NC_ERR_CUDA", "NC_ERR_OOM") and _lib is not None:
+            detail = _lib.nc_last_cuda_error().decode()
+        raise NcError(code, what, detail)
 
 
 def _stream(stream):

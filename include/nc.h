@@ -225,6 +225,13 @@ NC_API nc_status nc_profile_end(nc_model* m, nc_stream_t stream, double* ms, int
 /* Static description of a status code. */
 NC_API const char* nc_status_string(nc_status s);
 
+/*
+ * Description of the CUDA runtime error behind the last NC_ERR_CUDA or
+ * NC_ERR_OOM returned on the calling thread ("no error" if none).  The
+ * string is static; the state is per host thread.
+ */
+NC_API const char* nc_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif
