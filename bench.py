@@ -20,8 +20,8 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import hashlib
 import statistics
-import subprocess
 import sys
 import time
 
@@ -71,57 +71,102 @@ def decode_bytes(s, B, ctx):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons of one GPU, read through NVML every
+    10 ms by a background thread while the timed region runs.  Read only: no
+    GPU setting is changed."""
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
+               ("hw_power_brake", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = os.path.join("/tmp", f"nc_clocks_{os.getpid()}.csv")
+    def __init__(self, gpu_index, period_s=0.01):
+        self.gpu, self.period = gpu_index, period_s
+        self.sm, self.bits, self.mx, self.nv = [], 0, None, None
 
     def __enter__(self):
+        import threading
         try:
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+            import pynvml as nv
+            nv.nvmlInit()
+            self.nv = nv
+            self.h = self._handle(nv)
+            self.mx = float(nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM))
+            self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception:
+            self.nv = None
+            return self
+        self.stop = threading.Event()
+        self.th = threading.Thread(target=self._loop, daemon=True)
+        self.th.start()
         return self
 
-    def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
+    def _handle(self, nv):
+        # NVML numbers every GPU of the machine; find this process's device
+        # (CUDA index self.gpu) by its UUID
+        import torch
+        uuid = str(torch.cuda.get_device_properties(self.gpu).uuid)
+        for name in (uuid, "GPU-" + uuid):
             try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-            self.f.close()
+                return nv.nvmlDeviceGetHandleByUUID(name)
+            except Exception:
+                pass
+        return nv.nvmlDeviceGetHandleByIndex(self.gpu)
+
+    def _loop(self):
+        nv = self.nv
+        while not self.stop.is_set():
+            try:
+                self.sm.append(float(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)))
+                self.bits |= int(self.reasons_fn(self.h))
+            except Exception:
+                pass
+            self.stop.wait(self.period)
+
+    def __exit__(self, *a):
+        if self.nv is not None:
+            self.stop.set()
+            self.th.join(timeout=2)
+            try:
+                self.nv.nvmlShutdown()
+            except Exception:
+                pass
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
+        if self.nv is None or not self.sm:
             return None
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            p = [t.strip() for t in line.split(",")]
-            if len(p) < 9:
-                continue
+        reasons = sorted(n for n, c in self.REASONS if hasattr(self.nv, c) and self.bits & getattr(self.nv, c))
+        return {"sm_mhz": statistics.median(self.sm), "sm_max_mhz": self.mx, "reasons": reasons,
+                "samples": len(self.sm)}
+
+
+# DRAM traffic per launch of the dominant kernel, from the ncu captures
+# summarised in profiles/traffic.md: | class | workload | bytes | source | sha256 |.
+# The figure is used only while the kernel's source still hashes the same.
+KCLASS_SOURCE = {"lm_head": "k_gemm_tc.cuh", "qkv": "k_gemm_tc.cuh", "oproj": "k_gemm_tc.cuh",
+                 "fc": "k_gemm_tc.cuh", "proj": "k_gemm_tc.cuh", "attn": "k_attn_tc.cuh"}
+
+
+def source_sha256(name):
+    path = os.path.join(ROOT, "dense_gpt_transformer_fwd_b300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(kclass, workload):
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    src = KCLASS_SOURCE.get(kclass)
+    if src is None or not os.path.exists(path):
+        return None
+    for line in open(path):
+        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+        if len(cells) == 5 and cells[0] == kclass and cells[1] == workload and cells[3] == src:
             try:
-                sm.append(float(p[1]))
-                mx = float(p[2])
+                return float(cells[2]) if cells[4] == source_sha256(src) else None
             except ValueError:
-                continue
-            for n, v in zip(names, p[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        os.unlink(self.path)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                return None
+    return None
 
 
 def blas_threads():
@@ -304,10 +349,43 @@ def bench_decode(args, w, flat, prompt, nxt, steps=None):
     return {"ms": ms, "launches": launches, "bytes": float(byts), "ctx_mean": ctx_mean}
 
 
+def run_case(args):
+    """A plain run of the workload for profilers: warmup + steps iterations."""
+    import torch
+    import dense_gpt_transformer_fwd_b300 as ncp
+    from dense_gpt_transformer_fwd_b300 import build
+    build.build()
+    w = nc_inputs.WORKLOADS[args.config]
+    B, T = args.batch or w.batch, args.seq or w.prompt_len
+    flat = nc_inputs.gen_weights(w.shape, w.weight_seed)
+    prompt = nc_inputs.gen_tokens(w.shape.vocab, (B, T), w.prompt_seed)
+    n = args.warmup + args.steps
+    if args.case == "prefill":
+        m = ncp.Model(w.shape, flat, max_batch=B, max_seq=T)
+        tok = torch.from_numpy(prompt).cuda()
+        out = torch.empty((B * T, w.shape.vocab), dtype=torch.float32, device="cuda")
+        for _ in range(n):
+            m.kv_reset()
+            m.prefill(tok, out=out)
+    else:
+        steps = max(n, 1)
+        nxt = nc_inputs.gen_tokens(w.shape.vocab, (steps, B), (w.decode_seed or 0) + 1)
+        m = ncp.Model(w.shape, flat, max_batch=B, max_seq=T + steps)
+        m.prefill(torch.from_numpy(prompt).cuda(), last_only=True)
+        nd = torch.from_numpy(nxt).cuda()
+        out = torch.empty((B, w.shape.vocab), dtype=torch.float32, device="cuda")
+        for t in range(steps):
+            m.decode_step(nd[t], out=out)
+    m.sync()
+    print(json.dumps({"case": args.case, "workload": w.name, "batch": B, "seq": T, "iterations": n,
+                      "launches": m.launch_count}))
+    m.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="d12_prefill", choices=sorted(nc_inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -316,7 +394,13 @@ def main():
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--seq", type=int, default=None, help="override the workload's prompt length")
+    ap.add_argument("--case", choices=["prefill", "decode"], default=None,
+                    help="profiling case: run only --warmup + --steps iterations of the workload "
+                         "(no timing passes, no oracle) and print one short line; for ncu captures")
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
 
@@ -360,7 +444,8 @@ def main():
         if dom in flops:
             ach = flops[dom] / (prof[dom][0] / 1e3) / 1e12
             roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": peak,
-                    "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+                    "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                    "traffic": measured_traffic(dom, w.name),
                     "peak_source": f"{peak_src} bf16 dense (burst)"}
         else:
             roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": peaks["hbm_gbs"],
