@@ -35,7 +35,6 @@
 #pragma once
 
 #include <cuda.h>
-#include <type_traits>
 #include "nc_common.cuh"
 
 namespace nc {
@@ -51,8 +50,7 @@ constexpr int ATC_THREADS = 320;
 constexpr uint32_t ATC_HALF = 16384;                 // 128 rows x 128 B
 constexpr uint32_t ATC_TILE = 2 * ATC_HALF;          // 128 rows x 128 bf16
 constexpr uint32_t ATC_OFF_Q = 0;                    // 2 tiles
-constexpr uint32_t ATC_OFF_K = 2 * ATC_TILE;         // 2 stages
-constexpr uint32_t ATC_OFF_V = 4 * ATC_TILE;         // 1 stage
+constexpr uint32_t ATC_OFF_KV = 2 * ATC_TILE;        // ring of 3 slots: K_0 V_0 K_1 V_1 ...
 constexpr uint32_t ATC_OFF_P = 5 * ATC_TILE;         // 2 tiles
 constexpr uint32_t ATC_OFF_BAR = 7 * ATC_TILE;
 constexpr size_t ATC_SMEM = 1024 + 7 * (size_t)ATC_TILE + 256;
@@ -75,20 +73,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-// 2^x on the FMA pipe, for x <= 127: x = j + f with j = floor(x), f in [0, 1);
-// 2^f from a degree-3 polynomial fitted here to 2^f on [0, 1) (reweighted
-// least squares on Chebyshev nodes, max relative error 8.6e-5, far below the
-// bf16 rounding of P); 2^j is added to the exponent field.  Inputs below
-// -126 are clamped there (2^-126, negligible against the row maximum's 1).
-// Used for a share of the softmax exponentials so that the MUFU unit, which
-// evaluates ex2.approx, is not the only pipe doing that work.
-__device__ __forceinline__ float exp2_poly(float x) {
-  x = fmaxf(x, -126.f);
-  const float j = floorf(x);
-  const float f = x - j;
-  const float p = fmaf(f, fmaf(f, fmaf(f, 0.0770670473575592f, 0.22764497995376587f), 0.6951168179512024f), 1.0f);
-  return __int_as_float(__float_as_int(p) + ((int)j << 23));
 }
 // 32 lanes x 32 consecutive fp32 columns, registers -> TMEM
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
@@ -131,8 +115,8 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   auto bar = [&](int i) { return smem_u32(bars + i); };
   // barrier indices
-  const int QFULL = 0, KFULL = 1, KFREE = 3, VFULL = 5, VFREE = 6, SFULL = 7, SFREE = 9,
-            PFULL = 11, PVDONE = 13, DRAIN = 15;
+  const int QFULL = 0, KVFULL = 1, KVFREE = 4, SFULL = 7, SFREE = 9, PFULL = 11, PVDONE = 13,
+            DRAIN = 15;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pairs = args.n_head >> 1;
@@ -147,16 +131,16 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(QFULL), 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(bar(KVFULL + i), 1);
+      mbar_init(bar(KVFREE + i), 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(KFULL + i), 1);
-      mbar_init(bar(KFREE + i), 1);
       mbar_init(bar(SFULL + i), 1);
       mbar_init(bar(SFREE + i), 128);
       mbar_init(bar(PFULL + i), 128);
       mbar_init(bar(PVDONE + i), 1);
     }
-    mbar_init(bar(VFULL), 1);
-    mbar_init(bar(VFREE), 1);
     mbar_init(bar(DRAIN), 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -186,34 +170,35 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // tiles K_0, V_0, K_1, V_1, ... go round a ring of three slots: slot of
+    // tile i is i % 3, so V_{j+1} reuses the slot of K_j (free once both
+    // heads' S_j are done) and is in flight long before P V_{j+1} needs it
     if (lane == 0) {
       bool ok = true;
-      int kin[2] = {-1, -1}, vin = -1;               // parity of loads in flight
+      int inflight[3] = {-1, -1, -1};                // parity of loads in flight
       mbar_arrive_expect_tx(bar(QFULL), 2 * ATC_TILE);
       for (int t = 0; t < 2; ++t)
         for (int h = 0; h < 2; ++h)
           tma_load_3d(s0 + ATC_OFF_Q + t * ATC_TILE + h * ATC_HALF, &tmQ, bar(QFULL),
                       (2 * hp + t) * 128 + 64 * h, q0, b);
-      for (int j = 0; ok && j < nb; ++j) {
-        const int ks = j & 1;
-        if (!wait(KFREE + ks, ((j >> 1) & 1) ^ 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(KFULL + ks), ATC_TILE);
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(s0 + ATC_OFF_K + ks * ATC_TILE + h * ATC_HALF, &tmK, bar(KFULL + ks), 64 * h,
-                      j * 128, b);
-        kin[ks] = (j >> 1) & 1;
-        if (!wait(VFREE, (j & 1) ^ 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(VFULL), ATC_TILE);
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(s0 + ATC_OFF_V + h * ATC_HALF, &tmVt, bar(VFULL), j * 128 + 64 * h, 0, b);
-        vin = j & 1;
+      for (int i = 0; ok && i < 2 * nb; ++i) {
+        const int slot = i % 3, round = i / 3, j = i >> 1;
+        if (!wait(KVFREE + slot, (round & 1) ^ 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(KVFULL + slot), ATC_TILE);
+        const uint32_t dst = s0 + ATC_OFF_KV + slot * ATC_TILE;
+        for (int h = 0; h < 2; ++h) {
+          if ((i & 1) == 0)
+            tma_load_3d(dst + h * ATC_HALF, &tmK, bar(KVFULL + slot), 64 * h, j * 128, b);
+          else
+            tma_load_3d(dst + h * ATC_HALF, &tmVt, bar(KVFULL + slot), j * 128 + 64 * h, 0, b);
+        }
+        inflight[slot] = round & 1;
       }
       if (!ok) {
         // let every copy still in flight land before the CTA exits
         mbar_wait(bar(QFULL), 0, limit);
-        for (int s = 0; s < 2; ++s)
-          if (kin[s] >= 0) mbar_wait(bar(KFULL + s), (uint32_t)kin[s], limit);
-        if (vin >= 0) mbar_wait(bar(VFULL), (uint32_t)vin, limit);
+        for (int sl = 0; sl < 3; ++sl)
+          if (inflight[sl] >= 0) mbar_wait(bar(KVFULL + sl), (uint32_t)inflight[sl], limit);
       }
     }
   } else if (warp == 1) {
@@ -223,7 +208,7 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
       auto issue_s = [&](int t, int ks) {
-        const uint32_t qa = s0 + ATC_OFF_Q + t * ATC_TILE, ka = s0 + ATC_OFF_K + ks * ATC_TILE;
+        const uint32_t qa = s0 + ATC_OFF_Q + t * ATC_TILE, ka = s0 + ATC_OFF_KV + ks * ATC_TILE;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * ATC_HALF + (kk & 3) * 32;
@@ -232,7 +217,7 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
         tc_commit(bar(SFULL + t));
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t pa = s0 + ATC_OFF_P + t * ATC_TILE, va = s0 + ATC_OFF_V;
+        const uint32_t pa = s0 + ATC_OFF_P + t * ATC_TILE, va = s0 + ATC_OFF_KV + ((2 * j + 1) % 3) * ATC_TILE;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * ATC_HALF + (kk & 3) * 32;
@@ -241,29 +226,30 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
         }
         tc_commit(bar(PVDONE + t));
       };
-      bool ok = wait(QFULL, 0) && wait(KFULL + 0, 0), any = false;
+      // K_j is ring tile 2j, V_j ring tile 2j + 1 (slot i % 3, phase (i / 3) & 1)
+      bool ok = wait(QFULL, 0) && wait(KVFULL + 0, 0), any = false;
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
         issue_s(1, 0);
-        tc_commit(bar(KFREE + 0));
+        tc_commit(bar(KVFREE + 0));
         any = true;
       }
       for (int j = 0; ok && j < nb; ++j) {
         const bool more = j + 1 < nb;
-        const int ks1 = (j + 1) & 1;
-        if (!wait(VFULL, j & 1)) { ok = false; break; }
+        const int iv = 2 * j + 1, ik = 2 * j + 2;
+        if (!wait(KVFULL + iv % 3, (iv / 3) & 1)) { ok = false; break; }
         for (int t = 0; ok && t < 2; ++t) {
           if (!wait(PFULL + t, j & 1)) { ok = false; break; }
           tc_fence_after();
           issue_pv(t, j);
-          if (t == 1) tc_commit(bar(VFREE));
+          if (t == 1) tc_commit(bar(KVFREE + iv % 3));
           if (more) {
-            if (t == 0 && !wait(KFULL + ks1, ((j + 1) >> 1) & 1)) { ok = false; break; }
+            if (t == 0 && !wait(KVFULL + ik % 3, (ik / 3) & 1)) { ok = false; break; }
             if (!wait(SFREE + t, j & 1)) { ok = false; break; }
             tc_fence_after();
-            issue_s(t, ks1);
-            if (t == 1) tc_commit(bar(KFREE + ks1));
+            issue_s(t, ik % 3);
+            if (t == 1) tc_commit(bar(KVFREE + ik % 3));
           }
         }
       }
@@ -323,26 +309,17 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
       // P = exp2(s * sl2 - m * sl2) in bf16, 8 columns (one 16-byte chunk) at
       // a time straight into shared memory; row sum in 8 partial sums
       float lk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      // off the diagonal one exponential in four runs on the FMA pipe (the
-      // diagonal block has masked -inf entries: MUFU only)
-      auto emit = [&](auto split_pipes) {
 #pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-          float p[8];
+      for (int c = 0; c < 128; c += 8) {
+        float p[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float x = fmaf(v[c + i], sl2, -mb);
-            p[i] = (decltype(split_pipes)::value && (i & 3) == 3) ? exp2_poly(x) : ex2_approx(x);
-            lk[i] += p[i];
-          }
-          st_shared_v4u(atc_addr(pbuf, r, c), pack_bf16_2(p[0], p[1]), pack_bf16_2(p[2], p[3]),
-                        pack_bf16_2(p[4], p[5]), pack_bf16_2(p[6], p[7]));
+        for (int i = 0; i < 8; ++i) {
+          p[i] = ex2_approx(fmaf(v[c + i], sl2, -mb));
+          lk[i] += p[i];
         }
-      };
-      if (j == qt)
-        emit(std::false_type{});
-      else
-        emit(std::true_type{});
+        st_shared_v4u(atc_addr(pbuf, r, c), pack_bf16_2(p[0], p[1]), pack_bf16_2(p[2], p[3]),
+                      pack_bf16_2(p[4], p[5]), pack_bf16_2(p[6], p[7]));
+      }
       l += ((lk[0] + lk[1]) + (lk[2] + lk[3])) + ((lk[4] + lk[5]) + (lk[6] + lk[7]));
       if (rescale) {
 #pragma unroll 1

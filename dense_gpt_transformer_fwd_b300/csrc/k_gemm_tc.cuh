@@ -20,8 +20,9 @@
 //                 buffer and written by TMA bulk tensor stores.  The residual
 //                 epilogue uses the TMA reduce-add store, so x += acc happens
 //                 in L2 without reading x into the SM.
-// Tiles are visited m-fastest so that CTAs resident at the same time share
-// the W tile (and the whole A panel stays in L2).
+// Tiles are visited m-fastest, so that CTAs resident at the same time share
+// the W tile, or n-fastest when the A operand is the larger one (it is then
+// read from DRAM once while the W tiles stay in L2).
 #pragma once
 
 #include <cuda.h>
@@ -50,6 +51,9 @@ struct GemmArgs {
   float eps;
   // EPI_LOGITS
   float softcap;
+  // tile order: 0 = m fastest (CTAs running together share a W tile),
+  // 1 = n fastest (they share an A panel, each read from DRAM once)
+  int n_fast;
   // error reporting
   int* err;
   unsigned long long wait_limit_ns;
@@ -163,8 +167,11 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
   const int unit0 = MC ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int ustride = MC ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const int num_units = MC ? num_m2 * num_n : num_m * num_n;
-  auto unit_m0 = [&](int u) { return MC ? ((u % num_m2) * 2 + rank) * BM : (u % num_m) * BM; };
-  auto unit_n0 = [&](int u) { return MC ? (u / num_m2) * BN : (u / num_m) * BN; };
+  const int num_mu = MC ? num_m2 : num_m;          // m positions of a unit
+  auto unit_m = [&](int u) { return args.n_fast ? u / num_n : u % num_mu; };
+  auto unit_n = [&](int u) { return args.n_fast ? u % num_n : u / num_mu; };
+  auto unit_m0 = [&](int u) { return MC ? (unit_m(u) * 2 + rank) * BM : unit_m(u) * BM; };
+  auto unit_n0 = [&](int u) { return unit_n(u) * BN; };
   const int KB = (args.K + BK - 1) / BK;
   const uint64_t limit = args.wait_limit_ns;
 

@@ -352,6 +352,7 @@ GemmArgs base_args(nc_model* m, int M, int N, int K) {
   a.wait_limit_ns = m->wait_limit_ns;
   a.eps = m->cfg.rms_eps;
   a.softcap = m->cfg.softcap;
+  a.n_fast = (int64_t)M * K >= (int64_t)N * K;   // the A operand is at least as large as W
   return a;
 }
 
