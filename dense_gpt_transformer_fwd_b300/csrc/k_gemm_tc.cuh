@@ -59,16 +59,22 @@ struct GemmArgs {
   unsigned long long wait_limit_ns;
 };
 
-template <int BN, int EPI>
+// CL = 0: one CTA per tile; 1: pairs sharing W by multicast; 2: CTA pairs
+// computing a 256 x BN tile with tcgen05.mma.cta_group::2 (each CTA holds its
+// 128 rows of A and half of the W tile)
+template <int BN, int EPI, int CL = 0>
 struct TcCfg {
-  static constexpr int BM = 128, BK = 64;
+  // K per pipeline stage: 128 (two 64-column boxes per operand) for CTA pairs,
+  // which halves the per-stage barrier and commit work per FLOP
+  static constexpr int BM = 128, BK = CL == 2 ? 128 : 64;
+  static constexpr int KBOX = BK / 64;                 // 64-column TMA boxes per operand
   static constexpr int EPI_WARPS = 8;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   // the QKV epilogue stages both halves of a head (RoPE pairs dims j, j+64)
   static constexpr int EP_BUFS = EPI == EPI_QKV ? 2 : 1;
   static constexpr uint32_t EP_BUF = 4096;             // 32 rows x 128 B
   static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t B_BYTES = (CL == 2 ? BN / 2 : BN) * BK * 2;   // W rows held by this CTA
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr size_t EP_TOTAL = (size_t)EPI_WARPS * EP_BUFS * EP_BUF;
   static constexpr size_t SMEM_CAP = 232448 - 1024 - 256;
@@ -132,6 +138,54 @@ __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
       "h"(mask)
       : "memory");
 }
+// ------------------------------------------------- CTA-pair (cta_group::2)
+// Tensor memory is allocated and freed collectively by one warp of each CTA
+// of the pair; the address is written to each CTA's shared memory.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// TMA load into this CTA's shared memory whose completed bytes are counted on
+// an mbarrier of either CTA of the pair (bar is a shared::cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+// D[256 x N] (+)= A[256 x 16] B[N x 16]^T across the pair: rows 0..127 of A and
+// D live in the issuing CTA, rows 128..255 in its peer (same addresses); B's
+// first N/2 rows in the issuing CTA, the rest in the peer
+__device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          bar),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local_smem, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 __device__ __forceinline__ void cluster_barrier_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -142,11 +196,21 @@ __device__ __forceinline__ void cluster_barrier_all() {
 // tmB's box) and multicasts it to both, so each CTA reads a third less from
 // L2 per MMA.  A stage of either CTA is refilled only after both CTAs' MMAs
 // have released it (the MMA commit arrives on both CTAs' empty barrier).
-template <int BN, int EPI, bool MC = false>
-__global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
+// CL = 2: launched as clusters of two CTAs along M.  The even CTA (the
+// leader) issues tcgen05.mma.cta_group::2 for the 256-row tile of the pair;
+// each CTA loads its own 128 rows of A and BN/2 rows of W, and both CTAs'
+// loads count on the leader's full barrier.  The
+// leader's MMA commits arrive on both CTAs' empty and tfull barriers; both
+// CTAs' epilogue warps release an accumulator on the leader's tempty barrier.
+// Each CTA now needs 32 KB of shared memory per 64-wide K block instead of
+// 48 KB, so the ring holds 6 stages and covers the load latency.
+template <int BN, int EPI, int CL = 0>
+__global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
-  using C = TcCfg<BN, EPI>;
+  constexpr bool MC = CL != 0;                     // tiles come in vertical pairs
+  constexpr bool PAIR = CL == 2;
+  using C = TcCfg<BN, EPI, CL>;
   constexpr int BM = C::BM, BK = C::BK, STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -182,11 +246,11 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar(FULL + s), 1);
-      mbar_init(bar(EMPTY + s), MC ? 2 : 1);
+      mbar_init(bar(EMPTY + s), CL == 1 ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar(TFULL + a), 1);
-      mbar_init(bar(TEMPTY + a), 32 * C::EPI_WARPS);
+      mbar_init(bar(TEMPTY + a), PAIR ? 2 * C::EPI_WARPS : 32 * C::EPI_WARPS);
     }
     mbar_init(bar(DRAIN), 1);
     *abort_flag = 0;
@@ -197,10 +261,19 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  if constexpr (MC) {
+    // the peer's barriers are initialised before any remote arrive or copy
+    __syncthreads();
+    cluster_barrier_all();
+  }
+  if (warp == 1) {
+    if constexpr (PAIR)
+      tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+    else
+      tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  }
   tc_fence_before();
   __syncthreads();
-  if constexpr (MC) cluster_barrier_all();        // the peer's barriers are initialised
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -224,6 +297,25 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
             ok = false;
             break;
           }
+          if constexpr (PAIR) {
+            // this CTA's A rows and its half of the W tile; the bytes of both
+            // CTAs count on the leader's full barrier, whose one arrival (with
+            // the pair's total bytes) is the leader's.  A plain CTA-scope
+            // arrive: a cluster-scope release here would wait for this
+            // thread's earlier copies and serialise the ring.
+            const uint32_t fb = cluster_addr(bar(FULL + stage), 0);
+            if (rank == 0) mbar_arrive_expect_tx(bar(FULL + stage), 2 * C::STAGE_BYTES);
+#pragma unroll
+            for (int h = 0; h < C::KBOX; ++h) {
+              tma_load_2d_pair(smem_u32(sA + stage * C::A_BYTES + h * (C::A_BYTES / C::KBOX)), &tmA, fb,
+                               kb * BK + 64 * h, m0);
+              tma_load_2d_pair(smem_u32(sB + stage * C::B_BYTES + h * (C::B_BYTES / C::KBOX)), &tmB, fb,
+                               kb * BK + 64 * h, n0 + rank * (BN / 2));
+            }
+            issued[stage] = (int)phase;
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            continue;
+          }
           mbar_arrive_expect_tx(bar(FULL + stage), C::STAGE_BYTES);
           tma_load_2d(smem_u32(sA + stage * C::A_BYTES), &tmA, bar(FULL + stage), kb * BK, m0);
           // W boxes are BN/2 rows; the two halves sit back to back in the stage
@@ -239,16 +331,18 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
-      if (!ok) {
-        // let every copy still in flight land before the CTA exits
+      if (!ok && (!PAIR || rank == 0)) {
+        // let every copy still in flight land before the CTA exits (in a pair
+        // the leader's full barriers also count the peer's copies, and the
+        // peer waits for the leader at the final cluster barrier)
         for (int s = 0; s < STAGES; ++s)
           if (issued[s] >= 0) mbar_wait(bar(FULL + s), (uint32_t)issued[s], limit);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+    if (lane == 0 && (!PAIR || rank == 0)) {
+      constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true, any = false;
@@ -272,21 +366,38 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
           const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
           const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            tc_mma_f16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
-                       (kb | k) != 0);
+          for (int k = 0; k < BK / 16; ++k) {
+            // 16-column step k: box k / 4 of the stage, 32 bytes per step inside it
+            const uint32_t ao = (k >> 2) * (C::A_BYTES / C::KBOX) + (k & 3) * 32;
+            const uint32_t bo = (k >> 2) * (C::B_BYTES / C::KBOX) + (k & 3) * 32;
+            if constexpr (PAIR)
+              tc_mma_f16_pair(d_tmem, smem_desc_sw128(a0 + ao), smem_desc_sw128(b0 + bo), idesc, (kb | k) != 0);
+            else
+              tc_mma_f16(d_tmem, smem_desc_sw128(a0 + k * 32), smem_desc_sw128(b0 + k * 32), idesc,
+                         (kb | k) != 0);
+          }
           any = true;
-          if constexpr (MC)
+          if constexpr (PAIR)
+            tc_commit_pair(bar(EMPTY + stage), (uint16_t)0x3);
+          else if constexpr (MC)
             tc_commit_mc(bar(EMPTY + stage), (uint16_t)0x3);
           else
             tc_commit(bar(EMPTY + stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
-        if (ok) tc_commit(bar(TFULL + acc));
+        if (ok) {
+          if constexpr (PAIR)
+            tc_commit_pair(bar(TFULL + acc), (uint16_t)0x3);
+          else
+            tc_commit(bar(TFULL + acc));
+        }
       }
       if (!ok && any) {
         // every issued MMA must finish before TMEM is released
-        tc_commit(bar(DRAIN));
+        if constexpr (PAIR)
+          tc_commit_pair(bar(DRAIN), (uint16_t)0x1);
+        else
+          tc_commit(bar(DRAIN));
         mbar_wait(bar(DRAIN), 0, limit);
       }
     }
@@ -464,7 +575,12 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(bar(TEMPTY + acc));
+      if constexpr (PAIR) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(cluster_addr(bar(TEMPTY + acc), 0));
+      } else {
+        mbar_arrive(bar(TEMPTY + acc));
+      }
     }
     if (lane == 0) bulk_wait_all();                 // stores done before the CTA exits
     __syncwarp();
@@ -472,10 +588,16 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  // (MC) no CTA leaves while its peer may still signal its barriers
+  // (MC) no CTA leaves while its peer may still signal its barriers or, for a
+  // pair, write its tensor memory
   if constexpr (MC) cluster_barrier_all();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
 }
 
 }  // namespace nc

@@ -46,6 +46,8 @@ static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
 namespace {
 
 constexpr int64_t kGuardElems = 2048;       // sentinel guard before and after each cache
+// form of the prefill GEMMs: CTA pairs on tcgen05.mma.cta_group::2 (see launch_gemm_tc)
+constexpr int kPrefillCluster = 2;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 // log2(e) / sqrt(128): attention scale folded into the exp2 of the softmax
 constexpr float kAttnScaleLog2 = 1.4426950408889634f * 0.08838834764831845f;
@@ -281,47 +283,59 @@ cudaError_t launch_k(bool pdl, void (*k)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
 }
 
-// Prefill GEMM; tb is a weight map with a box of BN/2 rows.  With `mc` (and
-// at least two M tiles) it runs as clusters of two CTAs that share each
-// weight tile through TMA multicast.
+// Prefill GEMM; tb is a weight map with a box of BN/2 rows.  cl selects the
+// form (with at least two M tiles): 0 one CTA per tile, 1 CTA pairs sharing
+// each weight tile by TMA multicast, 2 CTA pairs computing 256-row tiles with
+// tcgen05.mma.cta_group::2.
+template <int BN, int EPI, int CL>
+cudaError_t set_gemm_smem() {
+  return cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)TcCfg<BN, EPI, CL>::SMEM);
+}
+
+template <int BN, int EPI, int CL>
+cudaError_t launch_gemm_cl(nc_model* m, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                           const GemmArgs& a, cudaStream_t s) {
+  using C = TcCfg<BN, EPI, CL>;
+  const int num_m = (a.M + 127) / 128, num_n = a.N / BN;
+  const int units = ((num_m + 1) / 2) * num_n;
+  const int pairs = units < m->num_sms / 2 ? units : m->num_sms / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, CL>, ta, tb, tc, a);
+  m->launches++;
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <int BN, int EPI>
 cudaError_t launch_gemm_tc(nc_model* m, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const CUtensorMap& tc, const GemmArgs& a, cudaStream_t s, bool mc = false) {
-  using C = TcCfg<BN, EPI>;
+                           const CUtensorMap& tc, const GemmArgs& a, cudaStream_t s, int cl = 0) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)C::SMEM);
+    cudaError_t e = set_gemm_smem<BN, EPI, 0>();
+    if (e == cudaSuccess) e = set_gemm_smem<BN, EPI, 1>();
+    if (e == cudaSuccess) e = set_gemm_smem<BN, EPI, 2>();
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int num_m = (a.M + 127) / 128, num_n = a.N / BN;
   if (num_m * num_n == 0) return cudaSuccess;
-  if (mc && num_m >= 2) {
-    const int units = ((num_m + 1) / 2) * num_n;
-    const int pairs = units < m->num_sms / 2 ? units : m->num_sms / 2;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * pairs, 1, 1);
-    cfg.blockDim = dim3(C::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, true>, ta, tb, tc, a);
-    m->launches++;
-    return e != cudaSuccess ? e : cudaGetLastError();
-  }
+  if (cl == 1 && num_m >= 2) return launch_gemm_cl<BN, EPI, 1>(m, ta, tb, tc, a, s);
+  if (cl == 2 && num_m >= 2) return launch_gemm_cl<BN, EPI, 2>(m, ta, tb, tc, a, s);
+  using C = TcCfg<BN, EPI, 0>;
   const int tiles = num_m * num_n;
   const int grid = tiles < m->num_sms ? tiles : m->num_sms;
-  gemm_tc_kernel<BN, EPI, false><<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tc, a);
+  gemm_tc_kernel<BN, EPI, 0><<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tc, a);
   m->launches++;
   return cudaGetLastError();
 }
@@ -415,7 +429,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
           a.vt = static_cast<bf16*>(m->vt);
           a.vt_S = m->vt_S;
         }
-        NC_TRY((launch_gemm_tc<256, EPI_QKV>(m, m->tm_h, m->tm_w128[4 * l + 0], m->tm_q_st, a, s, true)));
+        NC_TRY((launch_gemm_tc<256, EPI_QKV>(m, m->tm_h, m->tm_w128[4 * l + 0], m->tm_q_st, a, s, kPrefillCluster)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_STORE>(m, static_cast<const float*>(m->h),
                                             static_cast<const float*>(m->wqkv[l]), m->c32, M, NQKV,
@@ -465,7 +479,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       KScope ks(m, NC_K_OPROJ, s);
       if (bf) {
         GemmArgs a = base_args(m, M, d, NQ);
-        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_att, m->tm_w128[4 * l + 1], m->tm_x_st, a, s, true)));
+        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_att, m->tm_w128[4 * l + 1], m->tm_x_st, a, s, kPrefillCluster)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->att),
                                             static_cast<const float*>(m->wo[l]), m->x, M, d, NQ, d, s));
@@ -486,7 +500,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       KScope ks(m, NC_K_FC, s);
       if (bf) {
         GemmArgs a = base_args(m, M, F, d);
-        NC_TRY((launch_gemm_tc<256, EPI_RELU2>(m, m->tm_h, m->tm_w128[4 * l + 2], m->tm_u_st, a, s, true)));
+        NC_TRY((launch_gemm_tc<256, EPI_RELU2>(m, m->tm_h, m->tm_w128[4 * l + 2], m->tm_u_st, a, s, kPrefillCluster)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RELU2>(m, static_cast<const float*>(m->h),
                                             static_cast<const float*>(m->wfc[l]),
@@ -497,7 +511,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       KScope ks(m, NC_K_PROJ, s);
       if (bf) {
         GemmArgs a = base_args(m, M, d, F);
-        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_u, m->tm_w128[4 * l + 3], m->tm_x_st, a, s, true)));
+        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_u, m->tm_w128[4 * l + 3], m->tm_x_st, a, s, kPrefillCluster)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->u),
                                             static_cast<const float*>(m->wproj[l]), m->x, M, d, F, d, s));
@@ -526,7 +540,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       GemmArgs a = base_args(m, out_rows, V, d);
       CUtensorMap tm_out;
       if (!make_tmap(&tm_out, logits, out_rows, V, 32, true)) return NC_ERR_INVALID_ARG;
-      NC_TRY((launch_gemm_tc<256, EPI_LOGITS>(m, last_only ? m->tm_hlast : m->tm_h, m->tm_wu128, tm_out, a, s, true)));
+      NC_TRY((launch_gemm_tc<256, EPI_LOGITS>(m, last_only ? m->tm_hlast : m->tm_h, m->tm_wu128, tm_out, a, s, kPrefillCluster)));
     } else {
       NC_TRY(launch_simt_gemm<SEPI_LOGITS>(
           m, static_cast<const float*>(last_only ? m->h_last : m->h),
@@ -1087,14 +1101,14 @@ nc_status nc_gemm_bf16(nc_model* m, const void* A, const void* W, float* C, int3
                        int32_t K, nc_stream_t stream) {
   if (!m || !A || !W || !C || M < 1 || N < 256 || K < 8 || N % 256 || K % 8) return NC_ERR_INVALID_ARG;
   if (!is_device_ptr(A) || !is_device_ptr(W) || !is_device_ptr(C)) return NC_ERR_INVALID_ARG;
-  // M > 128 runs the two-CTA multicast path (the one the prefill uses)
-  const bool mc = M > 128;
+  // M > 128 runs the CTA-pair form the prefill uses
+  const int cl = M > 128 ? kPrefillCluster : 0;
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, A, M, K, 128) || !make_tmap(&tb, W, N, K, 128)) return NC_ERR_INVALID_ARG;
   CUtensorMap tc;
   if (!make_tmap(&tc, C, M, N, 32, true)) return NC_ERR_INVALID_ARG;
   GemmArgs a = base_args(m, M, N, K);
-  NC_TRY((launch_gemm_tc<256, EPI_STORE>(m, ta, tb, tc, a, stream, mc)));
+  NC_TRY((launch_gemm_tc<256, EPI_STORE>(m, ta, tb, tc, a, stream, cl)));
   return NC_OK;
 }
 
