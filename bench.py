@@ -83,6 +83,7 @@ class ClockSampler:
     def __init__(self, gpu_index, period_s=0.01):
         self.gpu, self.period = gpu_index, period_s
         self.sm, self.bits, self.mx, self.nv = [], 0, None, None
+        self.smi, self.note = None, None
 
     def __enter__(self):
         import threading
@@ -94,13 +95,60 @@ class ClockSampler:
             self.mx = float(nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM))
             self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
                 nv.nvmlDeviceGetCurrentClocksThrottleReasons
-        except Exception:
-            self.nv = None
+        except Exception as e:
+            # NVML unavailable: poll nvidia-smi instead (50 ms)
+            self.nv, self.note = None, f"nvml: {type(e).__name__}: {e}"[:160]
+            self._start_smi()
             return self
         self.stop = threading.Event()
         self.th = threading.Thread(target=self._loop, daemon=True)
         self.th.start()
         return self
+
+    SMI_Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def _start_smi(self):
+        import subprocess
+        import tempfile
+        try:
+            import torch
+            ident = str(torch.cuda.get_device_properties(self.gpu).uuid)
+            ident = ident if ident.startswith("GPU-") else "GPU-" + ident
+        except Exception:
+            ident = str(self.gpu)
+        self.smi_out = tempfile.TemporaryFile(mode="w+")
+        try:
+            self.smi = subprocess.Popen(["nvidia-smi", f"--id={ident}", f"--query-gpu={self.SMI_Q}",
+                                         "--format=csv,noheader,nounits", "-lms", "50"],
+                                        stdout=self.smi_out, stderr=subprocess.DEVNULL)
+        except OSError as e:
+            self.smi, self.note = None, (self.note or "") + f"; nvidia-smi: {e}"
+
+    def _stop_smi(self):
+        if self.smi is None:
+            return
+        self.smi.terminate()
+        try:
+            self.smi.wait(timeout=5)
+        except Exception:
+            self.smi.kill()
+        self.smi_out.seek(0)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        self.smi_reasons = set()
+        for line in self.smi_out:
+            p = [t.strip() for t in line.split(",")]
+            if len(p) < 6:
+                continue
+            try:
+                self.sm.append(float(p[0]))
+                self.mx = float(p[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[2:6]):
+                if v.lower() == "active":
+                    self.smi_reasons.add(n)
 
     def _handle(self, nv):
         # NVML numbers every GPU of the machine; find this process's device
@@ -125,6 +173,7 @@ class ClockSampler:
             self.stop.wait(self.period)
 
     def __exit__(self, *a):
+        self._stop_smi()
         if self.nv is not None:
             self.stop.set()
             self.th.join(timeout=2)
@@ -134,11 +183,18 @@ class ClockSampler:
                 pass
 
     def summary(self):
-        if self.nv is None or not self.sm:
-            return None
-        reasons = sorted(n for n, c in self.REASONS if hasattr(self.nv, c) and self.bits & getattr(self.nv, c))
-        return {"sm_mhz": statistics.median(self.sm), "sm_max_mhz": self.mx, "reasons": reasons,
-                "samples": len(self.sm)}
+        if not self.sm:
+            return {"sm_mhz": None, "sm_max_mhz": self.mx, "reasons": [], "samples": 0, "note": self.note}
+        if self.nv is not None:
+            reasons = sorted(n for n, c in self.REASONS if hasattr(self.nv, c) and self.bits & getattr(self.nv, c))
+            src = "nvml 10 ms"
+        else:
+            reasons, src = sorted(getattr(self, "smi_reasons", set())), "nvidia-smi 50 ms"
+        out = {"sm_mhz": statistics.median(self.sm), "sm_max_mhz": self.mx, "reasons": reasons,
+               "samples": len(self.sm), "source": src}
+        if self.note:
+            out["note"] = self.note
+        return out
 
 
 # DRAM traffic per launch of the dominant kernel, from the ncu captures

@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
       for (int u = unit0; ok && u < num_units; u += ustride) {
         const int m0 = unit_m0(u), n0 = unit_n0(u);
         for (int kb = 0; kb < KB; ++kb) {
-          if (*abort_flag || !mbar_wait(bar(EMPTY + stage), phase ^ 1, limit)) {
+          if (!mbar_test_wait(bar(EMPTY + stage), phase ^ 1) && (*abort_flag || !mbar_wait(bar(EMPTY + stage), phase ^ 1, limit))) {
             if (!*abort_flag) fail();
             ok = false;
             break;
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
       for (int u = unit0; ok && u < num_units; u += ustride, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        if (*abort_flag || !mbar_wait(bar(TEMPTY + acc), acc_phase ^ 1, limit)) {
+        if (!mbar_test_wait(bar(TEMPTY + acc), acc_phase ^ 1) && (*abort_flag || !mbar_wait(bar(TEMPTY + acc), acc_phase ^ 1, limit))) {
           if (!*abort_flag) fail();
           ok = false;
           break;
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < KB; ++kb) {
-          if (*abort_flag || !mbar_wait(bar(FULL + stage), phase, limit)) {
+          if (!mbar_test_wait(bar(FULL + stage), phase) && (*abort_flag || !mbar_wait(bar(FULL + stage), phase, limit))) {
             if (!*abort_flag) fail();
             ok = false;
             break;
