@@ -125,6 +125,16 @@ class ClockSampler:
                                         stdout=self.smi_out, stderr=subprocess.DEVNULL)
         except OSError as e:
             self.smi, self.note = None, (self.note or "") + f"; nvidia-smi: {e}"
+            return
+        # nvidia-smi takes a moment to start: let its first sample land before
+        # the timed region begins (at most 5 s)
+        import time
+        t0 = time.time()
+        while time.time() - t0 < 5 and self.smi.poll() is None:
+            self.smi_out.flush()
+            if os.fstat(self.smi_out.fileno()).st_size > 0:
+                break
+            time.sleep(0.05)
 
     def _stop_smi(self):
         if self.smi is None:
@@ -441,7 +451,7 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="d12_prefill", choices=sorted(nc_inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
