@@ -401,18 +401,19 @@ def bench_decode(args, w, flat, prompt, nxt, steps=None):
     torch.cuda.synchronize()
     l0 = m.launch_count
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for t in range(steps):
-        m.decode_step(nxt_d[t], out=out)
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ev0.record(stream)
+        for t in range(steps):
+            m.decode_step(nxt_d[t], out=out)
+        ev1.record(stream)
+        torch.cuda.synchronize()
     m.sync()
     ms = ev0.elapsed_time(ev1) / steps
     launches = (m.launch_count - l0) // steps
     ctx_mean = w.prompt_len + (steps + 1) / 2.0
     byts = np.mean([decode_bytes(w.shape, B, w.prompt_len + t + 1) for t in range(steps)])
     m.close()
-    return {"ms": ms, "launches": launches, "bytes": float(byts), "ctx_mean": ctx_mean}
+    return {"ms": ms, "launches": launches, "bytes": float(byts), "ctx_mean": ctx_mean, "clocks": clk.summary()}
 
 
 def run_case(args):
@@ -540,7 +541,8 @@ def main():
                 line["decode"] = {"workload": wd.name, "value": round(wd.batch / (rd["ms"] / 1e3), 1),
                                   "unit": "tokens/s", "ms_per_step": round(rd["ms"], 4),
                                   "gpu_launches_per_step": rd["launches"],
-                                  "hbm_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+                                  "hbm_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                                  "clocks": rd["clocks"]}
     else:
         rd = bench_decode(args, w, flat, prompt, nxt)
         value = world * w.batch / (rd["ms"] / 1e3)
@@ -554,6 +556,7 @@ def main():
             "roofline": {"bound": "hbm", "kernel": "decode step", "achieved": round(gbs, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None},
+            "clocks": rd["clocks"],
         })
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
