@@ -208,20 +208,22 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
       auto issue_s = [&](int t, int ks) {
-        const uint32_t qa = s0 + ATC_OFF_Q + t * ATC_TILE, ka = s0 + ATC_OFF_KV + ks * ATC_TILE;
+        const uint64_t dq = smem_desc_sw128(s0 + ATC_OFF_Q + t * ATC_TILE);
+        const uint64_t dk = smem_desc_sw128(s0 + ATC_OFF_KV + ks * ATC_TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * ATC_HALF + (kk & 3) * 32;
-          tc_mma_f16(tmem_base + t * 128, smem_desc_sw128(qa + off), smem_desc_sw128(ka + off), idesc, kk != 0);
+          tc_mma_f16(tmem_base + t * 128, desc_add(dq, off), desc_add(dk, off), idesc, kk != 0);
         }
         tc_commit(bar(SFULL + t));
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t pa = s0 + ATC_OFF_P + t * ATC_TILE, va = s0 + ATC_OFF_KV + ((2 * j + 1) % 3) * ATC_TILE;
+        const uint64_t dp = smem_desc_sw128(s0 + ATC_OFF_P + t * ATC_TILE);
+        const uint64_t dv = smem_desc_sw128(s0 + ATC_OFF_KV + ((2 * j + 1) % 3) * ATC_TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * ATC_HALF + (kk & 3) * 32;
-          tc_mma_f16(tmem_base + 256 + t * 128, smem_desc_sw128(pa + off), smem_desc_sw128(va + off), idesc,
+          tc_mma_f16(tmem_base + 256 + t * 128, desc_add(dp, off), desc_add(dv, off), idesc,
                      (j | kk) != 0);
         }
         tc_commit(bar(PVDONE + t));

@@ -175,11 +175,11 @@ __global__ void __launch_bounds__(128)
         break;
       }
       tc_fence_after();
-      const uint32_t w0 = smem_u32(sW + stage * C::W_BYTES), a0 = smem_u32(sA + stage * C::A_BYTES);
+      const uint64_t dw = smem_desc_sw128(smem_u32(sW + stage * C::W_BYTES));
+      const uint64_t da = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES));
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        tc_mma_f16(tmem_base, smem_desc_sw128(w0 + k * 32), smem_desc_sw128(a0 + k * 32), idesc,
-                   (kb | k) != 0);
+        tc_mma_f16(tmem_base, desc_add(dw, k * 32), desc_add(da, k * 32), idesc, (kb | k) != 0);
       any = true;
       tc_commit(bar(EMPTY + stage));
       if (++stage == STAGES) { stage = 0; phase ^= 1; }

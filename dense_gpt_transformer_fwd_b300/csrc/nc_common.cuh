@@ -249,6 +249,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// Descriptor of the same tile `byte_off` bytes further on: the start-address
+// field holds address >> 4 and shared addresses stay below 2^18, so the field
+// never carries into its neighbours.  Lets the MMA-issuing thread build each
+// operand's descriptor once per stage and add a constant per instruction.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off) {
+  return desc + (uint64_t)(byte_off >> 4);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, shape M x N (N multiple of 16 up to 256 for M = 128).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
