@@ -7,10 +7,11 @@
 // nanochat works" item 5).
 //
 // Decode kernel (split over the context): one CTA = one batch row and a
-// chunk of 128 cached keys; the row's n_head query vectors form the 16-row
-// A operand (heads padded to 16), each warp handles 32 keys; partial (max,
-// sum, output) go to a workspace, and the last CTA of the row to finish
-// (a per-row counter) merges the chunks into the bf16 output.
+// group of consecutive 64-key sub-chunks streamed through a cp.async ring;
+// the row's n_head query vectors form the 16-row A operand (heads padded to
+// 16), each warp handles 16 keys of every sub-chunk with a running softmax;
+// partial (max, sum, output) go to a workspace, and the last CTA of the row
+// to finish (a per-row counter) merges the groups into the bf16 output.
 #pragma once
 
 #include "nc_common.cuh"
@@ -56,59 +57,71 @@ constexpr int ATT_HD = 128;
 
 // ---------------------------------------------------------------- decode --
 // Q: [B][n_head*128] (one new position per row, at pos = ctx-1); keys 0..ctx-1.
-// Partial results per (row b, chunk c): m, l [B][nchunk][16][2], o [B][nchunk][16][128].
-constexpr int DEC_CHUNK = 128;             // keys per CTA
-constexpr int DEC_KPW = DEC_CHUNK / 4;     // keys per warp
+// CTA (group g, row b) streams `group` consecutive sub-chunks of DEC_SUB keys
+// (keys [g*group*DEC_SUB, ...)) through a DEC_STAGES-deep cp.async ring and
+// keeps a running (max, sum, output) per warp across them; each of the 4
+// warps owns DEC_SUB/4 keys of every sub-chunk.  Partial results per (row b,
+// group g): m, l [B][ngroups][16][2], o [B][ngroups][16][128].
+constexpr int DEC_CHUNK = 128;             // context granularity of the partial buffers
+constexpr int DEC_SUB = 64;                // keys per pipeline stage
+constexpr int DEC_STAGES = 3;
+constexpr int DEC_KPW = DEC_SUB / 4;       // keys per warp per sub-chunk
+constexpr uint32_t DEC_STAGE_BYTES = 2 * DEC_SUB * 256;   // K and V rows of a sub-chunk
 
 __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kc,
     const __nv_bfloat16* __restrict__ Vc, float* __restrict__ part_o, float* __restrict__ part_ml,
     __nv_bfloat16* __restrict__ O, int* __restrict__ counters, int n_head, int cache_S, int ctx,
-    const int* __restrict__ pos_dev, float scale_log2) {
+    const int* __restrict__ pos_dev, float scale_log2, int group) {
   pdl_trigger();
   // with pos_dev the context is read on the device (the step is graph-replayable);
   // the length only changes at the end of a step, so it may be read before
-  // waiting for the previous kernel.  Chunks beyond the context exit.
+  // waiting for the previous kernel.  Groups beyond the context exit.
   if (pos_dev) ctx = *pos_dev + 1;
-  const int nchunk = (ctx + DEC_CHUNK - 1) / DEC_CHUNK;
-  if ((int)blockIdx.x >= nchunk) return;
+  const int nsub = (ctx + DEC_SUB - 1) / DEC_SUB;
+  const int ngroups = (nsub + group - 1) / group;
+  const int grp = blockIdx.x, b = blockIdx.y;
+  const int c_begin = grp * group;
+  if (c_begin >= nsub) return;
+  const int n = min(group, nsub - c_begin);
   extern __shared__ __align__(128) uint8_t att_smem[];
   const uint32_t sQ = smem_u32(att_smem);                     // 16 rows
-  const uint32_t sK = sQ + 16 * 256;                           // DEC_CHUNK keys
-  const uint32_t sV = sK + DEC_CHUNK * 256;
-  float* red = reinterpret_cast<float*>(att_smem + (16 + 2 * DEC_CHUNK) * 256);  // [4][16][2]
-  float* ored = reinterpret_cast<float*>(att_smem + 16 * 256);  // [4][16][128], aliases K/V
+  const uint32_t sS = sQ + 16 * 256;                           // DEC_STAGES x (K, V) sub-chunks
+  float* red = reinterpret_cast<float*>(att_smem + 16 * 256 + DEC_STAGES * DEC_STAGE_BYTES);  // [4][16][2]
+  float* ored = reinterpret_cast<float*>(att_smem + 16 * 256);  // [4][16][128], aliases the stages
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int chunk_id = blockIdx.x, b = blockIdx.y;
-  const int k0 = chunk_id * DEC_CHUNK;
   const int ldq = n_head * ATT_HD;
   const __nv_bfloat16* kb = Kc + (size_t)b * cache_S * ATT_HD;
   const __nv_bfloat16* vb = Vc + (size_t)b * cache_S * ATT_HD;
-  // keys before the newest were written by earlier calls: stream them now
-  for (int i = tid; i < DEC_CHUNK * 16; i += 128) {
-    const int r = i >> 4, c = i & 15;
-    const int key = k0 + r;
-    if (key >= ctx - 1) continue;
-    const size_t off = (size_t)key * ATT_HD + c * 8;
-    cp_async16(swz(sK, r, c), kb + off, true);
-    cp_async16(swz(sV, r, c), vb + off, true);
+  // rows of sub-chunk i: keys (c_begin + i) * DEC_SUB + r.  `which`: 0 keys
+  // written by earlier calls only, 1 the newest key only, 2 all; keys >= ctx
+  // are zero-filled
+  auto load_sub = [&](int i, int which) {
+    const uint32_t sk = sS + (i % DEC_STAGES) * DEC_STAGE_BYTES, sv = sk + DEC_SUB * 256;
+    const int k0 = (c_begin + i) * DEC_SUB;
+    for (int e = tid; e < DEC_SUB * 16; e += 128) {
+      const int r = e >> 4, c = e & 15;
+      const int key = k0 + r;
+      if (which == 0 && key >= ctx - 1) continue;
+      if (which == 1 && key < ctx - 1) continue;
+      const bool ok = key < ctx;
+      const size_t off = (size_t)(ok ? key : 0) * ATT_HD + c * 8;
+      cp_async16(swz(sk, r, c), kb + off, ok);
+      cp_async16(swz(sv, r, c), vb + off, ok);
+    }
+  };
+  const int pre = n < DEC_STAGES - 1 ? n : DEC_STAGES - 1;
+  for (int i = 0; i < pre; ++i) {
+    load_sub(i, 0);
+    cp_async_commit();
   }
-  cp_async_commit();
   pdl_wait();                                                  // q and the newest K/V row
-  for (int i = tid; i < 16 * 16; i += 128) {
-    const int r = i >> 4, c = i & 15;
+  for (int e = tid; e < 16 * 16; e += 128) {
+    const int r = e >> 4, c = e & 15;
     const bool ok = r < n_head;
     cp_async16(swz(sQ, r, c), Q + (size_t)b * ldq + (ok ? r : 0) * ATT_HD + c * 8, ok);
   }
-  for (int i = tid; i < DEC_CHUNK * 16; i += 128) {
-    const int r = i >> 4, c = i & 15;
-    const int key = k0 + r;
-    if (key < ctx - 1) continue;
-    const bool ok = key < ctx;
-    const size_t off = (size_t)(ok ? key : 0) * ATT_HD + c * 8;
-    cp_async16(swz(sK, r, c), kb + off, ok);
-    cp_async16(swz(sV, r, c), vb + off, ok);
-  }
+  for (int i = 0; i < pre; ++i) load_sub(i, 1);
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
@@ -121,73 +134,97 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
   }
   constexpr int NT = DEC_KPW / 8;                              // 8-key tiles per warp
   const int wk = warp * DEC_KPW;
-  float s[NT][4];
+  float m_lo = -INFINITY, m_hi = -INFINITY;                    // running max (quad-uniform)
+  float sum_lo = 0.f, sum_hi = 0.f;                            // this lane's share of the sums
+  float o[16][4];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+
+  for (int i = 0; i < n; ++i) {
+    if (i + DEC_STAGES - 1 < n) load_sub(i + DEC_STAGES - 1, 2);
+    cp_async_commit();
+    cp_async_wait<DEC_STAGES - 1>();
+    __syncthreads();
+    const uint32_t sK = sS + (i % DEC_STAGES) * DEC_STAGE_BYTES, sV = sK + DEC_SUB * 256;
+    const int k0 = (c_begin + i) * DEC_SUB;
+    float s[NT][4];
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
+    for (int j = 0; j < NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
 #pragma unroll
-    for (int jp = 0; jp < NT / 2; ++jp) {
-      const int key = wk + jp * 16 + (lane & 7) + (lane >> 4) * 8;
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(swz(sK, key, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
-      mma_bf16(s[2 * jp], qf[kk], b0, b1);
-      mma_bf16(s[2 * jp + 1], qf[kk], b2, b3);
+    for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+      for (int jp = 0; jp < NT / 2; ++jp) {
+        const int key = wk + jp * 16 + (lane & 7) + (lane >> 4) * 8;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(swz(sK, key, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
+        mma_bf16(s[2 * jp], qf[kk], b0, b1);
+        mma_bf16(s[2 * jp + 1], qf[kk], b2, b3);
+      }
     }
-  }
-  float mx_lo = -INFINITY, mx_hi = -INFINITY;
+    float mx_lo = m_lo, mx_hi = m_hi;
 #pragma unroll
-  for (int j = 0; j < NT; ++j)
+    for (int j = 0; j < NT; ++j)
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int key = k0 + wk + j * 8 + (lane & 3) * 2 + e;
-      const bool ok = key < ctx;
-      s[j][e] = ok ? s[j][e] * scale_log2 : -INFINITY;
-      s[j][2 + e] = ok ? s[j][2 + e] * scale_log2 : -INFINITY;
-      mx_lo = fmaxf(mx_lo, s[j][e]);
-      mx_hi = fmaxf(mx_hi, s[j][2 + e]);
+      for (int e = 0; e < 2; ++e) {
+        const int key = k0 + wk + j * 8 + (lane & 3) * 2 + e;
+        const bool ok = key < ctx;
+        s[j][e] = ok ? s[j][e] * scale_log2 : -INFINITY;
+        s[j][2 + e] = ok ? s[j][2 + e] * scale_log2 : -INFINITY;
+        mx_lo = fmaxf(mx_lo, s[j][e]);
+        mx_hi = fmaxf(mx_hi, s[j][2 + e]);
+      }
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+    // rows with no valid key so far keep max -inf: subtract 0 so exp2 gives 0, not NaN
+    const float ml = mx_lo == -INFINITY ? 0.f : mx_lo, mh = mx_hi == -INFINITY ? 0.f : mx_hi;
+    const float c_lo = m_lo == -INFINITY ? 0.f : exp2f(m_lo - ml);
+    const float c_hi = m_hi == -INFINITY ? 0.f : exp2f(m_hi - mh);
+    m_lo = mx_lo;
+    m_hi = mx_hi;
+    sum_lo *= c_lo;
+    sum_hi *= c_hi;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      o[j][0] *= c_lo;
+      o[j][1] *= c_lo;
+      o[j][2] *= c_hi;
+      o[j][3] *= c_hi;
     }
-  mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-  mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-  mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-  mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-  // a warp whose keys all lie beyond ctx has max -inf: subtract 0 so exp2 gives 0, not NaN
-  const float ml = mx_lo == -INFINITY ? 0.f : mx_lo, mh = mx_hi == -INFINITY ? 0.f : mx_hi;
-  float sum_lo = 0.f, sum_hi = 0.f;
-  uint32_t pf[NT / 2][4];
+    uint32_t pf[NT / 2][4];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    const float p0 = exp2f(s[j][0] - ml), p1 = exp2f(s[j][1] - ml);
-    const float p2 = exp2f(s[j][2] - mh), p3 = exp2f(s[j][3] - mh);
-    sum_lo += p0 + p1;
-    sum_hi += p2 + p3;
-    pf[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
-    pf[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
+    for (int j = 0; j < NT; ++j) {
+      const float p0 = exp2f(s[j][0] - ml), p1 = exp2f(s[j][1] - ml);
+      const float p2 = exp2f(s[j][2] - mh), p3 = exp2f(s[j][3] - mh);
+      sum_lo += p0 + p1;
+      sum_hi += p2 + p3;
+      pf[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
+      pf[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
+    }
+#pragma unroll
+    for (int kk = 0; kk < NT / 2; ++kk) {
+#pragma unroll
+      for (int jp = 0; jp < 8; ++jp) {
+        const int key = wk + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(swz(sV, key, jp * 2 + (lane >> 4)), b0, b1, b2, b3);
+        mma_bf16(o[2 * jp], pf[kk], b0, b1);
+        mma_bf16(o[2 * jp + 1], pf[kk], b2, b3);
+      }
+    }
+    __syncthreads();                                           // the stage may be refilled
   }
   sum_lo += __shfl_xor_sync(0xffffffffu, sum_lo, 1);
   sum_lo += __shfl_xor_sync(0xffffffffu, sum_lo, 2);
   sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, 1);
   sum_hi += __shfl_xor_sync(0xffffffffu, sum_hi, 2);
-  float o[16][4];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < NT / 2; ++kk) {
-#pragma unroll
-    for (int jp = 0; jp < 8; ++jp) {
-      const int key = wk + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(swz(sV, key, jp * 2 + (lane >> 4)), b0, b1, b2, b3);
-      mma_bf16(o[2 * jp], pf[kk], b0, b1);
-      mma_bf16(o[2 * jp + 1], pf[kk], b2, b3);
-    }
-  }
   // ---- merge the 4 warps: per head row, rescale to the CTA max
   const int rlo = lane >> 2, rhi = rlo + 8;
   if ((lane & 3) == 0) {
-    red[(warp * 16 + rlo) * 2 + 0] = mx_lo;
+    red[(warp * 16 + rlo) * 2 + 0] = m_lo;
     red[(warp * 16 + rlo) * 2 + 1] = sum_lo;
-    red[(warp * 16 + rhi) * 2 + 0] = mx_hi;
+    red[(warp * 16 + rhi) * 2 + 0] = m_hi;
     red[(warp * 16 + rhi) * 2 + 1] = sum_hi;
   }
   __syncthreads();                                             // all warps done with K/V
@@ -197,8 +234,8 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
     cm_lo = fmaxf(cm_lo, red[(w * 16 + rlo) * 2]);
     cm_hi = fmaxf(cm_hi, red[(w * 16 + rhi) * 2]);
   }
-  const float f_lo = mx_lo == -INFINITY ? 0.f : exp2f(mx_lo - cm_lo);
-  const float f_hi = mx_hi == -INFINITY ? 0.f : exp2f(mx_hi - cm_hi);
+  const float f_lo = m_lo == -INFINITY ? 0.f : exp2f(m_lo - cm_lo);
+  const float f_hi = m_hi == -INFINITY ? 0.f : exp2f(m_hi - cm_hi);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int col = j * 8 + (lane & 3) * 2;
@@ -209,7 +246,7 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
   }
   __syncthreads();
   // thread = output column; loop over head rows
-  const size_t pbase = ((size_t)b * nchunk + chunk_id) * 16;
+  const size_t pbase = ((size_t)b * ngroups + grp) * 16;
   for (int r = 0; r < n_head; ++r) {
     float acc = 0.f;
 #pragma unroll
@@ -227,25 +264,25 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
     part_ml[(pbase + tid) * 2 + 1] = cl;
   }
 
-  // ---- the last chunk CTA of row b to finish merges every chunk (chunk
+  // ---- the last group CTA of row b to finish merges every group (group
   // order fixed, so the result does not depend on which CTA is last)
   __shared__ int s_last;
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&counters[b], 1) == nchunk - 1;
+  if (tid == 0) s_last = atomicAdd(&counters[b], 1) == ngroups - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   if (tid == 0) counters[b] = 0;                               // ready for the next call
-  float* wts = ored;                                           // [nchunk][16] merge weights
+  float* wts = ored;                                           // [ngroups][16] merge weights
   float* inv_l = red;                                          // [16]
   __syncthreads();                                             // ored / red no longer read
-  const size_t rb = (size_t)b * nchunk * 16;
+  const size_t rb = (size_t)b * ngroups * 16;
   if (tid < n_head) {
     float gm = -INFINITY;
-    for (int c = 0; c < nchunk; ++c) gm = fmaxf(gm, __ldcg(part_ml + (rb + c * 16 + tid) * 2));
+    for (int c = 0; c < ngroups; ++c) gm = fmaxf(gm, __ldcg(part_ml + (rb + c * 16 + tid) * 2));
     float l = 0.f;
-    for (int c = 0; c < nchunk; ++c) {
+    for (int c = 0; c < ngroups; ++c) {
       const float mc = __ldcg(part_ml + (rb + c * 16 + tid) * 2);
       const float f = mc == -INFINITY ? 0.f : exp2f(mc - gm);
       wts[c * 16 + tid] = f;
@@ -257,20 +294,20 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
   // thread = output column; all chunks of two heads requested at once
   for (int h0 = 0; h0 < n_head; h0 += 2) {
     float acc[2] = {0.f, 0.f};
-    for (int c0 = 0; c0 < nchunk; c0 += 8) {
+    for (int c0 = 0; c0 < ngroups; c0 += 8) {
       float o8[2][8];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int c = c0 + i, h = h0 + hh;
-          o8[hh][i] = (c < nchunk && h < n_head) ? __ldcg(part_o + (rb + c * 16 + h) * 128 + tid) : 0.f;
+          o8[hh][i] = (c < ngroups && h < n_head) ? __ldcg(part_o + (rb + c * 16 + h) * 128 + tid) : 0.f;
         }
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          if (c0 + i < nchunk && h0 + hh < n_head) acc[hh] += o8[hh][i] * wts[(c0 + i) * 16 + h0 + hh];
+          if (c0 + i < ngroups && h0 + hh < n_head) acc[hh] += o8[hh][i] * wts[(c0 + i) * 16 + h0 + hh];
     }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh)
@@ -279,6 +316,6 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
   }
 }
 
-constexpr size_t ATT_DECODE_SMEM = (16 + 2 * DEC_CHUNK) * 256 + 4 * 16 * 2 * 4;
+constexpr size_t ATT_DECODE_SMEM = 16 * 256 + DEC_STAGES * (size_t)DEC_STAGE_BYTES + 4 * 16 * 2 * 4;
 
 }  // namespace nc

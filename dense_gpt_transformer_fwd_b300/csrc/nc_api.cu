@@ -356,6 +356,19 @@ int choose_splits(int tiles, int kb, int sms) {
   return best;
 }
 
+// Decode attention launch shape: sub-chunks of DEC_SUB keys per CTA (at least
+// two, so a row never has more partials than ceil(context / DEC_CHUNK)) chosen
+// for about two CTAs per SM over the batch; grid.x covers max_seq.
+void decode_attn_shape(const nc_model* m, int B, int* group, int* grid_x) {
+  const int max_sub = (m->cfg.max_seq + DEC_SUB - 1) / DEC_SUB;
+  int target = (2 * m->num_sms + B / 2) / B;
+  if (target < 1) target = 1;
+  int g = (max_sub + target - 1) / target;
+  if (g < 2) g = 2;
+  *group = g;
+  *grid_x = (max_sub + g - 1) / g;
+}
+
 GemmArgs base_args(nc_model* m, int M, int N, int K) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -459,11 +472,12 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
         NC_TRY(cudaGetLastError());
       } else if (bf) {
         const int ctx = pos0 + 1;                     // decode: T == 1
-        const int nchunk = (ctx + DEC_CHUNK - 1) / DEC_CHUNK;
-        attn_decode_mma_kernel<<<dim3(nchunk, B), 128, ATT_DECODE_SMEM, s>>>(
+        int group = 2, gx = 1;
+        decode_attn_shape(m, B, &group, &gx);
+        attn_decode_mma_kernel<<<dim3(gx, B), 128, ATT_DECODE_SMEM, s>>>(
             static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
             static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, static_cast<bf16*>(m->att),
-            m->att_counters, nh, c.max_seq, ctx, nullptr, kAttnScaleLog2);
+            m->att_counters, nh, c.max_seq, ctx, nullptr, kAttnScaleLog2, group);
         m->launches++;
         NC_TRY(cudaGetLastError());
       } else {
@@ -628,11 +642,13 @@ nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logit
     }
     {
       KScope ks(m, NC_K_ATTN, s);
-      NC_TRY(launch_k(true, attn_decode_mma_kernel, dim3(m->max_chunks, B), dim3(128), ATT_DECODE_SMEM, s,
+      int group = 2, gx = 1;
+      decode_attn_shape(m, B, &group, &gx);
+      NC_TRY(launch_k(true, attn_decode_mma_kernel, dim3(gx, B), dim3(128), ATT_DECODE_SMEM, s,
                       static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
                       static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, static_cast<bf16*>(m->att),
                       m->att_counters, nh, (int)c.max_seq, 0, static_cast<const int*>(m->d_len),
-                      kAttnScaleLog2));
+                      kAttnScaleLog2, group));
       m->launches++;
     }
     {
