@@ -41,10 +41,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&t);
-}
 
 // A [rows][128] bf16 tile in shared memory, rows of 256 B split in 16 chunks
 // of 16 B; chunk c of row r is stored at chunk c ^ (r & 7) to keep ldmatrix
@@ -59,16 +55,22 @@ constexpr int ATT_HD = 128;
 // Q: [B][n_head*128] (one new position per row, at pos = ctx-1); keys 0..ctx-1.
 // CTA (group g, row b) streams `group` consecutive sub-chunks of DEC_SUB keys
 // (keys [g*group*DEC_SUB, ...)) through a DEC_STAGES-deep cp.async ring and
-// keeps a running (max, sum, output) per warp across them; each of the 4
-// warps owns DEC_SUB/4 keys of every sub-chunk.  Partial results per (row b,
-// group g): m, l [B][ngroups][16][2], o [B][ngroups][16][128].
+// keeps a running (max, sum, output) per warp across them; each of the
+// DEC_WARPS warps owns DEC_KPW keys of every sub-chunk.  One CTA fills most of
+// an SM's shared memory: its ring keeps two 64 KB sub-chunks in flight and
+// its 8 warps hide each other's MMA/softmax latency.  Partial results per
+// (row b, group g): m, l [B][ngroups][16][2], o [B][ngroups][16][128].
 constexpr int DEC_CHUNK = 128;             // context granularity of the partial buffers
-constexpr int DEC_SUB = 64;                // keys per pipeline stage
+constexpr int DEC_SUB = 128;               // keys per pipeline stage
 constexpr int DEC_STAGES = 3;
-constexpr int DEC_KPW = DEC_SUB / 4;       // keys per warp per sub-chunk
+constexpr int DEC_WARPS = 8;
+constexpr int DEC_THREADS = DEC_WARPS * 32;
+constexpr int DEC_KPW = DEC_SUB / DEC_WARPS;   // keys per warp per sub-chunk (two 8-key MMA tiles)
 constexpr uint32_t DEC_STAGE_BYTES = 2 * DEC_SUB * 256;   // K and V rows of a sub-chunk
+static_assert(DEC_KPW == 16, "the score tile loop assumes 16 keys per warp");
+static_assert(DEC_CHUNK % DEC_SUB == 0 || DEC_SUB % DEC_CHUNK == 0, "partial buffers sized by DEC_CHUNK");
 
-__global__ void __launch_bounds__(128) attn_decode_mma_kernel(
+__global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kc,
     const __nv_bfloat16* __restrict__ Vc, float* __restrict__ part_o, float* __restrict__ part_ml,
     __nv_bfloat16* __restrict__ O, int* __restrict__ counters, int n_head, int cache_S, int ctx,
@@ -87,9 +89,9 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
   extern __shared__ __align__(128) uint8_t att_smem[];
   const uint32_t sQ = smem_u32(att_smem);                     // 16 rows
   const uint32_t sS = sQ + 16 * 256;                           // DEC_STAGES x (K, V) sub-chunks
-  float* red = reinterpret_cast<float*>(att_smem + 16 * 256 + DEC_STAGES * DEC_STAGE_BYTES);  // [4][16][2]
-  float* ored = reinterpret_cast<float*>(att_smem + 16 * 256);  // [4][16][128], aliases the stages
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* red = reinterpret_cast<float*>(att_smem + 16 * 256 + DEC_STAGES * DEC_STAGE_BYTES);  // [DEC_WARPS][16][2]
+  float* ored = reinterpret_cast<float*>(att_smem + 16 * 256);  // [DEC_WARPS][16][128], aliases the stages
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, ocol = tid & 127;
   const int ldq = n_head * ATT_HD;
   const __nv_bfloat16* kb = Kc + (size_t)b * cache_S * ATT_HD;
   const __nv_bfloat16* vb = Vc + (size_t)b * cache_S * ATT_HD;
@@ -99,7 +101,7 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
   auto load_sub = [&](int i, int which) {
     const uint32_t sk = sS + (i % DEC_STAGES) * DEC_STAGE_BYTES, sv = sk + DEC_SUB * 256;
     const int k0 = (c_begin + i) * DEC_SUB;
-    for (int e = tid; e < DEC_SUB * 16; e += 128) {
+    for (int e = tid; e < DEC_SUB * 16; e += DEC_THREADS) {
       const int r = e >> 4, c = e & 15;
       const int key = k0 + r;
       if (which == 0 && key >= ctx - 1) continue;
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
     cp_async_commit();
   }
   pdl_wait();                                                  // q and the newest K/V row
-  for (int e = tid; e < 16 * 16; e += 128) {
+  for (int e = tid; e < 16 * 16; e += DEC_THREADS) {
     const int r = e >> 4, c = e & 15;
     const bool ok = r < n_head;
     cp_async16(swz(sQ, r, c), Q + (size_t)b * ldq + (ok ? r : 0) * ATT_HD + c * 8, ok);
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
   __syncthreads();                                             // all warps done with K/V
   float cm_lo = -INFINITY, cm_hi = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
+  for (int w = 0; w < DEC_WARPS; ++w) {
     cm_lo = fmaxf(cm_lo, red[(w * 16 + rlo) * 2]);
     cm_hi = fmaxf(cm_hi, red[(w * 16 + rhi) * 2]);
   }
@@ -245,21 +247,38 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
     ored[(warp * 16 + rhi) * 128 + col + 1] = o[j][3] * f_hi;
   }
   __syncthreads();
-  // thread = output column; loop over head rows
-  const size_t pbase = ((size_t)b * ngroups + grp) * 16;
-  for (int r = 0; r < n_head; ++r) {
-    float acc = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) acc += ored[(w * 16 + r) * 128 + tid];
-    part_o[(pbase + r) * 128 + tid] = acc;
-  }
+  // per head row: the CTA's max and sum over its warps
+  float cm = -INFINITY, cl = 0.f;
   if (tid < n_head) {
-    float cm = -INFINITY, cl = 0.f;
-    for (int w = 0; w < 4; ++w) cm = fmaxf(cm, red[(w * 16 + tid) * 2]);
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < DEC_WARPS; ++w) cm = fmaxf(cm, red[(w * 16 + tid) * 2]);
+    for (int w = 0; w < DEC_WARPS; ++w) {
       const float mw = red[(w * 16 + tid) * 2];
       if (mw != -INFINITY) cl += red[(w * 16 + tid) * 2 + 1] * exp2f(mw - cm);
     }
+  }
+  if (ngroups == 1) {
+    // the CTA covered the whole context: normalise and write the output
+    float* inv_l1 = reinterpret_cast<float*>(att_smem);         // the Q tile is in registers
+    if (tid < n_head) inv_l1[tid] = 1.f / cl;
+    __syncthreads();
+    // thread = output column of every other head row
+    for (int r = tid >> 7; r < n_head; r += DEC_THREADS / 128) {
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < DEC_WARPS; ++w) acc += ored[(w * 16 + r) * 128 + ocol];
+      O[((size_t)b * n_head + r) * ATT_HD + ocol] = f2bf(acc * inv_l1[r]);
+    }
+    return;
+  }
+  // thread = output column of every other head row
+  const size_t pbase = ((size_t)b * ngroups + grp) * 16;
+  for (int r = tid >> 7; r < n_head; r += DEC_THREADS / 128) {
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < DEC_WARPS; ++w) acc += ored[(w * 16 + r) * 128 + ocol];
+    part_o[(pbase + r) * 128 + ocol] = acc;
+  }
+  if (tid < n_head) {
     part_ml[(pbase + tid) * 2 + 0] = cm;
     part_ml[(pbase + tid) * 2 + 1] = cl;
   }
@@ -291,8 +310,9 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
     inv_l[tid] = 1.f / l;
   }
   __syncthreads();
-  // thread = output column; all chunks of two heads requested at once
-  for (int h0 = 0; h0 < n_head; h0 += 2) {
+  // thread = output column; all chunks of two heads requested at once (the
+  // two halves of the CTA take alternate head pairs)
+  for (int h0 = 2 * (tid >> 7); h0 < n_head; h0 += DEC_THREADS / 64) {
     float acc[2] = {0.f, 0.f};
     for (int c0 = 0; c0 < ngroups; c0 += 8) {
       float o8[2][8];
@@ -301,7 +321,7 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int c = c0 + i, h = h0 + hh;
-          o8[hh][i] = (c < ngroups && h < n_head) ? __ldcg(part_o + (rb + c * 16 + h) * 128 + tid) : 0.f;
+          o8[hh][i] = (c < ngroups && h < n_head) ? __ldcg(part_o + (rb + c * 16 + h) * 128 + ocol) : 0.f;
         }
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh)
@@ -312,10 +332,10 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh)
       if (h0 + hh < n_head)
-        O[((size_t)b * n_head + h0 + hh) * ATT_HD + tid] = f2bf(acc[hh] * inv_l[h0 + hh]);
+        O[((size_t)b * n_head + h0 + hh) * ATT_HD + ocol] = f2bf(acc[hh] * inv_l[h0 + hh]);
   }
 }
 
-constexpr size_t ATT_DECODE_SMEM = 16 * 256 + DEC_STAGES * (size_t)DEC_STAGE_BYTES + 4 * 16 * 2 * 4;
+constexpr size_t ATT_DECODE_SMEM = 16 * 256 + DEC_STAGES * (size_t)DEC_STAGE_BYTES + DEC_WARPS * 16 * 2 * 4;
 
 }  // namespace nc

@@ -53,7 +53,20 @@ struct SkinnyArgs {
   float eps, softcap;
   int* err;
   unsigned long long wait_limit_ns;
+  // RMSNorm folded into the epilogues (decode): a residual epilogue also
+  // writes h_out = bf16(x) and, per row b, the sum of squares of its 128
+  // columns to ss_out[tile * ss_ld + b]; a consumer of h (QKV, MLP up, logits)
+  // scales row b of its result by r_b = 1 / sqrt(sum_t ss_in[t * ss_ld + b] / K
+  // + eps), summed over the n_ss column blocks in order.  Null: no folding.
+  __nv_bfloat16* h_out;
+  float* ss_out;
+  const float* ss_in;
+  int n_ss, ss_ld;
+  int* len_inc;                   // EPI_LOGITS: the step's final kernel advances the cache length
 };
+
+// column blocks of 128 in a folded RMSNorm (d_model <= 2048)
+constexpr int SK_MAX_SS = 16;
 
 template <int NB>
 struct SkCfg {
@@ -62,7 +75,8 @@ struct SkCfg {
   static constexpr uint32_t STAGE_BYTES = W_BYTES + A_BYTES;
   static constexpr int STAGES = (int)(98304 / STAGE_BYTES) < 2 ? 2 : (int)(98304 / STAGE_BYTES);
   static constexpr uint32_t TMEM_COLS = NB < 32 ? 32 : NB;
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+  // + row scales [NB], RoPE row [128] and position
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + NB * 4 + 512 + 16;
   static_assert((size_t)STAGES * STAGE_BYTES >= (size_t)NB * 128 * 4, "partial tile must fit the ring");
 };
 
@@ -76,12 +90,124 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
+
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_addr, uint32_t rank) {
   uint32_t remote;
-  float v;
+  float4 v;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote) : "memory");
   return v;
+}
+
+// Sum of the S partial tiles P_q[b][n] (q = 0..S-1, in rank order) for the
+// batch rows b = rank (mod S) of this CTA, then the fused epilogue.  Warp w
+// takes every 4th of those rows, lane l the columns 4l..4l+3 of the tile, so
+// every distributed-shared-memory read is 16 bytes and a warp reads 512
+// contiguous bytes.  RPB rows per warp are in flight at once (RPB x S reads,
+// plus the residual for EPI_RESID), which makes the reduction one or two
+// round trips instead of one per row.
+template <int S, int EPI>
+__device__ __forceinline__ void sk_reduce_epilogue(const SkinnyArgs& args, uint32_t psm, const float* r_s,
+                                                   const float* rope_s, const int* pos_s, int rank, int warp,
+                                                   int lane, int tile, float inv_cap) {
+  constexpr int RPB = 16 / S > 8 ? 8 : 16 / S;
+  const int c = 4 * lane;
+  const int n0 = tile * 128;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  // EPI_QKV: the tile is one head; rope row of the new token's position
+  const bool is_v = EPI == EPI_QKV && tile == args.n_head + 1;
+  float4 cs = zero, sn = zero;
+  int pos = 0;
+  if constexpr (EPI == EPI_QKV) {
+    pos = *pos_s;
+    cs = *reinterpret_cast<const float4*>(rope_s + 4 * (lane & 15));
+    sn = *reinterpret_cast<const float4*>(rope_s + 64 + 4 * (lane & 15));
+  }
+  for (int b0 = rank + S * warp; b0 < args.B; b0 += 4 * S * RPB) {
+    float4 part[RPB][S], xo[RPB];
+#pragma unroll
+    for (int i = 0; i < RPB; ++i) {
+      const int b = b0 + 4 * S * i;
+      const bool in = b < args.B;
+#pragma unroll
+      for (int q = 0; q < S; ++q) part[i][q] = in ? ld_dsmem_v4(psm + (b * 128 + c) * 4, (uint32_t)q) : zero;
+      if constexpr (EPI == EPI_RESID)
+        xo[i] = in ? *reinterpret_cast<const float4*>(args.x + (size_t)b * args.N + n0 + c) : zero;
+    }
+#pragma unroll
+    for (int i = 0; i < RPB; ++i) {
+      const int b = b0 + 4 * S * i;
+      if (b >= args.B) break;
+      float v[4] = {part[i][0].x, part[i][0].y, part[i][0].z, part[i][0].w};
+#pragma unroll
+      for (int q = 1; q < S; ++q) {
+        v[0] += part[i][q].x;
+        v[1] += part[i][q].y;
+        v[2] += part[i][q].z;
+        v[3] += part[i][q].w;
+      }
+      if constexpr (EPI != EPI_RESID) {
+        const float rb = r_s[b];                     // folded RMSNorm of the input row
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] *= rb;
+      }
+      if constexpr (EPI == EPI_QKV) {
+        if (!is_v) {
+          // QK norm over the head's 128 dims, then RoPE on pairs (j, j + 64):
+          // lanes 0..15 hold j = 4l..4l+3, lanes 16..31 their partners
+          float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+          ss = warp_sum(ss);
+          const float r = rsqrtf(ss * (1.f / 128.f) + args.eps);
+          const float c4[4] = {cs.x, cs.y, cs.z, cs.w}, s4[4] = {sn.x, sn.y, sn.z, sn.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float own = v[k] * r;
+            const float other = __shfl_xor_sync(0xffffffffu, own, 16);
+            v[k] = lane < 16 ? own * c4[k] - other * s4[k] : other * s4[k] + own * c4[k];
+          }
+        }
+        __nv_bfloat16* dst;
+        if (tile < args.n_head)
+          dst = args.out_bf + (size_t)b * args.n_head * 128 + tile * 128;
+        else
+          dst = (is_v ? args.v_cache : args.k_cache) + ((size_t)b * args.cache_S + pos) * 128;
+        uint2 pk;
+        pk.x = pack_bf16(v[0], v[1]);
+        pk.y = pack_bf16(v[2], v[3]);
+        *reinterpret_cast<uint2*>(dst + c) = pk;
+      } else {
+        const size_t o = (size_t)b * args.N + n0 + c;
+        if constexpr (EPI == EPI_RESID) {
+          const float4 xn = make_float4(xo[i].x + v[0], xo[i].y + v[1], xo[i].z + v[2], xo[i].w + v[3]);
+          *reinterpret_cast<float4*>(args.x + o) = xn;
+          if (args.h_out) {
+            uint2 pk;
+            pk.x = pack_bf16(xn.x, xn.y);
+            pk.y = pack_bf16(xn.z, xn.w);
+            *reinterpret_cast<uint2*>(args.h_out + o) = pk;
+            const float ss = warp_sum(xn.x * xn.x + xn.y * xn.y + xn.z * xn.z + xn.w * xn.w);
+            if (lane == 0) args.ss_out[(size_t)tile * args.ss_ld + b] = ss;
+          }
+        } else if constexpr (EPI == EPI_RELU2) {
+          float r[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float t = fmaxf(v[k], 0.f);
+            r[k] = t * t;
+          }
+          uint2 pk;
+          pk.x = pack_bf16(r[0], r[1]);
+          pk.y = pack_bf16(r[2], r[3]);
+          *reinterpret_cast<uint2*>(args.out_bf + o) = pk;
+        } else {
+          *reinterpret_cast<float4*>(args.x + o) =
+              make_float4(softcap_f(v[0], inv_cap, args.softcap), softcap_f(v[1], inv_cap, args.softcap),
+                          softcap_f(v[2], inv_cap, args.softcap), softcap_f(v[3], inv_cap, args.softcap));
+        }
+      }
+    }
+  }
 }
 
 template <int NB, int EPI>
@@ -98,6 +224,9 @@ __global__ void __launch_bounds__(128)
   // bars: full[STAGES], empty[STAGES], done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);   // [0] abort
+  float* r_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);   // [NB] row scales
+  float* rope_s = r_s + NB;                                  // EPI_QKV: cos [64], sin [64] at pos
+  int* pos_s = reinterpret_cast<int*>(rope_s + 128);
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int FULL = 0, EMPTY = STAGES, DONE = 2 * STAGES;
 
@@ -192,6 +321,30 @@ __global__ void __launch_bounds__(128)
 
   // ------------------------------------------------------------- epilogue
   pdl_wait();                                        // x / positions of the previous kernels
+  // row scales (all n_ss loads in flight, summed in block order) and the
+  // RoPE row, while the MMAs run
+  if (threadIdx.x < NB) {
+    float r = 1.f;
+    if (args.ss_in && threadIdx.x < args.B) {
+      float p[SK_MAX_SS];
+#pragma unroll
+      for (int i = 0; i < SK_MAX_SS; ++i)
+        p[i] = i < args.n_ss ? args.ss_in[(size_t)i * args.ss_ld + threadIdx.x] : 0.f;
+      float t = 0.f;
+#pragma unroll
+      for (int i = 0; i < SK_MAX_SS; ++i) t += p[i];
+      r = rsqrtf(t / (float)args.K + args.eps);
+    }
+    r_s[threadIdx.x] = r;
+  }
+  if (EPI == EPI_QKV && threadIdx.x >= 64) {
+    const int pos = *args.pos_dev, j = threadIdx.x - 64;
+    rope_s[j] = args.rope_cos[(size_t)pos * 64 + j];
+    rope_s[64 + j] = args.rope_sin[(size_t)pos * 64 + j];
+    if (j == 0) *pos_s = pos;
+  }
+  if (EPI == EPI_LOGITS && args.len_inc && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    *args.len_inc += 1;                              // every reader of the length has finished
   const bool done_ok = mbar_wait(bar(DONE), 0, limit);
   if (!done_ok && threadIdx.x == 0) fail();
   tc_fence_after();
@@ -209,7 +362,8 @@ __global__ void __launch_bounds__(128)
         tmem_ld32(taddr + c, v);
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (c + j < args.B) args.x[(size_t)(c + j) * args.N + n0 + row] = softcap_f(v[j], inv_cap, args.softcap);
+          if (c + j < args.B)
+            args.x[(size_t)(c + j) * args.N + n0 + row] = softcap_f(v[j] * r_s[c + j], inv_cap, args.softcap);
       }
     }
   } else {
@@ -227,84 +381,17 @@ __global__ void __launch_bounds__(128)
       }
     }
     cluster_sync_all();                              // every CTA of the tile reaches it once
-    const int S = args.splits;
-    const int rank = (int)cluster_ctarank();
     if (run) {
-      if constexpr (EPI == EPI_QKV) {
-        // one warp per batch row; lane holds dims lane + 32 i (i = 0..3) so
-        // both members of a RoPE pair (j, j + 64) sit in the same lane
-        const int head = tile;
-        const bool is_v = head == args.n_head + 1;
-        const int pos = *args.pos_dev;
-        for (int b = rank + S * warp; b < args.B; b += 4 * S) {
-          // every partial requested before any is summed (rank order kept)
-          float part[4][8];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              part[i][q] = q < S ? ld_dsmem_f32(psm + (b * 128 + lane + 32 * i) * 4, (uint32_t)q) : 0.f;
-          float v[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float sum = 0.f;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) sum += part[i][q];
-            v[i] = sum;
-          }
-          if (!is_v) {
-            float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
-            ss = warp_sum(ss);
-            const float r = rsqrtf(ss * (1.f / 128.f) + args.eps);
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int j = lane + 32 * i;
-              const float cs = args.rope_cos[(size_t)pos * 64 + j], sn = args.rope_sin[(size_t)pos * 64 + j];
-              const float x0 = v[i] * r, x1 = v[i + 2] * r;
-              v[i] = x0 * cs - x1 * sn;
-              v[i + 2] = x0 * sn + x1 * cs;
-            }
-          }
-          __nv_bfloat16* dst;
-          if (head < args.n_head)
-            dst = args.out_bf + (size_t)b * args.n_head * 128 + head * 128;
-          else
-            dst = (is_v ? args.v_cache : args.k_cache) + ((size_t)b * args.cache_S + pos) * 128;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = f2bf(v[i]);
-        }
-      } else {
-        // rows b = rank, rank + S, ...; thread = column n0 + row (coalesced);
-        // four rows at a time with every load issued before the sums
-        for (int b0 = rank; b0 < args.B; b0 += 4 * S) {
-          float part[4][8], xo[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int b = b0 + i * S;
-            const bool in = b < args.B;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              part[i][q] = (in && q < S) ? ld_dsmem_f32(psm + (b * 128 + row) * 4, (uint32_t)q) : 0.f;
-            if constexpr (EPI == EPI_RESID) xo[i] = in ? args.x[(size_t)b * args.N + n0 + row] : 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int b = b0 + i * S;
-            if (b >= args.B) break;
-            float sum = 0.f;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) sum += part[i][q];
-            const size_t o = (size_t)b * args.N + n0 + row;
-            if constexpr (EPI == EPI_RESID) {
-              args.x[o] = xo[i] + sum;
-            } else if constexpr (EPI == EPI_RELU2) {
-              const float r = fmaxf(sum, 0.f);
-              args.out_bf[o] = f2bf(r * r);
-            } else {
-              args.x[o] = softcap_f(sum, inv_cap, args.softcap);
-            }
-          }
-        }
+      const int rank = (int)cluster_ctarank();
+      switch (args.splits) {
+        case 1: sk_reduce_epilogue<1, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
+        case 2: sk_reduce_epilogue<2, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
+        case 3: sk_reduce_epilogue<3, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
+        case 4: sk_reduce_epilogue<4, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
+        case 5: sk_reduce_epilogue<5, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
+        case 6: sk_reduce_epilogue<6, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
+        case 7: sk_reduce_epilogue<7, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
+        default: sk_reduce_epilogue<8, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
       }
     }
     cluster_sync_all();                              // remote reads done before any CTA exits

@@ -15,11 +15,15 @@
 namespace nc {
 
 // One warp per row: x[m] = rms(E[tok[m]]) in fp32, h[m] = TA(rms(x[m])).
+// With ss_out (decode, norm folded into the next projection) h[m] = TA(x[m])
+// instead, and ss_out[t * ss_ld + m] = sum of x[m][j]^2 over the 128-column
+// block t (d a multiple of 128).
 // An out-of-range token raises NC_DEVFLAG_TOKEN and reads row 0 instead.
 template <typename TW, typename TA>
 __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tok, const TW* __restrict__ E,
                                      float* __restrict__ x, TA* __restrict__ h, int M, int d,
-                                     int vocab, float eps, int* err, int* len_set, int len_val) {
+                                     int vocab, float eps, int* err, int* len_set, int len_val,
+                                     float* __restrict__ ss_out, int ss_ld) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
   pdl_wait();
@@ -39,6 +43,20 @@ __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tok, const TW* 
   }
   ss = warp_sum(ss);
   const float r0 = rsqrtf(ss / d + eps);
+  if (ss_out) {
+    for (int t = 0; t < d / 128; ++t) {
+      float st = 0.f;
+      for (int j = 128 * t + lane; j < 128 * (t + 1); j += 32) {
+        const float v = to_f(e[j]) * r0;
+        x[(size_t)warp * d + j] = v;
+        h[(size_t)warp * d + j] = from_f<TA>(v);
+        st = fmaf(v, v, st);
+      }
+      st = warp_sum(st);
+      if (lane == 0) ss_out[(size_t)t * ss_ld + warp] = st;
+    }
+    return;
+  }
   // second norm of the (already normalised) row: its mean square is ss*r0^2/d
   float ss1 = 0.f;
   for (int j = lane; j < d; j += 32) {

@@ -154,6 +154,7 @@ struct nc_model {
   void* u = nullptr;                   // [max_rows][d_mlp]
   float* c32 = nullptr;                // fp32 path: raw QKV [max_rows][(n_head+2)*hd]
   void* h_last = nullptr;              // [max_batch][d]
+  float* ss_part = nullptr;            // decode: [d / 128][max_batch] per-block sums of squares of x
   int32_t* tok_stage = nullptr;
   float* logit_stage = nullptr;
   size_t logit_stage_bytes = 0;
@@ -209,7 +210,7 @@ void free_model(nc_model* m) {
   void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->k_alloc, m->v_alloc, m->x,
                   m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
                   m->tok_stage, m->logit_stage, m->err, m->part_o, m->part_ml, m->vt,
-                  m->d_len, m->att_counters};
+                  m->d_len, m->att_counters, m->ss_part};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete m;
@@ -356,15 +357,19 @@ int choose_splits(int tiles, int kb, int sms) {
   return best;
 }
 
-// Decode attention launch shape: sub-chunks of DEC_SUB keys per CTA (at least
-// two, so a row never has more partials than ceil(context / DEC_CHUNK)) chosen
-// for about two CTAs per SM over the batch; grid.x covers max_seq.
+// Decode attention launch shape: sub-chunks of DEC_SUB keys per CTA (a
+// group covers at least DEC_CHUNK keys, so a row never has more partials than
+// ceil(context / DEC_CHUNK)) chosen for one wave of one CTA per SM over the
+// batch (a CTA holds most of an SM's shared memory); grid.x covers max_seq.
+// A batch of num_sms / 2 rows or more gets one CTA per row, which writes its
+// output without a merge.
 void decode_attn_shape(const nc_model* m, int B, int* group, int* grid_x) {
   const int max_sub = (m->cfg.max_seq + DEC_SUB - 1) / DEC_SUB;
-  int target = (2 * m->num_sms + B / 2) / B;
+  int target = m->num_sms / B;
   if (target < 1) target = 1;
   int g = (max_sub + target - 1) / target;
-  if (g < 2) g = 2;
+  const int min_g = (DEC_CHUNK + DEC_SUB - 1) / DEC_SUB;
+  if (g < min_g) g = min_g;
   *group = g;
   *grid_x = (max_sub + g - 1) / g;
 }
@@ -417,11 +422,11 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
     if (bf)
       embed_rmsnorm_kernel<bf16, bf16><<<blocks_for_warps(M), 256, 0, s>>>(
           tok, static_cast<const bf16*>(m->E), m->x, static_cast<bf16*>(m->h), M, d, V, eps, m->err,
-          len_set, T);
+          len_set, T, (float*)nullptr, 0);
     else
       embed_rmsnorm_kernel<float, float><<<blocks_for_warps(M), 256, 0, s>>>(
           tok, static_cast<const float*>(m->E), m->x, static_cast<float*>(m->h), M, d, V, eps, m->err,
-          len_set, T);
+          len_set, T, (float*)nullptr, 0);
     m->launches++;
     NC_TRY(cudaGetLastError());
   }
@@ -474,7 +479,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
         const int ctx = pos0 + 1;                     // decode: T == 1
         int group = 2, gx = 1;
         decode_attn_shape(m, B, &group, &gx);
-        attn_decode_mma_kernel<<<dim3(gx, B), 128, ATT_DECODE_SMEM, s>>>(
+        attn_decode_mma_kernel<<<dim3(gx, B), DEC_THREADS, ATT_DECODE_SMEM, s>>>(
             static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
             static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, static_cast<bf16*>(m->att),
             m->att_counters, nh, c.max_seq, ctx, nullptr, kAttnScaleLog2, group);
@@ -619,10 +624,25 @@ nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logit
   const int NQKV = (nh + 2) * 128, NQ = nh * 128;
   const float eps = c.rms_eps;
   using bf16 = __nv_bfloat16;
+  // RMSNorm folded into the projections: every residual update writes
+  // h = bf16(x) and per-block sums of squares; QKV, MLP up and lm_head scale
+  // their rows by 1/rms(x) (r (x W^T) = (r x) W^T)
+  const int ss_ld = c.max_batch, n_ss = d / 128;
+  auto fold_in = [&](SkinnyArgs& a) {
+    a.ss_in = m->ss_part;
+    a.n_ss = n_ss;
+    a.ss_ld = ss_ld;
+  };
+  auto fold_out = [&](SkinnyArgs& a) {
+    a.h_out = static_cast<bf16*>(m->h);
+    a.ss_out = m->ss_part;
+    a.ss_ld = ss_ld;
+  };
   {
     KScope ks(m, NC_K_EMBED, s);
     embed_rmsnorm_kernel<bf16, bf16><<<blocks_for_warps(B), 256, 0, s>>>(
-        tok, static_cast<const bf16*>(m->E), m->x, static_cast<bf16*>(m->h), B, d, V, eps, m->err, nullptr, 0);
+        tok, static_cast<const bf16*>(m->E), m->x, static_cast<bf16*>(m->h), B, d, V, eps, m->err, nullptr, 0,
+        m->ss_part, ss_ld);
     m->launches++;
     NC_TRY(cudaGetLastError());
   }
@@ -638,13 +658,14 @@ nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logit
       a.pos_dev = m->d_len;
       a.n_head = nh;
       a.cache_S = c.max_seq;
+      fold_in(a);
       NC_TRY((launch_skinny<NB, EPI_QKV>(m, m->tm_w128[4 * l + 0], m->tm_h_nb, a, NQKV / 128, s)));
     }
     {
       KScope ks(m, NC_K_ATTN, s);
       int group = 2, gx = 1;
       decode_attn_shape(m, B, &group, &gx);
-      NC_TRY(launch_k(true, attn_decode_mma_kernel, dim3(gx, B), dim3(128), ATT_DECODE_SMEM, s,
+      NC_TRY(launch_k(true, attn_decode_mma_kernel, dim3(gx, B), dim3(DEC_THREADS), ATT_DECODE_SMEM, s,
                       static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
                       static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, static_cast<bf16*>(m->att),
                       m->att_counters, nh, (int)c.max_seq, 0, static_cast<const int*>(m->d_len),
@@ -655,38 +676,30 @@ nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logit
       KScope ks(m, NC_K_OPROJ, s);
       SkinnyArgs a = skinny_args(m, B, d, NQ, m->sk_splits[1]);
       a.x = m->x;
+      fold_out(a);
       NC_TRY((launch_skinny<NB, EPI_RESID>(m, m->tm_w128[4 * l + 1], m->tm_att_nb, a, d / 128, s)));
-    }
-    {
-      KScope ks(m, NC_K_NORM, s);
-      NC_TRY(launch_k(true, rmsnorm_kernel<bf16>, dim3(blocks_for_warps(B)), dim3(256), 0, s,
-                      static_cast<const float*>(m->x), static_cast<bf16*>(m->h), B, d, 1, 0, eps, (int*)nullptr));
-      m->launches++;
     }
     {
       KScope ks(m, NC_K_FC, s);
       SkinnyArgs a = skinny_args(m, B, F, d, m->sk_splits[2]);
       a.out_bf = static_cast<bf16*>(m->u);
+      fold_in(a);
       NC_TRY((launch_skinny<NB, EPI_RELU2>(m, m->tm_w128[4 * l + 2], m->tm_h_nb, a, F / 128, s)));
     }
     {
       KScope ks(m, NC_K_PROJ, s);
       SkinnyArgs a = skinny_args(m, B, d, F, m->sk_splits[3]);
       a.x = m->x;
+      fold_out(a);
       NC_TRY((launch_skinny<NB, EPI_RESID>(m, m->tm_w128[4 * l + 3], m->tm_u_nb, a, d / 128, s)));
-    }
-    {
-      KScope ks(m, NC_K_NORM, s);
-      int* len_inc = l == c.n_layer - 1 ? m->d_len : nullptr;
-      NC_TRY(launch_k(true, rmsnorm_kernel<bf16>, dim3(blocks_for_warps(B)), dim3(256), 0, s,
-                      static_cast<const float*>(m->x), static_cast<bf16*>(m->h), B, d, 1, 0, eps, len_inc));
-      m->launches++;
     }
   }
   {
     KScope ks(m, NC_K_LMHEAD, s);
     SkinnyArgs a = skinny_args(m, B, V, d, 1);
     a.x = logits;
+    fold_in(a);
+    a.len_inc = m->d_len;                            // the step's last kernel
     NC_TRY((launch_skinny<NB, EPI_LOGITS>(m, m->tm_wu128, m->tm_h_nb, a, V / 128, s)));
   }
   return NC_OK;
@@ -938,6 +951,7 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   CREATE_TRY(cudaMalloc(&m->att, R * NQ * m->wbytes));
   CREATE_TRY(cudaMalloc(&m->u, R * F * m->wbytes));
   CREATE_TRY(cudaMalloc(&m->h_last, (int64_t)c.max_batch * d * m->wbytes));
+  CREATE_TRY(cudaMalloc(&m->ss_part, (int64_t)(d / 128 + 1) * c.max_batch * 4));
   if (!m->bf16) CREATE_TRY(cudaMalloc(&m->c32, R * NQKV * 4));
   CREATE_TRY(cudaMalloc(&m->tok_stage, R * 4));
   if (m->bf16) {
@@ -957,7 +971,7 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   CREATE_TRY(cudaMemset(m->d_len, 0, sizeof(int)));
   CREATE_TRY(cudaMalloc(&m->att_counters, c.max_batch * sizeof(int)));
   CREATE_TRY(cudaMemset(m->att_counters, 0, c.max_batch * sizeof(int)));
-  if (m->bf16) {
+  if (m->bf16 && d <= SK_MAX_SS * 128) {
     // decode-step skinny GEMMs: batch padded to 32, 64 or 128 columns
     m->sk_nb = c.max_batch <= 32 ? 32 : (c.max_batch <= 64 ? 64 : 128);
     const int64_t Ns[4] = {NQKV, d, F, d}, Ks[4] = {d, NQ, d, F};
