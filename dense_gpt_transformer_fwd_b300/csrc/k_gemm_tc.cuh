@@ -45,6 +45,13 @@ struct GemmArgs {
   __nv_bfloat16* v_cache;         // this layer's V: [B_max][S][128]
   const float* rope_cos;          // [S][64]
   const float* rope_sin;          // [S][64]
+  const float* rope_cos_t;        // the same tables dim-major: [64][S]
+  const float* rope_sin_t;
+  // K and V caches of all layers as [rows][128] bf16 tensor maps in device
+  // memory ([0] K, [1] V; 32 x 64 boxes); this layer's cache row (b, pos) is
+  // kv_row0 + b * cache_S + pos
+  const CUtensorMap* tm_kv;
+  long long kv_row0;
   int n_head, T, pos0, cache_S;
   __nv_bfloat16* vt;              // optional V^T [B_max][128][vt_S] for the prefill attention
   int vt_S;
@@ -483,44 +490,54 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
         const int pos = args.pos0 + (my_row - b * args.T);
         const int pos_c = pos < args.cache_S ? pos : args.cache_S - 1;   // rows >= M only
         const uint32_t bufA = buf0, bufB = buf0 + C::EP_BUF;
+        // the warp's 32 rows are consecutive positions of one sequence (then
+        // the K/V cache rows are consecutive too): TMA stores to the cache
+        const int b0w = row0 / args.T;
+        const bool kv_tma = args.tm_kv != nullptr && row0 + 32 <= args.M && (row0 + 31) / args.T == b0w;
 #pragma unroll 1
         for (int hh = 0; hh < HALF / 128; ++hh) {
           const int head = ((n0 + ch0) >> 7) + hh;
           const bool is_v = head == args.n_head + 1;
           const uint32_t hbase = taddr + hh * 128;
+          // RoPE factors of dims c..c+31 at this row's position from the
+          // dim-major tables: for each dim the warp reads 32 consecutive
+          // positions (128 contiguous bytes).  Chunk 0's are requested before
+          // the QK-norm pass so that their latency overlaps it.
+          float rc[32], rs[32];
+          auto load_rope = [&](int c) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              rc[j] = __ldg(args.rope_cos_t + (size_t)(c + j) * args.cache_S + pos_c);
+              rs[j] = __ldg(args.rope_sin_t + (size_t)(c + j) * args.cache_S + pos_c);
+            }
+          };
           float scale = 1.f;
           if (!is_v) {
-            float ss = 0.f;
+            load_rope(0);
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
             for (int c = 0; c < 128; c += 32) {
               float v[32];
               tmem_ld32(hbase + c, v);
 #pragma unroll
-              for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+              for (int j = 0; j < 32; ++j) s4[j & 3] = fmaf(v[j], v[j], s4[j & 3]);
             }
-            scale = rsqrtf(ss * (1.f / 128.f) + args.eps);
+            scale = rsqrtf(((s4[0] + s4[1]) + (s4[2] + s4[3])) * (1.f / 128.f) + args.eps);
           }
           if (lane == 0) bulk_wait_read<0>();       // both buffers free
           __syncwarp();
 #pragma unroll 1
           for (int c = 0; c < 64; c += 32) {
             float a[32], bb[32];
+            if (!is_v && c > 0) load_rope(c);
             tmem_ld32(hbase + c, a);
             tmem_ld32(hbase + 64 + c, bb);
             if (!is_v) {
-              const float4* cp = reinterpret_cast<const float4*>(args.rope_cos + (size_t)pos_c * 64 + c);
-              const float4* sp = reinterpret_cast<const float4*>(args.rope_sin + (size_t)pos_c * 64 + c);
 #pragma unroll
-              for (int j4 = 0; j4 < 8; ++j4) {
-                const float4 cs = __ldg(cp + j4), sn = __ldg(sp + j4);
-                const float cc4[4] = {cs.x, cs.y, cs.z, cs.w}, sn4[4] = {sn.x, sn.y, sn.z, sn.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const int j = 4 * j4 + k;
-                  const float x0 = a[j] * scale, x1 = bb[j] * scale;
-                  a[j] = x0 * cc4[k] - x1 * sn4[k];
-                  bb[j] = x0 * sn4[k] + x1 * cc4[k];
-                }
+              for (int j = 0; j < 32; ++j) {
+                const float x0 = a[j] * scale, x1 = bb[j] * scale;
+                a[j] = x0 * rc[j] - x1 * rs[j];
+                bb[j] = x0 * rs[j] + x1 * rc[j];
               }
             }
             if (is_v && args.vt != nullptr && my_row < args.M) {
@@ -551,6 +568,16 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
             if (lane == 0) {
               tma_store_2d(&tmC, bufA, head * 128, row0);
               tma_store_2d(&tmC, bufB, head * 128 + 64, row0);
+              bulk_commit();
+            }
+          } else if (kv_tma) {
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const CUtensorMap* tkv = args.tm_kv + (is_v ? 1 : 0);
+              const int crow = (int)(args.kv_row0 + (long long)b0w * args.cache_S + args.pos0 + (row0 - b0w * args.T));
+              tma_store_2d(tkv, bufA, 0, crow);
+              tma_store_2d(tkv, bufB, 64, crow);
               bulk_commit();
             }
           } else {

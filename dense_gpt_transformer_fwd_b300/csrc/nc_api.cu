@@ -142,6 +142,9 @@ struct nc_model {
   std::vector<const void*> wqkv, wo, wfc, wproj;
   float* rope_cos = nullptr;           // [max_seq][hd/2]
   float* rope_sin = nullptr;
+  float* rope_cos_t = nullptr;         // [hd/2][max_seq] (dim-major copies)
+  float* rope_sin_t = nullptr;
+  CUtensorMap* d_tm_kv = nullptr;      // device: K and V caches of all layers as [rows][128] bf16
   void* k_alloc = nullptr;             // [guard][L][B_max][S][hd][guard]
   void* v_alloc = nullptr;
   int64_t kv_elems = 0, layer_elems = 0;
@@ -207,7 +210,8 @@ void free_model(nc_model* m) {
   for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
   if (m->g_exec) cudaGraphExecDestroy(m->g_exec);
   if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
-  void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->k_alloc, m->v_alloc, m->x,
+  void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->rope_cos_t, m->rope_sin_t, m->d_tm_kv,
+                  m->k_alloc, m->v_alloc, m->x,
                   m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
                   m->tok_stage, m->logit_stage, m->err, m->part_o, m->part_ml, m->vt,
                   m->d_len, m->att_counters, m->ss_part};
@@ -439,6 +443,10 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
         a.v_cache = static_cast<bf16*>(m->vc(l));
         a.rope_cos = m->rope_cos;
         a.rope_sin = m->rope_sin;
+        a.rope_cos_t = m->rope_cos_t;
+        a.rope_sin_t = m->rope_sin_t;
+        a.tm_kv = m->d_tm_kv;
+        a.kv_row0 = kGuardElems / 128 + (long long)l * c.max_batch * c.max_seq;
         a.n_head = nh;
         a.T = T;
         a.pos0 = pos0;
@@ -932,6 +940,16 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
     CREATE_TRY(cudaMalloc(&m->rope_sin, sn.size() * 4));
     CREATE_TRY(cudaMemcpy(m->rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
     CREATE_TRY(cudaMemcpy(m->rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
+    std::vector<float> cst(cs.size()), snt(sn.size());
+    for (int64_t p = 0; p < c.max_seq; ++p)
+      for (int64_t j = 0; j < half; ++j) {
+        cst[j * c.max_seq + p] = cs[p * half + j];
+        snt[j * c.max_seq + p] = sn[p * half + j];
+      }
+    CREATE_TRY(cudaMalloc(&m->rope_cos_t, cst.size() * 4));
+    CREATE_TRY(cudaMalloc(&m->rope_sin_t, snt.size() * 4));
+    CREATE_TRY(cudaMemcpy(m->rope_cos_t, cst.data(), cst.size() * 4, cudaMemcpyHostToDevice));
+    CREATE_TRY(cudaMemcpy(m->rope_sin_t, snt.data(), snt.size() * 4, cudaMemcpyHostToDevice));
   }
 
   // KV cache with sentinel guards
@@ -1010,6 +1028,15 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
       const uint64_t strides[2] = {256, (uint64_t)c.max_seq * 256};
       const uint32_t box[3] = {64, 128, 1};
       ok = make_tmap3(&m->tm_kc[l], m->kc(l), dims, strides, box);
+    }
+    // K and V caches of all layers (guards included) as [rows][128] for the
+    // prefill QKV epilogue's TMA stores
+    CUtensorMap kv[2];
+    ok = ok && make_tmap(&kv[0], m->k_alloc, (uint64_t)(m->kv_elems / 128), 128, 32) &&
+         make_tmap(&kv[1], m->v_alloc, (uint64_t)(m->kv_elems / 128), 128, 32);
+    if (ok) {
+      CREATE_TRY(cudaMalloc(&m->d_tm_kv, sizeof(kv)));
+      CREATE_TRY(cudaMemcpy(m->d_tm_kv, kv, sizeof(kv), cudaMemcpyHostToDevice));
     }
     if (!ok) {
       free_model(m);
