@@ -59,8 +59,11 @@ constexpr int ATT_HD = 128;
 // DEC_WARPS warps owns DEC_KPW keys of every sub-chunk.  One CTA fills most of
 // an SM's shared memory: its ring keeps two 64 KB sub-chunks in flight and
 // its 8 warps hide each other's MMA/softmax latency.  Partial results per
-// (row b, group g): m, l [B][ngroups][16][2], o [B][ngroups][16][128].
-constexpr int DEC_CHUNK = 128;             // context granularity of the partial buffers
+// (row b, group g) stay in the CTA's shared memory: the groups of a row are
+// the CTAs of one thread-block cluster (grid.x = cluster size <=
+// DEC_MAX_GROUPS), which merge through distributed shared memory.
+constexpr int DEC_CHUNK = 128;             // a group covers at least this many keys
+constexpr int DEC_MAX_GROUPS = 8;          // portable cluster size
 constexpr int DEC_SUB = 128;               // keys per pipeline stage
 constexpr int DEC_STAGES = 3;
 constexpr int DEC_WARPS = 8;
@@ -72,20 +75,19 @@ static_assert(DEC_CHUNK % DEC_SUB == 0 || DEC_SUB % DEC_CHUNK == 0, "partial buf
 
 __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kc,
-    const __nv_bfloat16* __restrict__ Vc, float* __restrict__ part_o, float* __restrict__ part_ml,
-    __nv_bfloat16* __restrict__ O, int* __restrict__ counters, int n_head, int cache_S, int ctx,
+    const __nv_bfloat16* __restrict__ Vc, __nv_bfloat16* __restrict__ O, int n_head, int cache_S, int ctx,
     const int* __restrict__ pos_dev, float scale_log2, int group) {
   pdl_trigger();
   // with pos_dev the context is read on the device (the step is graph-replayable);
   // the length only changes at the end of a step, so it may be read before
-  // waiting for the previous kernel.  Groups beyond the context exit.
+  // waiting for the previous kernel.  Groups beyond the context have no keys
+  // (they still take part in the cluster's barriers).
   if (pos_dev) ctx = *pos_dev + 1;
   const int nsub = (ctx + DEC_SUB - 1) / DEC_SUB;
   const int ngroups = (nsub + group - 1) / group;
   const int grp = blockIdx.x, b = blockIdx.y;
   const int c_begin = grp * group;
-  if (c_begin >= nsub) return;
-  const int n = min(group, nsub - c_begin);
+  const int n = max(0, min(group, nsub - c_begin));
   extern __shared__ __align__(128) uint8_t att_smem[];
   const uint32_t sQ = smem_u32(att_smem);                     // 16 rows
   const uint32_t sS = sQ + 16 * 256;                           // DEC_STAGES x (K, V) sub-chunks
@@ -257,7 +259,9 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
     }
   }
   if (ngroups == 1) {
-    // the CTA covered the whole context: normalise and write the output
+    // group 0 covered the whole context: normalise and write the output (no
+    // CTA of the cluster waits on a cluster barrier in this case)
+    if (grp != 0) return;
     float* inv_l1 = reinterpret_cast<float*>(att_smem);         // the Q tile is in registers
     if (tid < n_head) inv_l1[tid] = 1.f / cl;
     __syncthreads();
@@ -270,70 +274,48 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
     }
     return;
   }
-  // thread = output column of every other head row
-  const size_t pbase = ((size_t)b * ngroups + grp) * 16;
+  // ---- merge the groups of row b (the CTAs of this cluster, rank = grp):
+  // each parks its partial (o summed over its warps, m, l) in its own shared
+  // memory; after a cluster barrier CTA q merges head rows q, q + G, ... from
+  // every rank in rank order (the result does not depend on timing)
+  float* po = reinterpret_cast<float*>(att_smem + 16 * 256 + DEC_WARPS * 16 * 128 * 4);  // [16][128]
+  float* pml = po + 16 * 128;                                                            // [16][2]
   for (int r = tid >> 7; r < n_head; r += DEC_THREADS / 128) {
     float acc = 0.f;
 #pragma unroll
     for (int w = 0; w < DEC_WARPS; ++w) acc += ored[(w * 16 + r) * 128 + ocol];
-    part_o[(pbase + r) * 128 + ocol] = acc;
+    po[r * 128 + ocol] = acc;
   }
   if (tid < n_head) {
-    part_ml[(pbase + tid) * 2 + 0] = cm;
-    part_ml[(pbase + tid) * 2 + 1] = cl;
+    pml[tid * 2 + 0] = cm;
+    pml[tid * 2 + 1] = cl;
   }
-
-  // ---- the last group CTA of row b to finish merges every group (group
-  // order fixed, so the result does not depend on which CTA is last)
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&counters[b], 1) == ngroups - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (tid == 0) counters[b] = 0;                               // ready for the next call
-  float* wts = ored;                                           // [ngroups][16] merge weights
-  float* inv_l = red;                                          // [16]
-  __syncthreads();                                             // ored / red no longer read
-  const size_t rb = (size_t)b * ngroups * 16;
-  if (tid < n_head) {
+  cluster_sync_all();
+  const int G = (int)gridDim.x;
+  const uint32_t po_s = smem_u32(po), pml_s = smem_u32(pml);
+  for (int r = grp + G * (tid >> 7); r < n_head; r += G * (DEC_THREADS / 128)) {
+    float mg[DEC_MAX_GROUPS], lg[DEC_MAX_GROUPS], og[DEC_MAX_GROUPS];
+#pragma unroll
+    for (int g = 0; g < DEC_MAX_GROUPS; ++g) {
+      const bool in = g < G;
+      mg[g] = in ? ld_cluster_f32(pml_s + r * 8, (uint32_t)g) : -INFINITY;
+      lg[g] = in ? ld_cluster_f32(pml_s + r * 8 + 4, (uint32_t)g) : 0.f;
+      og[g] = in ? ld_cluster_f32(po_s + (r * 128 + ocol) * 4, (uint32_t)g) : 0.f;
+    }
     float gm = -INFINITY;
-    for (int c = 0; c < ngroups; ++c) gm = fmaxf(gm, __ldcg(part_ml + (rb + c * 16 + tid) * 2));
-    float l = 0.f;
-    for (int c = 0; c < ngroups; ++c) {
-      const float mc = __ldcg(part_ml + (rb + c * 16 + tid) * 2);
-      const float f = mc == -INFINITY ? 0.f : exp2f(mc - gm);
-      wts[c * 16 + tid] = f;
-      l += __ldcg(part_ml + (rb + c * 16 + tid) * 2 + 1) * f;
+#pragma unroll
+    for (int g = 0; g < DEC_MAX_GROUPS; ++g) gm = fmaxf(gm, mg[g]);
+    float l = 0.f, acc = 0.f;
+#pragma unroll
+    for (int g = 0; g < DEC_MAX_GROUPS; ++g) {
+      if (g >= G) break;
+      const float f = mg[g] == -INFINITY ? 0.f : exp2f(mg[g] - gm);
+      l += lg[g] * f;
+      acc += og[g] * f;
     }
-    inv_l[tid] = 1.f / l;
+    O[((size_t)b * n_head + r) * ATT_HD + ocol] = f2bf(acc * (1.f / l));
   }
-  __syncthreads();
-  // thread = output column; all chunks of two heads requested at once (the
-  // two halves of the CTA take alternate head pairs)
-  for (int h0 = 2 * (tid >> 7); h0 < n_head; h0 += DEC_THREADS / 64) {
-    float acc[2] = {0.f, 0.f};
-    for (int c0 = 0; c0 < ngroups; c0 += 8) {
-      float o8[2][8];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = c0 + i, h = h0 + hh;
-          o8[hh][i] = (c < ngroups && h < n_head) ? __ldcg(part_o + (rb + c * 16 + h) * 128 + ocol) : 0.f;
-        }
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (c0 + i < ngroups && h0 + hh < n_head) acc[hh] += o8[hh][i] * wts[(c0 + i) * 16 + h0 + hh];
-    }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh)
-      if (h0 + hh < n_head)
-        O[((size_t)b * n_head + h0 + hh) * ATT_HD + ocol] = f2bf(acc[hh] * inv_l[h0 + hh]);
-  }
+  cluster_sync_all();                                          // remote reads done before any CTA exits
 }
 
 constexpr size_t ATT_DECODE_SMEM = 16 * 256 + DEC_STAGES * (size_t)DEC_STAGE_BYTES + DEC_WARPS * 16 * 2 * 4;

@@ -80,17 +80,6 @@ struct SkCfg {
   static_assert((size_t)STAGES * STAGE_BYTES >= (size_t)NB * 128 * 4, "partial tile must fit the ring");
 };
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// all threads of all CTAs of the cluster; release/acquire orders the shared
-// memory writes before the barrier with the remote reads after it
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_addr, uint32_t rank) {
   uint32_t remote;
   float4 v;

@@ -288,6 +288,27 @@ cudaError_t launch_k(bool pdl, void (*k)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
 }
 
+// Decode attention: the grid.x groups of a row form one thread-block cluster
+// (they merge through distributed shared memory); `pdl` as for launch_k.
+template <typename... Args>
+cudaError_t launch_attn_decode(bool pdl, dim3 grid, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(DEC_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = ATT_DECODE_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = grid.x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, attn_decode_mma_kernel, std::forward<Args>(args)...);
+}
+
 // Prefill GEMM; tb is a weight map with a box of BN/2 rows.  cl selects the
 // form (with at least two M tiles): 0 one CTA per tile, 1 CTA pairs sharing
 // each weight tile by TMA multicast, 2 CTA pairs computing 256-row tiles with
@@ -362,15 +383,16 @@ int choose_splits(int tiles, int kb, int sms) {
 }
 
 // Decode attention launch shape: sub-chunks of DEC_SUB keys per CTA (a
-// group covers at least DEC_CHUNK keys, so a row never has more partials than
-// ceil(context / DEC_CHUNK)) chosen for one wave of one CTA per SM over the
-// batch (a CTA holds most of an SM's shared memory); grid.x covers max_seq.
-// A batch of num_sms / 2 rows or more gets one CTA per row, which writes its
-// output without a merge.
+// group covers at least DEC_CHUNK keys) chosen for one wave of one CTA per SM
+// over the batch (a CTA holds most of an SM's shared memory), at most
+// DEC_MAX_GROUPS groups (one cluster) per row; grid.x covers max_seq.  A batch
+// of num_sms / 2 rows or more gets one CTA per row, which writes its output
+// without a merge.
 void decode_attn_shape(const nc_model* m, int B, int* group, int* grid_x) {
   const int max_sub = (m->cfg.max_seq + DEC_SUB - 1) / DEC_SUB;
   int target = m->num_sms / B;
   if (target < 1) target = 1;
+  if (target > DEC_MAX_GROUPS) target = DEC_MAX_GROUPS;
   int g = (max_sub + target - 1) / target;
   const int min_g = (DEC_CHUNK + DEC_SUB - 1) / DEC_SUB;
   if (g < min_g) g = min_g;
@@ -487,12 +509,11 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
         const int ctx = pos0 + 1;                     // decode: T == 1
         int group = 2, gx = 1;
         decode_attn_shape(m, B, &group, &gx);
-        attn_decode_mma_kernel<<<dim3(gx, B), DEC_THREADS, ATT_DECODE_SMEM, s>>>(
-            static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
-            static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, static_cast<bf16*>(m->att),
-            m->att_counters, nh, c.max_seq, ctx, nullptr, kAttnScaleLog2, group);
+        NC_TRY(launch_attn_decode(false, dim3(gx, B), s, static_cast<const bf16*>(m->q),
+                                  static_cast<const bf16*>(m->kc(l)), static_cast<const bf16*>(m->vc(l)),
+                                  static_cast<bf16*>(m->att), nh, (int)c.max_seq, ctx, (const int*)nullptr,
+                                  kAttnScaleLog2, group));
         m->launches++;
-        NC_TRY(cudaGetLastError());
       } else {
         attn_simt_kernel<float, float><<<blocks_for_warps((int64_t)M * nh), 256, 0, s>>>(
             static_cast<const float*>(m->q), static_cast<const float*>(m->kc(l)),
@@ -673,11 +694,10 @@ nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logit
       KScope ks(m, NC_K_ATTN, s);
       int group = 2, gx = 1;
       decode_attn_shape(m, B, &group, &gx);
-      NC_TRY(launch_k(true, attn_decode_mma_kernel, dim3(gx, B), dim3(DEC_THREADS), ATT_DECODE_SMEM, s,
-                      static_cast<const bf16*>(m->q), static_cast<const bf16*>(m->kc(l)),
-                      static_cast<const bf16*>(m->vc(l)), m->part_o, m->part_ml, static_cast<bf16*>(m->att),
-                      m->att_counters, nh, (int)c.max_seq, 0, static_cast<const int*>(m->d_len),
-                      kAttnScaleLog2, group));
+      NC_TRY(launch_attn_decode(true, dim3(gx, B), s, static_cast<const bf16*>(m->q),
+                                static_cast<const bf16*>(m->kc(l)), static_cast<const bf16*>(m->vc(l)),
+                                static_cast<bf16*>(m->att), nh, (int)c.max_seq, 0,
+                                static_cast<const int*>(m->d_len), kAttnScaleLog2, group));
       m->launches++;
     }
     {
