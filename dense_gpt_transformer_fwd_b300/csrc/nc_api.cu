@@ -20,7 +20,6 @@
 #include <cstdlib>
 #include <cstdio>
 #include <cstring>
-#include <mutex>
 #include <new>
 #include <utility>
 #include <vector>
@@ -34,14 +33,6 @@
 #include "nc_common.cuh"
 
 using namespace nc;
-
-// Fixed scratch for nc_decode_step_noalloc: the split-context decode
-// attention's partial results, per (batch row, 128-key chunk, head slot of
-// 16) a 128-float output plus (max, sum).  Sized for B * chunks <= 2560
-// (21.3 MB); every GPU that loads this library holds it until exit.
-constexpr int64_t kNoAllocMaxRowChunks = 2560;
-constexpr int64_t kNoAllocFloats = kNoAllocMaxRowChunks * 16 * (128 + 2);
-static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
 
 namespace {
 
@@ -175,7 +166,6 @@ struct nc_model {
   size_t ev_used = 0;
   std::vector<ProfRec> recs;
   int* d_len = nullptr;                // device copy of the cache length (decode reads it)
-  int* att_counters = nullptr;         // decode attention: chunks finished per batch row
   // decode-step skinny GEMMs (bf16, B <= sk_nb)
   int sk_nb = 0;                       // padded batch of the MMA N operand: 32, 64 or 128 (0 = off)
   int sk_splits[4] = {1, 1, 1, 1};     // K splits of QKV, O-proj, FC, PROJ
@@ -192,9 +182,6 @@ struct nc_model {
   int vt_S = 0;
   CUtensorMap tm_vt{};                 // 3-D map over vt, box 64 keys x 128 dims
   std::vector<CUtensorMap> tm_kc;      // per layer 3-D map over the K cache, box 64 x 128 keys
-  float* part_o = nullptr;             // decode attention partials [max_batch][chunks][16][128]
-  float* part_ml = nullptr;            // [max_batch][chunks][16][2]
-  int max_chunks = 0;
   // A-operand maps (box 64 x 128), epilogue maps (box 128 B x 32); weight maps below
   CUtensorMap tm_h{}, tm_att{}, tm_u{}, tm_hlast{};
   CUtensorMap tm_q_st{}, tm_x_st{}, tm_u_st{};
@@ -213,8 +200,7 @@ void free_model(nc_model* m) {
   void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->rope_cos_t, m->rope_sin_t, m->d_tm_kv,
                   m->k_alloc, m->v_alloc, m->x,
                   m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
-                  m->tok_stage, m->logit_stage, m->err, m->part_o, m->part_ml, m->vt,
-                  m->d_len, m->att_counters, m->ss_part};
+                  m->tok_stage, m->logit_stage, m->err, m->vt, m->d_len, m->ss_part};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete m;
@@ -832,26 +818,6 @@ __global__ void wait_nothing_kernel(int* err, unsigned long long limit_ns) {
   if (threadIdx.x == 0 && !mbar_wait(smem_u32(&bar), 0, limit_ns)) atomicOr(err, NC_DEVFLAG_TIMEOUT);
 }
 
-// Device address of g_noalloc_scratch for `device` (which must be current).
-// Host code only sees a stand-in for the array's name, so the address is
-// looked up once per device with cudaGetSymbolAddress and cached.
-constexpr int kMaxDevices = 64;
-float* g_noalloc_ptr[kMaxDevices] = {};
-std::mutex g_noalloc_mu;
-
-nc_status noalloc_scratch(int device, float** out) {
-  if (device < 0 || device >= kMaxDevices) return NC_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[device]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) return NC_ERR_CUDA;
-    g_noalloc_ptr[device] = static_cast<float*>(p);
-  }
-  *out = g_noalloc_ptr[device];
-  return NC_OK;
-}
-
 }  // namespace
 
 extern "C" {
@@ -871,7 +837,7 @@ const char* nc_status_string(nc_status s) {
     case NC_ERR_TOKEN: return "token id out of range";
     case NC_ERR_TIMEOUT: return "device wait timed out";
     case NC_ERR_CUDA: return "CUDA error";
-    case NC_ERR_SCRATCH_LIMIT: return "batch x context exceeds the fixed no-allocation scratch";
+    case NC_ERR_SCRATCH_LIMIT: return "reserved (not returned by this version)";
   }
   return "unknown status";
 }
@@ -993,9 +959,6 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   if (!m->bf16) CREATE_TRY(cudaMalloc(&m->c32, R * NQKV * 4));
   CREATE_TRY(cudaMalloc(&m->tok_stage, R * 4));
   if (m->bf16) {
-    m->max_chunks = (c.max_seq + DEC_CHUNK - 1) / DEC_CHUNK;
-    CREATE_TRY(cudaMalloc(&m->part_o, (int64_t)c.max_batch * m->max_chunks * 16 * 128 * 4));
-    CREATE_TRY(cudaMalloc(&m->part_ml, (int64_t)c.max_batch * m->max_chunks * 16 * 2 * 4));
     CREATE_TRY(cudaFuncSetAttribute(attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)ATC_SMEM));
     m->vt_S = (c.max_seq + 127) / 128 * 128;
@@ -1007,8 +970,6 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   CREATE_TRY(cudaMalloc(&m->err, sizeof(int)));
   CREATE_TRY(cudaMalloc(&m->d_len, sizeof(int)));
   CREATE_TRY(cudaMemset(m->d_len, 0, sizeof(int)));
-  CREATE_TRY(cudaMalloc(&m->att_counters, c.max_batch * sizeof(int)));
-  CREATE_TRY(cudaMemset(m->att_counters, 0, c.max_batch * sizeof(int)));
   if (m->bf16 && d <= SK_MAX_SS * 128) {
     // decode-step skinny GEMMs: batch padded to 32, 64 or 128 columns
     m->sk_nb = c.max_batch <= 32 ? 32 : (c.max_batch <= 64 ? 64 : 128);
@@ -1114,22 +1075,11 @@ nc_status nc_decode_step_noalloc(nc_model* m, const int32_t* tokens, int32_t B, 
   if (B != m->batch) return NC_ERR_INVALID_ARG;
   if (m->length >= m->cfg.max_seq) return NC_ERR_CAPACITY;
   if (!is_device_ptr(tokens) || !is_device_ptr(logits)) return NC_ERR_INVALID_ARG;
-  const int64_t nchunk = (m->length + 1 + DEC_CHUNK - 1) / DEC_CHUNK;
-  if ((int64_t)B * nchunk > kNoAllocMaxRowChunks) return NC_ERR_SCRATCH_LIMIT;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != m->device) return NC_ERR_INVALID_ARG;
-  float* scratch = nullptr;
-  nc_status st = noalloc_scratch(dev, &scratch);
-  if (st != NC_OK) return st;
-  // the decode attention reads its partial buffers from the model: point them
-  // at the fixed scratch for this call only
-  float* const keep_o = m->part_o;
-  float* const keep_ml = m->part_ml;
-  m->part_o = scratch;
-  m->part_ml = scratch + (int64_t)B * nchunk * 16 * 128;
-  st = forward_decode(m, tokens, B, logits, stream);
-  m->part_o = keep_o;
-  m->part_ml = keep_ml;
+  // every buffer of the step is model-owned and sized at creation; the eager
+  // launch sequence (no graph instantiation) allocates nothing
+  const nc_status st = forward_decode(m, tokens, B, logits, stream);
   if (st != NC_OK) return st;
   m->length += 1;
   return NC_OK;

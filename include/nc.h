@@ -55,7 +55,7 @@ typedef enum {
   NC_ERR_TOKEN = 6,       /* (device) a token id outside [0, vocab) was seen */
   NC_ERR_TIMEOUT = 7,     /* (device) a bounded pipeline wait expired */
   NC_ERR_CUDA = 8,        /* a CUDA runtime error */
-  NC_ERR_SCRATCH_LIMIT = 9 /* the call needs more than nc_decode_step_noalloc's fixed scratch */
+  NC_ERR_SCRATCH_LIMIT = 9 /* reserved: earlier versions of nc_decode_step_noalloc returned it */
 } nc_status;
 
 typedef enum { NC_F32 = 0, NC_BF16 = 1 } nc_dtype;
@@ -134,22 +134,16 @@ NC_API nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, f
  * grows a staging buffer the first time it is given host logits); this call
  * never calls cudaMalloc, cudaFree or any allocating routine.
  *
- * Same arguments, state rules and results as nc_decode_step, with two limits:
- *  - tokens and logits must be device pointers (host buffers would need
- *    staging memory): otherwise NC_ERR_INVALID_ARG;
- *  - the split-context attention keeps its partial results in one fixed
- *    scratch array compiled into the library (21.3 MB of device memory, held by
- *    every GPU that loads the library until the process exits), which fits
- *    B * ceil((length + 1) / 128) <= 2560; a larger call returns
- *    NC_ERR_SCRATCH_LIMIT with nothing enqueued.
+ * Same arguments, state rules and results as nc_decode_step, except that
+ * tokens and logits must be device pointers (host buffers would need staging
+ * memory): otherwise NC_ERR_INVALID_ARG.  Every intermediate of the step lives
+ * in buffers the model allocated at creation (the split-context attention
+ * merges its partial results in on-chip shared memory), and the step is
+ * launched kernel by kernel rather than through a CUDA graph (whose
+ * instantiation would allocate).  Calls on different models do not share any
+ * memory.
  * Only bf16 models (NC_ERR_UNSUPPORTED otherwise); the current device must be
  * the model's device (NC_ERR_INVALID_ARG otherwise).
- * The first call on a device looks up that device's address of the scratch
- * array (cudaGetSymbolAddress); make that first call before any stream capture.
- * Every call, from every model on the device, shares the one array: calls that
- * may overlap on the GPU (different streams, no ordering between them) race on
- * it and must be serialized by the caller.  Each call writes every scratch
- * entry it later reads, so nothing needs clearing between calls.
  */
 NC_API nc_status nc_decode_step_noalloc(nc_model* m, const int32_t* tokens, int32_t B,
                                         float* logits, nc_stream_t stream);
