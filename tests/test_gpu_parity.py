@@ -113,6 +113,37 @@ def test_decode_graph_replay_matches_oracle_and_eager(B, T, steps):
     e.close()
 
 
+def test_decode_attention_cluster_of_eight_groups():
+    """Small batch, long context: the decode attention splits each row over a
+    cluster of 8 group CTAs (max_seq 2048 -> 16 sub-chunks of 128 keys, 2 per
+    group); at context 1501..1503 groups 6 and 7 hold no keys and only take part
+    in the cluster barriers.  Graph-replayed steps match the oracle and the
+    eager steps of a second model bit for bit."""
+    sh = small_bf16_shape(n_layer=2, vocab=2048)
+    flat = nc_inputs.gen_weights(sh, 71)
+    B, T, steps, S = 2, 1500, 3, 2048
+    prompt = nc_inputs.gen_tokens(sh.vocab, (B, T), 72)
+    nxt = nc_inputs.gen_tokens(sh.vocab, (steps, B), 73)
+    o = oracle_for(flat, sh)
+    o.prefill(prompt, logit_positions=[T - 1])
+    g = ncp.Model(sh, flat, max_batch=B, max_seq=S)
+    e = ncp.Model(sh, flat, max_batch=B, max_seq=S)
+    g.prefill(to_dev(prompt), last_only=True)
+    e.prefill(to_dev(prompt), last_only=True)
+    out = torch.full((B, sh.vocab), float("nan"), device="cuda")
+    for t in range(steps):
+        tok = to_dev(nxt[t])
+        got = g.decode_step(tok, out=out).cpu().numpy()
+        ref = e.decode_step(tok).cpu().numpy()
+        np.testing.assert_array_equal(got, ref)
+        check_close(got, o.decode(nxt[t]), "bf16", f"clustered decode step {t}")
+    g.sync()
+    e.sync()
+    assert g.kv_length() == e.kv_length() == (T + steps, B)
+    g.close()
+    e.close()
+
+
 def test_small_bf16_last_only_and_host_buffers():
     sh = small_bf16_shape()
     flat = nc_inputs.gen_weights(sh, 23)
