@@ -7,11 +7,13 @@
 // nanochat works" item 5).
 //
 // Decode kernel (split over the context): one CTA = one batch row and a
-// group of consecutive 64-key sub-chunks streamed through a cp.async ring;
+// group of consecutive 128-key sub-chunks streamed through a cp.async ring;
 // the row's n_head query vectors form the 16-row A operand (heads padded to
-// 16), each warp handles 16 keys of every sub-chunk with a running softmax;
-// partial (max, sum, output) go to a workspace, and the last CTA of the row
-// to finish (a per-row counter) merges the groups into the bf16 output.
+// 16), each of 8 warps handles 16 keys of every sub-chunk with a running
+// softmax.  A row covered by one group writes its output directly; otherwise
+// the groups of the row form a thread-block cluster, and they merge their
+// partial (max, sum, output) through distributed shared memory into the bf16
+// output.
 #pragma once
 
 #include "nc_common.cuh"

@@ -77,7 +77,8 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, TA* __restrict__ h, 
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
   pdl_wait();
-  // the final norm of a decode step advances the device-side cache length;
+  // the final norm of a decode step on the generic path (fp32 models, or a
+  // batch wider than the decode GEMMs) advances the device-side cache length;
   // every kernel of the step that reads it has finished (stream order)
   if (len_inc && blockIdx.x == 0 && threadIdx.x == 0) *len_inc += 1;
   if (warp >= rows) return;

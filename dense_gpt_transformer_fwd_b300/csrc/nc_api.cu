@@ -556,7 +556,8 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       const bool final_last = last_only && l == c.n_layer - 1;
       const int rows = final_last ? B : M;
       void* dst = final_last ? m->h_last : m->h;
-      // a decode step (pos0 > 0) advances the device-side length in its final norm
+      // a decode step on this generic path (pos0 > 0) advances the device-side
+      // length in its final norm
       int* len_inc = (pos0 > 0 && l == c.n_layer - 1) ? m->d_len : nullptr;
       if (bf)
         rmsnorm_kernel<bf16><<<blocks_for_warps(rows), 256, 0, s>>>(
