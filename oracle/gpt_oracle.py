@@ -31,8 +31,21 @@ Readings taken where the pages are silent or garbled (identical in the CUDA path
   R7 softcap(z) = c * tanh(z / c), c = 15 [yelogs].
   R8 no biases anywhere [yelogs]; untied E and Wu [yelogs], [apidog 1].
   R9 weights enter as the bf16-rounded values for bf16 models, then fp64.
+  R10 engine steps on either side of the pass [apidog 6], [szyisi inference
+     engine]: a prompt may be prefilled in chunks (each chunk continues the
+     cache); "batch generation clones the KV cache for parallel sampling" is
+     read as copying one row's cache to every row of the batch.
+  R11 sampling (the pages name parallel sampling but not its rule; plainest
+     reading): temperature 0 is greedy, the lowest index among equal maxima;
+     otherwise the candidates are ordered by (logit descending, index
+     ascending), the first top_k are kept (0 keeps all), p_i is proportional to
+     exp((l_i - l_max) / temperature), and a uniform draw u in [0, 1) picks the
+     first candidate whose cumulative probability exceeds u.  The draws are
+     inputs.
 """
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -233,3 +246,54 @@ class OracleModel:
             raise RuntimeError("decode before prefill")
         tokens = np.asarray(tokens).reshape(-1, 1)
         return self._forward(tokens)[:, 0, :]
+
+    def extend(self, tokens, logit_positions=None):
+        """Chunked prefill (R10): T more positions per row after the cached
+        ones, from ``self.length``; logits [B, T, V] (or the listed positions)."""
+        if self.length == 0:
+            raise RuntimeError("extend before prefill")
+        return self._forward(tokens, logit_positions)
+
+    def clone_row(self, src, n):
+        """Batch generation (R10): the cache becomes n copies of row ``src``."""
+        if self.length == 0:
+            raise RuntimeError("clone before prefill")
+        for li in range(self.s.n_layer):
+            self.k_cache[li] = np.repeat(self.k_cache[li][src:src + 1], n, axis=0)
+            self.v_cache[li] = np.repeat(self.v_cache[li][src:src + 1], n, axis=0)
+
+
+# --------------------------------------------------------------------------- #
+# sampling the next token (R11)
+# --------------------------------------------------------------------------- #
+
+
+def sample_tokens(logits, temperature, top_k, u):
+    """Next token per row from logits [B, V] (R11).
+
+    temperature == 0: argmax, the lowest index among equal maxima.  Otherwise
+    the candidates are ordered by (logit descending, index ascending), the first
+    top_k kept (top_k == 0 keeps all V), weighted by exp((l - l_max) / T) and
+    the first whose cumulative weight exceeds u[b] times the total is taken.
+    """
+    logits = np.asarray(logits, dtype=np.float64)
+    B, V = logits.shape
+    u = np.asarray(u, dtype=np.float64).reshape(B)
+    out = np.empty(B, dtype=np.int64)
+    for b in range(B):
+        row = logits[b]
+        if temperature == 0:
+            out[b] = int(np.flatnonzero(row == row.max())[0])
+            continue
+        order = sorted(range(V), key=lambda i: (-row[i], i))
+        keep = order if top_k <= 0 else order[:top_k]
+        w = np.array([math.exp((row[i] - row[keep[0]]) / temperature) for i in keep])
+        total = w.sum()
+        cum, pick = 0.0, keep[-1]
+        for i, wi in zip(keep, w):
+            cum += wi
+            if cum > u[b] * total:
+                pick = i
+                break
+        out[b] = pick
+    return out
