@@ -66,9 +66,9 @@ struct GemmArgs {
   unsigned long long wait_limit_ns;
 };
 
-// CL = 0: one CTA per tile; 1: pairs sharing W by multicast; 2: CTA pairs
-// computing a 256 x BN tile with tcgen05.mma.cta_group::2 (each CTA holds its
-// 128 rows of A and half of the W tile)
+// CL = 0: one CTA per 128 x BN tile; 2: CTA pairs computing a 256 x BN tile
+// with tcgen05.mma.cta_group::2 (each CTA holds its 128 rows of A and half of
+// the W tile)
 template <int BN, int EPI, int CL = 0>
 struct TcCfg {
   // K per pipeline stage: 128 (two 64-column boxes per operand) for CTA pairs,
@@ -125,26 +125,6 @@ __device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, uint32_t src
       : "memory");
 }
 
-// TMA load of one box, written at the same shared-memory offset of every CTA
-// in `mask` within the cluster; each destination CTA's mbarrier (same offset)
-// receives the completed bytes
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
-      : "memory");
-}
-// arrive on the mbarrier at the same offset in every CTA of `mask` once all
-// previously issued tcgen05.mma of this thread have completed
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          bar),
-      "h"(mask)
-      : "memory");
-}
 // ------------------------------------------------- CTA-pair (cta_group::2)
 // Tensor memory is allocated and freed collectively by one warp of each CTA
 // of the pair; the address is written to each CTA's shared memory.
@@ -198,11 +178,6 @@ __device__ __forceinline__ void cluster_barrier_all() {
 }
 
 // tmB's box is BN/2 rows x 64 columns.
-// MC = true: launched as clusters of two CTAs along M that work on the same
-// weight tile at the same time; each CTA loads half of every W box (BN/2 rows,
-// tmB's box) and multicasts it to both, so each CTA reads a third less from
-// L2 per MMA.  A stage of either CTA is refilled only after both CTAs' MMAs
-// have released it (the MMA commit arrives on both CTAs' empty barrier).
 // CL = 2: launched as clusters of two CTAs along M.  The even CTA (the
 // leader) issues tcgen05.mma.cta_group::2 for the 256-row tile of the pair;
 // each CTA loads its own 128 rows of A and BN/2 rows of W, and both CTAs'
@@ -215,8 +190,8 @@ template <int BN, int EPI, int CL = 0>
 __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
-  constexpr bool MC = CL != 0;                     // tiles come in vertical pairs
-  constexpr bool PAIR = CL == 2;
+  static_assert(CL == 0 || CL == 2, "one CTA per tile, or CTA pairs on cta_group::2");
+  constexpr bool PAIR = CL == 2;                   // tiles come in vertical pairs
   using C = TcCfg<BN, EPI, CL>;
   constexpr int BM = C::BM, BK = C::BK, STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -232,16 +207,16 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_m = (args.M + BM - 1) / BM;
   const int num_n = args.N / BN;
-  // work units: tiles, or (MC) pairs of vertically adjacent tiles, m fastest
+  // work units: tiles, or (PAIR) pairs of vertically adjacent tiles, m fastest
   const int num_m2 = (num_m + 1) / 2;
-  const int rank = MC ? (int)(blockIdx.x & 1) : 0;
-  const int unit0 = MC ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int ustride = MC ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  const int num_units = MC ? num_m2 * num_n : num_m * num_n;
-  const int num_mu = MC ? num_m2 : num_m;          // m positions of a unit
+  const int rank = PAIR ? (int)(blockIdx.x & 1) : 0;
+  const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ustride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int num_units = PAIR ? num_m2 * num_n : num_m * num_n;
+  const int num_mu = PAIR ? num_m2 : num_m;          // m positions of a unit
   auto unit_m = [&](int u) { return args.n_fast ? u / num_n : u % num_mu; };
   auto unit_n = [&](int u) { return args.n_fast ? u % num_n : u / num_mu; };
-  auto unit_m0 = [&](int u) { return MC ? (unit_m(u) * 2 + rank) * BM : unit_m(u) * BM; };
+  auto unit_m0 = [&](int u) { return PAIR ? (unit_m(u) * 2 + rank) * BM : unit_m(u) * BM; };
   auto unit_n0 = [&](int u) { return unit_n(u) * BN; };
   const int KB = (args.K + BK - 1) / BK;
   const uint64_t limit = args.wait_limit_ns;
@@ -253,7 +228,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar(FULL + s), 1);
-      mbar_init(bar(EMPTY + s), CL == 1 ? 2 : 1);
+      mbar_init(bar(EMPTY + s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar(TFULL + a), 1);
@@ -268,7 +243,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
   }
-  if constexpr (MC) {
+  if constexpr (PAIR) {
     // the peer's barriers are initialised before any remote arrive or copy
     __syncthreads();
     cluster_barrier_all();
@@ -326,14 +301,9 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
           mbar_arrive_expect_tx(bar(FULL + stage), C::STAGE_BYTES);
           tma_load_2d(smem_u32(sA + stage * C::A_BYTES), &tmA, bar(FULL + stage), kb * BK, m0);
           // W boxes are BN/2 rows; the two halves sit back to back in the stage
-          if constexpr (MC) {
-            tma_load_2d_mc(smem_u32(sB + stage * C::B_BYTES + rank * (C::B_BYTES / 2)), &tmB, bar(FULL + stage),
-                           kb * BK, n0 + rank * (BN / 2), (uint16_t)0x3);
-          } else {
-            tma_load_2d(smem_u32(sB + stage * C::B_BYTES), &tmB, bar(FULL + stage), kb * BK, n0);
-            tma_load_2d(smem_u32(sB + stage * C::B_BYTES + C::B_BYTES / 2), &tmB, bar(FULL + stage), kb * BK,
-                        n0 + BN / 2);
-          }
+          tma_load_2d(smem_u32(sB + stage * C::B_BYTES), &tmB, bar(FULL + stage), kb * BK, n0);
+          tma_load_2d(smem_u32(sB + stage * C::B_BYTES + C::B_BYTES / 2), &tmB, bar(FULL + stage), kb * BK,
+                      n0 + BN / 2);
           issued[stage] = (int)phase;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -386,8 +356,6 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
           any = true;
           if constexpr (PAIR)
             tc_commit_pair(bar(EMPTY + stage), (uint16_t)0x3);
-          else if constexpr (MC)
-            tc_commit_mc(bar(EMPTY + stage), (uint16_t)0x3);
           else
             tc_commit(bar(EMPTY + stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -615,9 +583,9 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  // (MC) no CTA leaves while its peer may still signal its barriers or, for a
-  // pair, write its tensor memory
-  if constexpr (MC) cluster_barrier_all();
+  // (pair) no CTA leaves while its peer may still signal its barriers or
+  // write its tensor memory
+  if constexpr (PAIR) cluster_barrier_all();
   tc_fence_after();
   if (warp == 1) {
     if constexpr (PAIR)

@@ -92,13 +92,19 @@ bool make_tmap3(CUtensorMap* tm, const void* ptr, const uint64_t dims[3], const 
   return r == CUDA_SUCCESS;
 }
 
-bool is_device_ptr(const void* p) {
+// Where a buffer lives: PTR_HOST (pageable or pinned host memory),
+// PTR_DEVICE (memory of device `dev`, or managed memory) or PTR_OTHER_DEVICE
+// (device memory of another GPU, which no call accepts).
+enum PtrKind { PTR_HOST = 0, PTR_DEVICE = 1, PTR_OTHER_DEVICE = 2 };
+PtrKind ptr_kind(const void* p, int dev) {
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     cudaGetLastError();
-    return false;
+    return PTR_HOST;
   }
-  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+  if (a.type == cudaMemoryTypeManaged) return PTR_DEVICE;
+  if (a.type == cudaMemoryTypeDevice) return a.device == dev ? PTR_DEVICE : PTR_OTHER_DEVICE;
+  return PTR_HOST;
 }
 
 // last CUDA error this thread turned into NC_ERR_CUDA / NC_ERR_OOM
@@ -296,9 +302,8 @@ cudaError_t launch_attn_decode(bool pdl, dim3 grid, cudaStream_t s, Args&&... ar
 }
 
 // Prefill GEMM; tb is a weight map with a box of BN/2 rows.  cl selects the
-// form (with at least two M tiles): 0 one CTA per tile, 1 CTA pairs sharing
-// each weight tile by TMA multicast, 2 CTA pairs computing 256-row tiles with
-// tcgen05.mma.cta_group::2.
+// form (with at least two M tiles): 0 one CTA per tile, 2 CTA pairs computing
+// 256-row tiles with tcgen05.mma.cta_group::2.
 template <int BN, int EPI, int CL>
 cudaError_t set_gemm_smem() {
   return cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -332,17 +337,8 @@ cudaError_t launch_gemm_cl(nc_model* m, const CUtensorMap& ta, const CUtensorMap
 template <int BN, int EPI>
 cudaError_t launch_gemm_tc(nc_model* m, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const GemmArgs& a, cudaStream_t s, int cl = 0) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = set_gemm_smem<BN, EPI, 0>();
-    if (e == cudaSuccess) e = set_gemm_smem<BN, EPI, 1>();
-    if (e == cudaSuccess) e = set_gemm_smem<BN, EPI, 2>();
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   const int num_m = (a.M + 127) / 128, num_n = a.N / BN;
   if (num_m * num_n == 0) return cudaSuccess;
-  if (cl == 1 && num_m >= 2) return launch_gemm_cl<BN, EPI, 1>(m, ta, tb, tc, a, s);
   if (cl == 2 && num_m >= 2) return launch_gemm_cl<BN, EPI, 2>(m, ta, tb, tc, a, s);
   using C = TcCfg<BN, EPI, 0>;
   const int tiles = num_m * num_n;
@@ -589,13 +585,6 @@ template <int NB, int EPI>
 cudaError_t launch_skinny(nc_model* m, const CUtensorMap& tw, const CUtensorMap& ta, SkinnyArgs a, int tiles,
                           cudaStream_t s) {
   using C = SkCfg<NB>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles, a.splits, 1);
   cfg.blockDim = dim3(128, 1, 1);
@@ -720,6 +709,66 @@ nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logit
   return NC_OK;
 }
 
+// Every kernel a model can launch is loaded and given its dynamic shared
+// memory limit here, on the model's device, when the model is created.  The
+// CUDA runtime loads kernels lazily and function attributes are per device,
+// so no later call loads a module or sets an attribute (a first launch could
+// otherwise allocate device memory inside a call).
+template <int EPI>
+cudaError_t configure_gemm_tc() {
+  cudaError_t e = set_gemm_smem<256, EPI, 0>();
+  return e != cudaSuccess ? e : set_gemm_smem<256, EPI, 2>();
+}
+template <int NB>
+cudaError_t configure_skinny() {
+  const int sm = (int)SkCfg<NB>::SMEM;
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI_QKV>, a, sm);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI_RESID>, a, sm);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI_RELU2>, a, sm);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI_LOGITS>, a, sm);
+  return e;
+}
+template <typename K>
+cudaError_t load_kernel(K* k) {
+  cudaFuncAttributes fa;
+  return cudaFuncGetAttributes(&fa, k);
+}
+
+cudaError_t configure_kernels(const nc_model* m) {
+  using bf16 = __nv_bfloat16;
+  cudaError_t e = cudaSuccess;
+  auto step = [&](cudaError_t r) {
+    if (e == cudaSuccess) e = r;
+  };
+  if (m->bf16) {
+    step(configure_gemm_tc<EPI_QKV>());
+    step(configure_gemm_tc<EPI_RESID>());
+    step(configure_gemm_tc<EPI_RELU2>());
+    step(configure_gemm_tc<EPI_LOGITS>());
+    step(configure_gemm_tc<EPI_STORE>());
+    step(configure_skinny<32>());
+    step(configure_skinny<64>());
+    step(configure_skinny<128>());
+    step(cudaFuncSetAttribute(attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)ATC_SMEM));
+    step(cudaFuncSetAttribute(attn_decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)ATT_DECODE_SMEM));
+    step(load_kernel(embed_rmsnorm_kernel<bf16, bf16>));
+    step(load_kernel(rmsnorm_kernel<bf16>));
+  } else {
+    step(load_kernel(gemm_simt_f32_kernel<SEPI_STORE>));
+    step(load_kernel(gemm_simt_f32_kernel<SEPI_RESID>));
+    step(load_kernel(gemm_simt_f32_kernel<SEPI_RELU2>));
+    step(load_kernel(gemm_simt_f32_kernel<SEPI_LOGITS>));
+    step(load_kernel(qkv_post_kernel<float, float>));
+    step(load_kernel(attn_simt_kernel<float, float>));
+    step(load_kernel(embed_rmsnorm_kernel<float, float>));
+    step(load_kernel(rmsnorm_kernel<float>));
+  }
+  return e;
+}
+
 bool decode_on_skinny(const nc_model* m, int B) { return m->bf16 && m->sk_nb > 0 && B <= m->sk_nb; }
 
 nc_status forward_decode(nc_model* m, const int32_t* tok, int B, float* logits, cudaStream_t s) {
@@ -783,14 +832,16 @@ nc_status decode_graph(nc_model* m, const int32_t* tok, int B, float* logits, cu
 nc_status run_call(nc_model* m, const int32_t* tokens, int B, int T, int pos0, float* logits,
                    bool last_only, cudaStream_t s) {
   const int M = B * T;
+  const PtrKind tk = ptr_kind(tokens, m->device), lk = ptr_kind(logits, m->device);
+  if (tk == PTR_OTHER_DEVICE || lk == PTR_OTHER_DEVICE) return NC_ERR_INVALID_ARG;
   const int32_t* tok_dev = tokens;
-  if (!is_device_ptr(tokens)) {
+  if (tk == PTR_HOST) {
     NC_TRY(cudaMemcpyAsync(m->tok_stage, tokens, (size_t)M * 4, cudaMemcpyHostToDevice, s));
     tok_dev = m->tok_stage;
   }
   const size_t out_bytes = (size_t)(last_only ? B : M) * m->cfg.vocab * 4;
   float* out_dev = logits;
-  const bool host_out = !is_device_ptr(logits);
+  const bool host_out = lk == PTR_HOST;
   if (host_out) {
     if (m->logit_stage_bytes < out_bytes) {
       NC_TRY(cudaStreamSynchronize(s));
@@ -876,7 +927,12 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   CREATE_TRY(cudaMalloc(&m->weights, n_params * m->wbytes));
   if (m->bf16) {
     float* tmp = nullptr;
-    const bool dev_src = is_device_ptr(weights);
+    const PtrKind wk = ptr_kind(weights, m->device);
+    if (wk == PTR_OTHER_DEVICE) {
+      free_model(m);
+      return NC_ERR_INVALID_ARG;
+    }
+    const bool dev_src = wk == PTR_DEVICE;
     if (!dev_src) {
       CREATE_TRY(cudaMalloc(&tmp, n_params * 4));
       cudaError_t e = cudaMemcpy(tmp, weights, n_params * 4, cudaMemcpyHostToDevice);
@@ -960,14 +1016,11 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   if (!m->bf16) CREATE_TRY(cudaMalloc(&m->c32, R * NQKV * 4));
   CREATE_TRY(cudaMalloc(&m->tok_stage, R * 4));
   if (m->bf16) {
-    CREATE_TRY(cudaFuncSetAttribute(attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)ATC_SMEM));
     m->vt_S = (c.max_seq + 127) / 128 * 128;
     CREATE_TRY(cudaMalloc(&m->vt, (int64_t)c.max_batch * 128 * m->vt_S * 2));
     CREATE_TRY(cudaMemset(m->vt, 0, (int64_t)c.max_batch * 128 * m->vt_S * 2));
-    CREATE_TRY(cudaFuncSetAttribute(attn_decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)ATT_DECODE_SMEM));
   }
+  CREATE_TRY(configure_kernels(m));
   CREATE_TRY(cudaMalloc(&m->err, sizeof(int)));
   CREATE_TRY(cudaMalloc(&m->d_len, sizeof(int)));
   CREATE_TRY(cudaMemset(m->d_len, 0, sizeof(int)));
@@ -1075,7 +1128,8 @@ nc_status nc_decode_step_noalloc(nc_model* m, const int32_t* tokens, int32_t B, 
   if (m->length == 0) return NC_ERR_STATE;
   if (B != m->batch) return NC_ERR_INVALID_ARG;
   if (m->length >= m->cfg.max_seq) return NC_ERR_CAPACITY;
-  if (!is_device_ptr(tokens) || !is_device_ptr(logits)) return NC_ERR_INVALID_ARG;
+  if (ptr_kind(tokens, m->device) != PTR_DEVICE || ptr_kind(logits, m->device) != PTR_DEVICE)
+    return NC_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != m->device) return NC_ERR_INVALID_ARG;
   // every buffer of the step is model-owned and sized at creation; the eager
@@ -1128,7 +1182,9 @@ int64_t nc_launch_count(const nc_model* m) { return m ? m->launches : -1; }
 nc_status nc_gemm_bf16(nc_model* m, const void* A, const void* W, float* C, int32_t M, int32_t N,
                        int32_t K, nc_stream_t stream) {
   if (!m || !A || !W || !C || M < 1 || N < 256 || K < 8 || N % 256 || K % 8) return NC_ERR_INVALID_ARG;
-  if (!is_device_ptr(A) || !is_device_ptr(W) || !is_device_ptr(C)) return NC_ERR_INVALID_ARG;
+  if (ptr_kind(A, m->device) != PTR_DEVICE || ptr_kind(W, m->device) != PTR_DEVICE ||
+      ptr_kind(C, m->device) != PTR_DEVICE)
+    return NC_ERR_INVALID_ARG;
   // M > 128 runs the CTA-pair form the prefill uses
   const int cl = M > 128 ? kPrefillCluster : 0;
   CUtensorMap ta, tb;
