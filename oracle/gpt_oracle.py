@@ -40,8 +40,10 @@ Readings taken where the pages are silent or garbled (identical in the CUDA path
      otherwise the candidates are ordered by (logit descending, index
      ascending), the first top_k are kept (0 keeps all), p_i is proportional to
      exp((l_i - l_max) / temperature), and a uniform draw u in [0, 1) picks the
-     first candidate whose cumulative probability exceeds u.  The draws are
-     inputs.
+     first candidate whose cumulative probability exceeds u.  The cumulative
+     weights C_j are summed in candidate order and the total is the last of
+     them, so "cumulative probability exceeds u" is C_j > u * C_last.  The
+     draws are inputs.
 """
 from __future__ import annotations
 
@@ -273,8 +275,9 @@ def sample_tokens(logits, temperature, top_k, u):
 
     temperature == 0: argmax, the lowest index among equal maxima.  Otherwise
     the candidates are ordered by (logit descending, index ascending), the first
-    top_k kept (top_k == 0 keeps all V), weighted by exp((l - l_max) / T) and
-    the first whose cumulative weight exceeds u[b] times the total is taken.
+    top_k kept (top_k == 0 keeps all V), weighted by exp((l - l_max) / T),
+    the weights summed in that order into cumulative weights C_j, and the
+    first candidate with C_j > u[b] * C_last is taken.
     """
     logits = np.asarray(logits, dtype=np.float64)
     B, V = logits.shape
@@ -287,12 +290,15 @@ def sample_tokens(logits, temperature, top_k, u):
             continue
         order = sorted(range(V), key=lambda i: (-row[i], i))
         keep = order if top_k <= 0 else order[:top_k]
-        w = np.array([math.exp((row[i] - row[keep[0]]) / temperature) for i in keep])
-        total = w.sum()
-        cum, pick = 0.0, keep[-1]
-        for i, wi in zip(keep, w):
-            cum += wi
-            if cum > u[b] * total:
+        w = [math.exp((row[i] - row[keep[0]]) / temperature) for i in keep]
+        cums, c = [], 0.0                 # cumulative weights in candidate order
+        for wi in w:
+            c += wi
+            cums.append(c)
+        total = cums[-1]
+        pick = keep[-1]
+        for i, ci in zip(keep, cums):
+            if ci > u[b] * total:
                 pick = i
                 break
         out[b] = pick
