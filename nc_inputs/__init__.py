@@ -51,6 +51,11 @@ class ModelShape:
     softcap: float = 15.0
     rms_eps: float = 1e-6
     dtype: str = "bf16"          # "bf16" or "f32": the precision the model computes in
+    # sliding-window attention: layer l uses `window` (keys p - window + 1 .. p)
+    # where window_pattern[l % len] is "S", the whole causal context for "L";
+    # an empty pattern (the default) leaves every layer unrestricted
+    window: int = 0
+    window_pattern: str = ""
 
     def with_(self, **kw) -> "ModelShape":
         return replace(self, **kw)

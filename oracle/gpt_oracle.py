@@ -35,6 +35,13 @@ Readings taken where the pages are silent or garbled (identical in the CUDA path
      engine]: a prompt may be prefilled in chunks (each chunk continues the
      cache); "batch generation clones the KV cache for parallel sampling" is
      read as copying one row's cache to every row of the batch.
+  R12 grouped-query attention [apidog 1]: n_kv K/V heads, query head h reads
+     K/V head h // (n_head / n_kv); one K/V head is multi-query attention.
+  R13 sliding-window attention [apidog 1, 5] (a configurable pattern such as
+     "SSSL" of short and long windows; the pages give no sizes): layer l uses
+     the letter pattern[l % len(pattern)]; "S" limits a query at position p to
+     the keys p - window + 1 .. p, "L" is the unrestricted causal window.  An
+     empty pattern or window 0 leaves every layer unrestricted.
   R11 sampling (the pages name parallel sampling but not its rule; plainest
      reading): temperature 0 is greedy, the lowest index among equal maxima;
      otherwise the candidates are ordered by (logit descending, index
@@ -128,18 +135,22 @@ def apply_rope(x, cos, sin):
     return np.concatenate([a * c - b * s, a * s + b * c], axis=-1)
 
 
-def causal_attention(q, k, v, q_pos, k_pos):
-    """Causal multi-query attention (R5) [yelogs], [apidog 5].
+def causal_attention(q, k, v, q_pos, k_pos, window=0):
+    """Causal multi-query / grouped-query attention (R5, R12) [yelogs], [apidog 1, 5].
 
     q: [Tq, n_head, hd]; k, v: [Tk, n_kv, hd]; query head h reads key/value
     head h // (n_head / n_kv) -- with one KV head every query head shares it.
-    A query at position p sees the keys at positions <= p.
+    A query at position p sees the keys at positions <= p, and with a window
+    W > 0 only those > p - W (R13).
     Returns [Tq, n_head, hd].
     """
     n_head, hd = q.shape[1], q.shape[2]
     n_kv = k.shape[1]
     group = n_head // n_kv
-    allowed = np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None]   # [Tq, Tk]
+    kp, qp = np.asarray(k_pos)[None, :], np.asarray(q_pos)[:, None]
+    allowed = kp <= qp                                                    # [Tq, Tk]
+    if window > 0:
+        allowed = allowed & (kp > qp - window)
     out = np.empty_like(q)
     for h in range(n_head):
         kh, vh = k[:, h // group, :], v[:, h // group, :]
@@ -150,6 +161,16 @@ def causal_attention(q, k, v, q_pos, k_pos):
         p = p / p.sum(axis=1, keepdims=True)
         out[:, h, :] = p @ vh
     return out
+
+
+def layer_window(shape, li):
+    """Attention window of layer li (R13): the short window for an "S" of the
+    pattern, 0 (unrestricted) otherwise."""
+    pattern = getattr(shape, "window_pattern", "") or ""
+    window = getattr(shape, "window", 0) or 0
+    if not pattern or window <= 0:
+        return 0
+    return window if pattern[li % len(pattern)] == "S" else 0
 
 
 def relu_squared(x):
@@ -212,7 +233,7 @@ class OracleModel:
             new_k.append(kc)
             new_v.append(vc)
             k_pos = np.arange(kc.shape[0])
-            y[b] = causal_attention(qb, kc, vc, positions, k_pos)
+            y[b] = causal_attention(qb, kc, vc, positions, k_pos, layer_window(s, li))
         self.k_cache[li] = np.stack(new_k)
         self.v_cache[li] = np.stack(new_v)
 
