@@ -2,11 +2,16 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
-Default workload: d12 (12 layers, d_model 768, 6 query heads x 128, one KV
-head, MLP 3072, vocab 65536) prefill of 8 rows x 2048 uniform-random tokens,
-all-position fp32 logits.  One step = one nc_prefill over the whole batch.
-A second measurement (key "decode") times d12 decode: 32 rows, 512-token
-prompt, 256 decode steps, tokens/s over the decode steps.
+Default workload: the largest model, d24 (24 layers, d_model 1536, 12 query
+heads x 128, one KV head, MLP 6144, vocab 65536).  The headline leg is its
+prefill of 8 rows x 2048 uniform-random tokens with all-position fp32 logits;
+one step = one nc_prefill over the whole batch.  The "decode" leg times the
+same model's decode workload: 128 rows, 2048-token prompt, 128 decode steps,
+tokens/s over the decode steps (one step = one nc_decode_step for the batch).
+With --config d12_prefill / d20_prefill the legs are that model's workloads.
+Each leg carries its own roofline (dominant kernel class), end-to-end figure
+through the public API with pinned host buffers, and fp64 CPU-oracle
+baseline.  At N = 1 the d12 workloads are measured too (key "d12").
 
 Prints ONE JSON line on rank 0.  Under torchrun every rank runs its own
 replica of the workload on its own GPU (rows are independent, no collective);
@@ -18,11 +23,13 @@ workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import ctypes
+import hashlib
 import json
 import os
-import hashlib
 import statistics
 import sys
+import threading
 import time
 
 import numpy as np
@@ -34,6 +41,7 @@ import nc_inputs  # noqa: E402
 
 METRIC = "prefill tokens/s and decode tokens/s at 1 B300; % of bf16 TC peak / HBM BW"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+DECODE_OF = {"d12_prefill": "d12_decode", "d20_prefill": "d20_decode", "d24_prefill": "d24_decode"}
 
 
 def load_peaks():
@@ -44,6 +52,10 @@ def load_peaks():
         return d, "measured"
     return dict(PEAKS_FALLBACK), "fallback"
 
+
+# --------------------------------------------------------------------------- #
+# algorithmic work (numerators of every roofline fraction)
+# --------------------------------------------------------------------------- #
 
 def prefill_flops(s, B, T, last_only=False):
     """Algorithmic FLOPs of one prefill, per kernel class (2 per MAC; causal
@@ -60,50 +72,94 @@ def prefill_flops(s, B, T, last_only=False):
     }
 
 
-def decode_bytes(s, B, ctx):
+def decode_bytes_by_class(s, B, ctx):
     """Algorithmic HBM bytes of one decode step at context length ctx (keys
-    0..ctx-1 read, one new K/V row written): bf16 weights once, KV read+write,
-    embedding rows, fp32 logits."""
+    0..ctx-1 read, one new K/V row written), split by the kernel class that
+    moves them: bf16 weights once (QKV, O, FC, PROJ, unembedding), the K/V
+    read (attention), the new K/V row (QKV), the embedding rows and the fp32
+    logits."""
     d, hd, nh, F, V, L = s.d_model, s.head_dim, s.n_head, s.d_mlp, s.vocab, s.n_layer
-    layer = (nh + 2) * hd * d + d * nh * hd + 2 * F * d
-    return (2.0 * (L * layer + V * d) + L * B * 2 * ctx * hd * 2 + L * B * 2 * hd * 2
-            + B * d * 2 + B * V * 4)
+    return {
+        "embed": B * d * 2.0,
+        "qkv": 2.0 * L * (nh + 2) * hd * d + L * B * 2 * hd * 2.0,
+        "attn": L * B * 2.0 * ctx * hd * 2,
+        "oproj": 2.0 * L * d * nh * hd,
+        "fc": 2.0 * L * F * d,
+        "proj": 2.0 * L * d * F,
+        "lm_head": 2.0 * V * d + B * V * 4.0,
+    }
 
+
+def decode_bytes(s, B, ctx):
+    """Algorithmic HBM bytes of one decode step (sum over the classes)."""
+    return sum(decode_bytes_by_class(s, B, ctx).values())
+
+
+def weight_bytes(s, elem=2):
+    return elem * nc_inputs.param_count(s)
+
+
+# --------------------------------------------------------------------------- #
+# clocks during the timed region (read-only queries)
+# --------------------------------------------------------------------------- #
 
 class ClockSampler:
-    """SM clock and clock-event reasons of one GPU, read through NVML every
-    10 ms by a background thread while the timed region runs.  Read only: no
-    GPU setting is changed."""
-    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
-               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
-               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
-               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
-               ("hw_power_brake", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
+    """SM clock and clock-event reasons of this process's GPU, sampled every
+    10 ms by a background thread while the timed region runs.  NVML is
+    called through ctypes (libnvidia-ml); nvidia-smi at 50 ms is the
+    fallback.  Read only: no GPU setting is changed."""
+    NVML_CLOCK_SM = 1
+    # clock-event reason bits of the NVML API
+    REASON_BITS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+                   ("hw_thermal_slowdown", 0x40), ("hw_power_brake", 0x80))
 
     def __init__(self, gpu_index, period_s=0.01):
         self.gpu, self.period = gpu_index, period_s
-        self.sm, self.bits, self.mx, self.nv = [], 0, None, None
+        self.sm, self.bits, self.mx = [], 0, None
+        self.nvml = None
         self.smi, self.note = None, None
 
+    def _uuid(self):
+        import torch
+        u = str(torch.cuda.get_device_properties(self.gpu).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+
+    def _open_nvml(self):
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        h = ctypes.c_void_p()
+        if L.nvmlDeviceGetHandleByUUID(self._uuid().encode(), ctypes.byref(h)) != 0:
+            if L.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle for this device")
+        self.reasons_fn = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            L.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if L.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+            self.mx = float(mx.value)
+        self.nvml, self.h = L, h
+
     def __enter__(self):
-        import threading
         try:
-            import pynvml as nv
-            nv.nvmlInit()
-            self.nv = nv
-            self.h = self._handle(nv)
-            self.mx = float(nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM))
-            self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._open_nvml()
         except Exception as e:
-            # NVML unavailable: poll nvidia-smi instead (50 ms)
-            self.nv, self.note = None, f"nvml: {type(e).__name__}: {e}"[:160]
+            self.nvml, self.note = None, f"nvml: {type(e).__name__}: {e}"[:160]
             self._start_smi()
             return self
         self.stop = threading.Event()
         self.th = threading.Thread(target=self._loop, daemon=True)
         self.th.start()
         return self
+
+    def _loop(self):
+        L, h = self.nvml, self.h
+        c, r = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if L.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(c)) == 0:
+                self.sm.append(float(c.value))
+            if self.reasons_fn(h, ctypes.byref(r)) == 0:
+                self.bits |= int(r.value)
+            self.stop.wait(self.period)
 
     SMI_Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -113,9 +169,7 @@ class ClockSampler:
         import subprocess
         import tempfile
         try:
-            import torch
-            ident = str(torch.cuda.get_device_properties(self.gpu).uuid)
-            ident = ident if ident.startswith("GPU-") else "GPU-" + ident
+            ident = self._uuid()
         except Exception:
             ident = str(self.gpu)
         self.smi_out = tempfile.TemporaryFile(mode="w+")
@@ -126,10 +180,7 @@ class ClockSampler:
         except OSError as e:
             self.smi, self.note = None, (self.note or "") + f"; nvidia-smi: {e}"
             return
-        # nvidia-smi takes a moment to start: let its first sample land before
-        # the timed region begins (at most 5 s)
-        import time
-        t0 = time.time()
+        t0 = time.time()                    # let the first sample land (at most 5 s)
         while time.time() - t0 < 5 and self.smi.poll() is None:
             self.smi_out.flush()
             if os.fstat(self.smi_out.fileno()).st_size > 0:
@@ -160,44 +211,22 @@ class ClockSampler:
                 if v.lower() == "active":
                     self.smi_reasons.add(n)
 
-    def _handle(self, nv):
-        # NVML numbers every GPU of the machine; find this process's device
-        # (CUDA index self.gpu) by its UUID
-        import torch
-        uuid = str(torch.cuda.get_device_properties(self.gpu).uuid)
-        for name in (uuid, "GPU-" + uuid):
-            try:
-                return nv.nvmlDeviceGetHandleByUUID(name)
-            except Exception:
-                pass
-        return nv.nvmlDeviceGetHandleByIndex(self.gpu)
-
-    def _loop(self):
-        nv = self.nv
-        while not self.stop.is_set():
-            try:
-                self.sm.append(float(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)))
-                self.bits |= int(self.reasons_fn(self.h))
-            except Exception:
-                pass
-            self.stop.wait(self.period)
-
     def __exit__(self, *a):
         self._stop_smi()
-        if self.nv is not None:
+        if self.nvml is not None:
             self.stop.set()
             self.th.join(timeout=2)
             try:
-                self.nv.nvmlShutdown()
+                self.nvml.nvmlShutdown()
             except Exception:
                 pass
 
     def summary(self):
         if not self.sm:
             return {"sm_mhz": None, "sm_max_mhz": self.mx, "reasons": [], "samples": 0, "note": self.note}
-        if self.nv is not None:
-            reasons = sorted(n for n, c in self.REASONS if hasattr(self.nv, c) and self.bits & getattr(self.nv, c))
-            src = "nvml 10 ms"
+        if self.nvml is not None:
+            reasons = sorted(n for n, bit in self.REASON_BITS if self.bits & bit)
+            src = "nvml (ctypes) 10 ms"
         else:
             reasons, src = sorted(getattr(self, "smi_reasons", set())), "nvidia-smi 50 ms"
         out = {"sm_mhz": statistics.median(self.sm), "sm_max_mhz": self.mx, "reasons": reasons,
@@ -207,11 +236,17 @@ class ClockSampler:
         return out
 
 
-# DRAM traffic per launch of the dominant kernel, from the ncu captures
-# summarised in profiles/traffic.md: | class | workload | bytes | source | sha256 |.
-# The figure is used only while the kernel's source still hashes the same.
+# --------------------------------------------------------------------------- #
+# DRAM traffic of the dominant kernels, from ncu captures
+# --------------------------------------------------------------------------- #
+
+# profiles/traffic.json lists, per kernel class and workload, the DRAM bytes
+# (read + write) of one launch measured by ncu and the SHA-256 prefix of the
+# kernel's source file at capture time; a figure is used only while the
+# source still hashes the same (otherwise the kernel changed and it is null).
 KCLASS_SOURCE = {"lm_head": "k_gemm_tc.cuh", "qkv": "k_gemm_tc.cuh", "oproj": "k_gemm_tc.cuh",
-                 "fc": "k_gemm_tc.cuh", "proj": "k_gemm_tc.cuh", "attn": "k_attn_tc.cuh"}
+                 "fc": "k_gemm_tc.cuh", "proj": "k_gemm_tc.cuh", "attn": "k_attn_tc.cuh",
+                 "decode_attn": "k_attn_mma.cuh", "decode_gemm": "k_gemm_skinny.cuh"}
 
 
 def source_sha256(name):
@@ -221,19 +256,23 @@ def source_sha256(name):
 
 
 def measured_traffic(kclass, workload):
-    path = os.path.join(ROOT, "profiles", "traffic.md")
-    src = KCLASS_SOURCE.get(kclass)
-    if src is None or not os.path.exists(path):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
         return None
-    for line in open(path):
-        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
-        if len(cells) == 5 and cells[0] == kclass and cells[1] == workload and cells[3] == src:
-            try:
-                return float(cells[2]) if cells[4] == source_sha256(src) else None
-            except ValueError:
-                return None
+    with open(path) as f:
+        rows = json.load(f).get("launches", [])
+    for r in rows:
+        if r.get("class") == kclass and r.get("workload") == workload:
+            src = r.get("source")
+            if src and os.path.exists(os.path.join(ROOT, "dense_gpt_transformer_fwd_b300", "csrc", src)) \
+                    and source_sha256(src) == r.get("sha256"):
+                return float(r["bytes_per_launch"])
     return None
 
+
+# --------------------------------------------------------------------------- #
+# the fp64 CPU oracle (reported baseline)
+# --------------------------------------------------------------------------- #
 
 def blas_threads():
     """Threads the oracle's BLAS uses (OpenBLAS defaults to every available core, up to 64)."""
@@ -245,15 +284,36 @@ def blas_threads():
         return int(env) if env else min(len(os.sched_getaffinity(0)), 64)
 
 
-def oracle_tokens_per_s(w, flat, prompt, rows, T):
-    """fp64 oracle prefill of `rows` x T tokens; returns (tokens/s, seconds, threads)."""
+def oracle_baselines(w, wd, flat, prompt, nxt, decode_steps=8):
+    """fp64 oracle on row 0: the prefill of its prompt (timed), then
+    `decode_steps` decode steps continuing from that cache (timed apart).
+    Returns the two cpu_baseline objects."""
     from oracle.gpt_oracle import OracleModel
     o = OracleModel(flat, w.shape)
+    T = w.prompt_len
     t0 = time.perf_counter()
-    o.prefill(prompt[rows, :T])
+    o.prefill(prompt[:1, :T])
     dt = time.perf_counter() - t0
-    return len(rows) * T / dt, dt, blas_threads()
+    threads = blas_threads()
+    pre = {"value": round(T / dt, 2), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+           "sample": f"fp64 prefill of row 0 ({T} tokens, all-position logits) of {w.name}; {dt:.1f} s"}
+    dec = None
+    if wd is not None and nxt is not None:
+        t0 = time.perf_counter()
+        for t in range(decode_steps):
+            o.decode(nxt[t][:1])
+        dd = time.perf_counter() - t0
+        dec = {"value": round(decode_steps / dd, 3), "unit": "tokens/s", "cores": threads,
+               "kind": "oracle",
+               "sample": (f"fp64 decode of row 0 for {decode_steps} steps at context {T + 1}..{T + decode_steps} "
+                          f"(continuing the prefill above; {wd.name} decodes at context "
+                          f"{wd.prompt_len + 1}..{wd.max_seq}); {dd:.1f} s")}
+    return pre, dec
 
+
+# --------------------------------------------------------------------------- #
+# ranks
+# --------------------------------------------------------------------------- #
 
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -281,15 +341,23 @@ def max_over_ranks(world, v):
     return float(t.item())
 
 
+def reference_tokens_per_step(shape):
+    """Prefix length the reference arm prefills per step: about 0.2 TFLOP of
+    fp64 work (a few seconds on the host cores), whatever the model."""
+    per_token = 2.0 * (shape.n_layer * nc_inputs.layer_param_count(shape) + shape.vocab * shape.d_model)
+    t = int(2e11 / per_token)
+    return max(32, min(512, 1 << (t.bit_length() - 1)))
+
+
 def run_reference(args, world, rank):
     """The oracle, as it stands, on the host cores: each step is the prefill of
-    row 0's first 512 tokens of the benchmark workload."""
+    row 0's first tokens of the benchmark workload (all-position logits)."""
     if rank != 0:
         return
     w = nc_inputs.WORKLOADS[args.config]
     flat = nc_inputs.gen_weights(w.shape, w.weight_seed)
     prompt, _ = _tokens(w)
-    T = min(512, w.prompt_len)
+    T = min(reference_tokens_per_step(w.shape), w.prompt_len)
     from oracle.gpt_oracle import OracleModel
     o = OracleModel(flat, w.shape)
     for _ in range(args.warmup):
@@ -320,6 +388,10 @@ def _tokens(w):
     return prompt, nxt
 
 
+# --------------------------------------------------------------------------- #
+# GPU legs
+# --------------------------------------------------------------------------- #
+
 def bench_prefill(args, world, local, w, flat, prompt):
     import torch
     import dense_gpt_transformer_fwd_b300 as ncp
@@ -347,7 +419,7 @@ def bench_prefill(args, world, local, w, flat, prompt):
         ev1.record(stream)
         torch.cuda.synchronize()
     m.sync()
-    launches = (m.launch_count - l0) // args.steps
+    launches = m.launch_count - l0
     ms = ev0.elapsed_time(ev1) / args.steps
     barrier(world)
     ms_max = max_over_ranks(world, ms)
@@ -367,13 +439,15 @@ def bench_prefill(args, world, local, w, flat, prompt):
         m.prefill(tok_h, out=out_h)
     torch.cuda.synchronize()
     barrier(world)
-    t0 = time.perf_counter()
     e2e_steps = max(1, min(args.steps, 5))
+    ev0.record(stream)
+    t0 = time.perf_counter()
     for _ in range(e2e_steps):
         m.kv_reset()
         m.prefill(tok_h, out=out_h)
+    ev1.record(stream)
     torch.cuda.synchronize()
-    e2e_s = max_over_ranks(world, (time.perf_counter() - t0) / e2e_steps)
+    e2e_s = max_over_ranks(world, max(time.perf_counter() - t0, ev0.elapsed_time(ev1) / 1e3) / e2e_steps)
     m.sync()
     m.close()
     del logits, out_h
@@ -382,26 +456,31 @@ def bench_prefill(args, world, local, w, flat, prompt):
             "e2e_s": e2e_s, "h2d": B * T * 4, "d2h": B * T * V * 4}
 
 
-def bench_decode(args, w, flat, prompt, nxt, steps=None):
+def bench_decode(args, world, local, w, flat, prompt, nxt):
+    """Decode leg: the workload's steps replayed from the captured graph into
+    one logits buffer (timed), an eager pass with per-kernel-class events, and
+    an end-to-end pass with pinned host token and logit buffers."""
     import torch
     import dense_gpt_transformer_fwd_b300 as ncp
-    B = w.batch
-    steps = steps or w.decode_steps
+    B, V = w.batch, w.shape.vocab
+    steps = w.decode_steps
     m = ncp.Model(w.shape, flat, max_batch=B, max_seq=w.max_seq)
     tok = torch.from_numpy(prompt).to("cuda")
     nxt_d = torch.from_numpy(nxt).to("cuda")
-    out = torch.empty((B, w.shape.vocab), dtype=torch.float32, device="cuda")
+    out = torch.empty((B, V), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
-    # warm-up pass (prefill + a few steps), then the timed pass
+    # warm-up pass (prefill + a few steps: the graph is captured at the second)
     m.prefill(tok, last_only=True)
-    for t in range(min(3, steps)):
+    for t in range(min(max(args.warmup, 3), steps)):
         m.decode_step(nxt_d[t], out=out)
     m.kv_reset()
     m.prefill(tok, last_only=True)
+    m.sync()
+    barrier(world)
     torch.cuda.synchronize()
     l0 = m.launch_count
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as clk:
+    with ClockSampler(local) as clk:
         ev0.record(stream)
         for t in range(steps):
             m.decode_step(nxt_d[t], out=out)
@@ -409,11 +488,122 @@ def bench_decode(args, w, flat, prompt, nxt, steps=None):
         torch.cuda.synchronize()
     m.sync()
     ms = ev0.elapsed_time(ev1) / steps
-    launches = (m.launch_count - l0) // steps
-    ctx_mean = w.prompt_len + (steps + 1) / 2.0
-    byts = np.mean([decode_bytes(w.shape, B, w.prompt_len + t + 1) for t in range(steps)])
+    launches = m.launch_count - l0
+    barrier(world)
+    ms_max = max_over_ranks(world, ms)
+
+    # eager pass with events around every kernel: device time per class
+    m.kv_reset()
+    m.prefill(tok, last_only=True)
+    m.profile_begin()
+    for t in range(steps):
+        m.decode_step(nxt_d[t], out=out)
+    prof = m.profile_end()
+    prof = {k: (t / steps, n // steps) for k, (t, n) in prof.items()}
+
+    # end to end: pinned host tokens in, pinned host logits out, every step
+    tok_h = torch.from_numpy(nxt).pin_memory()
+    out_h = torch.empty((B, V), dtype=torch.float32, pin_memory=True)
+    m.kv_reset()
+    m.prefill(tok, last_only=True)
+    for t in range(2):                                 # the host-buffer graph is captured here
+        m.decode_step(tok_h[t], out=out_h)
+    m.kv_reset()
+    m.prefill(tok, last_only=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for t in range(steps):
+        m.decode_step(tok_h[t], out=out_h)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(world, (time.perf_counter() - t0) / steps)
+    m.sync()
     m.close()
-    return {"ms": ms, "launches": launches, "bytes": float(byts), "ctx_mean": ctx_mean, "clocks": clk.summary()}
+    torch.cuda.empty_cache()
+    ctxs = [w.prompt_len + t + 1 for t in range(steps)]
+    by_class = {k: float(np.mean([decode_bytes_by_class(w.shape, B, c)[k] for c in ctxs]))
+                for k in decode_bytes_by_class(w.shape, B, ctxs[0])}
+    return {"ms": ms_max, "launches": launches, "prof": prof, "bytes_by_class": by_class,
+            "bytes": float(sum(by_class.values())), "clocks": clk.summary(), "e2e_s": e2e_s,
+            "h2d": B * 4, "d2h": B * V * 4}
+
+
+def class_table(prof, work, unit_scale):
+    """Per kernel class: device ms per step, launches, share and the achieved
+    rate (work per step / device time)."""
+    total = sum(t for t, _ in prof.values()) or 1.0
+    out = {}
+    for k, (t, n) in prof.items():
+        if t <= 0:
+            continue
+        e = {"ms": round(t, 4), "launches": n, "share": round(t / total, 4)}
+        if k in work:
+            e["rate"] = round(work[k] / (t / 1e3) / unit_scale, 1)
+        out[k] = e
+    return out
+
+
+def prefill_leg(args, world, local, w, flat, prompt, peaks, peak_src):
+    r = bench_prefill(args, world, local, w, flat, prompt)
+    B, T = w.batch, w.prompt_len
+    flops = prefill_flops(w.shape, B, T)
+    prof = r["prof"]
+    dom = max((k for k in prof if k in flops), key=lambda k: prof[k][0])
+    peak = peaks["bf16_tflops"]
+    ach = flops[dom] / (prof[dom][0] / 1e3) / 1e12
+    roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+            "traffic": measured_traffic(dom, w.name),
+            "peak_source": f"{peak_src} bf16 dense (burst)",
+            "frac_of_sustained": round(ach / peaks.get("bf16_tflops_sustained", peak), 4),
+            "per_launch": f"{flops[dom] / max(prof[dom][1], 1) / 1e9:.1f} GFLOP per launch, "
+                          f"{prof[dom][0] / max(prof[dom][1], 1) * 1e3:.1f} us per launch"}
+    total = sum(flops.values())
+    return r, {
+        "value": round(world * B * T / (r["ms"] / 1e3), 1), "ms_per_step": round(r["ms"], 4),
+        "gpu_launches": r["launches"], "gpu_launches_per_step": r["launches"] // args.steps,
+        "e2e": {"value": round(world * B * T / r["e2e_s"], 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "roofline": roof,
+        "step_tflops": round(total / (r["ms"] / 1e3) / 1e12, 1),
+        "step_frac_of_peak": round(total / (r["ms"] / 1e3) / 1e12 / peak, 4),
+        "kernels": class_table(prof, flops, 1e12),
+        "kernel_rate_unit": "TFLOP/s",
+        "clocks": r["clocks"],
+    }
+
+
+def decode_leg(args, world, local, w, flat, prompt, nxt, peaks, peak_src):
+    r = bench_decode(args, world, local, w, flat, prompt, nxt)
+    prof, by = r["prof"], r["bytes_by_class"]
+    dom = max((k for k in prof if k in by), key=lambda k: prof[k][0])
+    hbm = peaks["hbm_gbs"]
+    ach = by[dom] / (prof[dom][0] / 1e3) / 1e9
+    gbs = r["bytes"] / (r["ms"] / 1e3) / 1e9
+    tclass = "decode_attn" if dom == "attn" else "decode_gemm"
+    roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(ach / hbm, 4), "traffic": measured_traffic(tclass, w.name),
+            "peak_source": f"{peak_src} HBM copy",
+            "per_launch": f"{by[dom] / max(prof[dom][1], 1) / 1e6:.1f} MB per launch, "
+                          f"{prof[dom][0] / max(prof[dom][1], 1) * 1e3:.1f} us per launch (eager pass)"}
+    return r, {
+        "workload": w.name,
+        "value": round(world * w.batch / (r["ms"] / 1e3), 1), "unit": "tokens/s",
+        "ms_per_step": round(r["ms"], 4), "steps": w.decode_steps,
+        "gpu_launches": r["launches"], "gpu_launches_per_step": r["launches"] // w.decode_steps,
+        "step_gbs": round(gbs, 1), "step_frac_of_hbm": round(gbs / hbm, 4),
+        "step_frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
+        "e2e": {"value": round(world * w.batch / r["e2e_s"], 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "roofline": roof,
+        "kernels": class_table(prof, by, 1e9),
+        "kernel_rate_unit": "GB/s",
+        "config": {"global_batch": w.batch * world, "prompt_len": w.prompt_len,
+                   "decode_steps": w.decode_steps,
+                   "l2": f"working set > L2 (weights {weight_bytes(w.shape) / 1e9:.2f} GB, "
+                         f"KV cache {r['bytes_by_class']['attn'] / 1e9:.2f} GB read per step)"},
+        "clocks": r["clocks"],
+    }
 
 
 def run_case(args):
@@ -452,11 +642,12 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="d12_prefill", choices=sorted(nc_inputs.WORKLOADS))
+    ap.add_argument("--config", default="d24_prefill", choices=sorted(nc_inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-decode", action="store_true", help="skip the d12 decode measurement")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode leg")
+    ap.add_argument("--no-extra", action="store_true", help="skip the d12 measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases for profiling)")
@@ -491,79 +682,50 @@ def main():
     line = {"metric": METRIC, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.shape.dtype, "data": "synthetic"}
+    wd = pd = nd = None
 
     if w.decode_steps == 0:
-        r = bench_prefill(args, world, local, w, flat, prompt)
-        B, T = w.batch, w.prompt_len
-        value = world * B * T / (r["ms"] / 1e3)
-        flops = prefill_flops(w.shape, B, T)
-        prof = r["prof"]
-        # dominant kernel class by device time
-        dom = max(prof, key=lambda k: prof[k][0])
-        kern = {}
-        for k, (t, n) in prof.items():
-            if t > 0:
-                e = {"ms": round(t, 4), "launches": n, "share": round(t / sum(v[0] for v in prof.values()), 4)}
-                if k in flops:
-                    e["tflops"] = round(flops[k] / (t / 1e3) / 1e12, 1)
-                kern[k] = e
-        peak = peaks["bf16_tflops"]
-        if dom in flops:
-            ach = flops[dom] / (prof[dom][0] / 1e3) / 1e12
-            roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": peak,
-                    "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                    "traffic": measured_traffic(dom, w.name),
-                    "peak_source": f"{peak_src} bf16 dense (burst)"}
-        else:
-            roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": None, "traffic": None}
-        total_flops = sum(flops.values())
-        line.update({
-            "value": round(value, 1), "ms_per_step": round(r["ms"], 4),
-            "config": {"workload": w.name, "global_batch": B * world, "seq_len": T,
-                       "parallelism": f"replicas{world}", "logits": "fp32, all positions",
-                       "l2": "working set > L2 (weights 347 MB, logits 4.3 GB per step)"},
-            "gpu_launches": r["launches"],
-            "e2e": {"value": round(world * B * T / r["e2e_s"], 1), "unit": "tokens/s",
-                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-            "roofline": roof,
-            "step_tflops": round(total_flops / (r["ms"] / 1e3) / 1e12, 1),
-            "step_frac_of_peak": round(total_flops / (r["ms"] / 1e3) / 1e12 / peak, 4),
-            "kernels": kern,
-            "clocks": r["clocks"],
-        })
-        if not args.no_decode and rank == 0:
-            wd = nc_inputs.WORKLOADS["d12_decode"] if w.shape.name == "d12" else None
-            if wd is not None:
-                pd, nd = _tokens(wd)
-                rd = bench_decode(args, wd, flat, pd, nd)
-                gbs = rd["bytes"] / (rd["ms"] / 1e3) / 1e9
-                line["decode"] = {"workload": wd.name, "value": round(wd.batch / (rd["ms"] / 1e3), 1),
-                                  "unit": "tokens/s", "ms_per_step": round(rd["ms"], 4),
-                                  "gpu_launches_per_step": rd["launches"],
-                                  "hbm_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
-                                  "clocks": rd["clocks"]}
+        _, leg = prefill_leg(args, world, local, w, flat, prompt, peaks, peak_src)
+        line.update(leg)
+        line["config"] = {"workload": w.name, "global_batch": w.batch * world, "seq_len": w.prompt_len,
+                          "parallelism": f"replicas{world}", "logits": "fp32, all positions",
+                          "l2": f"working set > L2 (weights {weight_bytes(w.shape) / 1e9:.2f} GB, logits "
+                                f"{w.batch * w.prompt_len * w.shape.vocab * 4 / 1e9:.1f} GB per step)"}
+        if not args.no_decode and w.name in DECODE_OF:
+            wd = nc_inputs.WORKLOADS[DECODE_OF[w.name]]
+            pd, nd = _tokens(wd)
+            _, line["decode"] = decode_leg(args, world, local, wd, flat, pd, nd, peaks, peak_src)
     else:
-        rd = bench_decode(args, w, flat, prompt, nxt)
-        value = world * w.batch / (rd["ms"] / 1e3)
-        gbs = rd["bytes"] / (rd["ms"] / 1e3) / 1e9
-        line.update({
-            "value": round(value, 1), "ms_per_step": round(rd["ms"], 4),
-            "config": {"workload": w.name, "global_batch": w.batch * world,
-                       "seq_len": w.prompt_len, "decode_steps": w.decode_steps,
-                       "parallelism": f"replicas{world}"},
-            "gpu_launches": rd["launches"],
-            "roofline": {"bound": "hbm", "kernel": "decode step", "achieved": round(gbs, 1),
-                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None},
-            "clocks": rd["clocks"],
-        })
+        wd, pd, nd = w, prompt, nxt
+        _, leg = decode_leg(args, world, local, w, flat, prompt, nxt, peaks, peak_src)
+        cfg = leg.pop("config")
+        line.update({k: v for k, v in leg.items() if k not in ("workload", "unit")})
+        line["config"] = {"workload": w.name, "seq_len": w.prompt_len, "parallelism": f"replicas{world}",
+                          **cfg}
+
+    if world == 1 and not args.no_extra and w.shape.name != "d12" and not (args.batch or args.seq):
+        # the smallest bf16 model as extra keys (not the headline)
+        extra = {}
+        w12 = nc_inputs.WORKLOADS["d12_prefill"]
+        f12 = nc_inputs.gen_weights(w12.shape, w12.weight_seed)
+        p12, _ = _tokens(w12)
+        _, e = prefill_leg(args, world, local, w12, f12, p12, peaks, peak_src)
+        extra["prefill"] = {k: e[k] for k in ("value", "ms_per_step", "step_frac_of_peak", "roofline", "e2e")}
+        w12d = nc_inputs.WORKLOADS["d12_decode"]
+        p12d, n12d = _tokens(w12d)
+        _, e = decode_leg(args, world, local, w12d, f12, p12d, n12d, peaks, peak_src)
+        extra["decode"] = {k: e[k] for k in ("workload", "value", "ms_per_step", "step_gbs",
+                                             "step_frac_of_hbm", "roofline", "e2e")}
+        line["d12"] = extra
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, dt, threads = oracle_tokens_per_s(w, flat, prompt, [0], w.prompt_len)
-        line["cpu_baseline"] = {"value": round(tps, 2), "unit": "tokens/s", "cores": threads,
-                                "kind": "oracle",
-                                "sample": f"fp64 prefill of row 0 ({w.prompt_len} tokens) of {w.name}; {dt:.1f} s"}
+        pre, dec = oracle_baselines(w, wd, flat, prompt if w.decode_steps == 0 else pd, nd)
+        if w.decode_steps == 0:
+            line["cpu_baseline"] = pre
+            if dec is not None and "decode" in line:
+                line["decode"]["cpu_baseline"] = dec
+        else:
+            line["cpu_baseline"] = dec
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

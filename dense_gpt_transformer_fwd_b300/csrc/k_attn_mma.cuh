@@ -55,6 +55,11 @@ constexpr int ATT_HD = 128;
 
 // ---------------------------------------------------------------- decode --
 // Q: [B][n_head*128] (one new position per row, at pos = ctx-1); keys 0..ctx-1.
+// With pos_dev, row b's context is pos_dev[b] + 1 (per-row cache lengths).
+// Grouped-query attention (apidog.com/th item 1): grid.y runs over the K/V
+// sequences s = b * n_kv + g, and the CTA serves the n_head / n_kv query heads
+// of K/V head g; a sliding window (window > 0) limits the keys to the last
+// `window` positions (the sub-chunks before it are skipped).
 // CTA (group g, row b) streams `group` consecutive sub-chunks of DEC_SUB keys
 // (keys [g*group*DEC_SUB, ...)) through a DEC_STAGES-deep cp.async ring and
 // keeps a running (max, sum, output) per warp across them; each of the
@@ -77,19 +82,25 @@ static_assert(DEC_CHUNK % DEC_SUB == 0 || DEC_SUB % DEC_CHUNK == 0, "partial buf
 
 __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kc,
-    const __nv_bfloat16* __restrict__ Vc, __nv_bfloat16* __restrict__ O, int n_head, int cache_S, int ctx,
-    const int* __restrict__ pos_dev, float scale_log2, int group) {
+    const __nv_bfloat16* __restrict__ Vc, __nv_bfloat16* __restrict__ O, int n_head, int cache_S, int ctx_arg,
+    const int* __restrict__ pos_dev, float scale_log2, int group, int n_kv, int window) {
   pdl_trigger();
-  // with pos_dev the context is read on the device (the step is graph-replayable);
-  // the length only changes at the end of a step, so it may be read before
-  // waiting for the previous kernel.  Groups beyond the context have no keys
-  // (they still take part in the cluster's barriers).
-  if (pos_dev) ctx = *pos_dev + 1;
-  const int nsub = (ctx + DEC_SUB - 1) / DEC_SUB;
-  const int ngroups = (nsub + group - 1) / group;
-  const int grp = blockIdx.x, b = blockIdx.y;
-  const int c_begin = grp * group;
-  const int n = max(0, min(group, nsub - c_begin));
+  const int grp = blockIdx.x, bs = blockIdx.y;                 // K/V sequence bs = b * n_kv + g
+  const int b = bs / n_kv, g = bs % n_kv;
+  const int nq = n_head / n_kv, h0 = g * nq;                   // query heads h0 .. h0 + nq - 1
+  int c_begin = grp * group;                                   // first sub-chunk of this CTA
+  // With pos_dev the context is read on the device (the step is
+  // graph-replayable).  The previous step advances the length in its last
+  // kernel, which may still be running when this kernel starts (dependent
+  // launches chain), so a length read before the wait is the current one or
+  // one less.  The keys below that early length minus one were written two
+  // or more steps ago either way: they are streamed before the wait.  The
+  // exact context is read after it and the remaining keys are loaded then.
+  // Groups beyond the context have no keys (they still take part in the
+  // cluster's barriers).  A windowed layer loads nothing early (its first
+  // sub-chunk depends on the exact context).
+  const int early_keys = window > 0 ? 0 : (pos_dev ? pos_dev[b] - 1 : ctx_arg - 1);   // keys [0, early_keys)
+  const int n_early = max(0, min(group, (early_keys + DEC_SUB - 1) / DEC_SUB - c_begin));
   extern __shared__ __align__(128) uint8_t att_smem[];
   const uint32_t sQ = smem_u32(att_smem);                     // 16 rows
   const uint32_t sS = sQ + 16 * 256;                           // DEC_STAGES x (K, V) sub-chunks
@@ -97,37 +108,48 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
   float* ored = reinterpret_cast<float*>(att_smem + 16 * 256);  // [DEC_WARPS][16][128], aliases the stages
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, ocol = tid & 127;
   const int ldq = n_head * ATT_HD;
-  const __nv_bfloat16* kb = Kc + (size_t)b * cache_S * ATT_HD;
-  const __nv_bfloat16* vb = Vc + (size_t)b * cache_S * ATT_HD;
-  // rows of sub-chunk i: keys (c_begin + i) * DEC_SUB + r.  `which`: 0 keys
-  // written by earlier calls only, 1 the newest key only, 2 all; keys >= ctx
-  // are zero-filled
-  auto load_sub = [&](int i, int which) {
+  const __nv_bfloat16* kb = Kc + (size_t)bs * cache_S * ATT_HD;
+  const __nv_bfloat16* vb = Vc + (size_t)bs * cache_S * ATT_HD;
+  // rows of sub-chunk i: keys (c_begin + i) * DEC_SUB + r.  `early`: only
+  // the keys below key_lim (written by earlier calls); otherwise the keys the
+  // early pass did not load (below early_lim nothing is reloaded), with keys
+  // >= ctx zero-filled
+  int ctx = ctx_arg;
+  auto load_sub = [&](int i, bool early, int key_lim, int early_lim) {
     const uint32_t sk = sS + (i % DEC_STAGES) * DEC_STAGE_BYTES, sv = sk + DEC_SUB * 256;
     const int k0 = (c_begin + i) * DEC_SUB;
     for (int e = tid; e < DEC_SUB * 16; e += DEC_THREADS) {
       const int r = e >> 4, c = e & 15;
       const int key = k0 + r;
-      if (which == 0 && key >= ctx - 1) continue;
-      if (which == 1 && key < ctx - 1) continue;
-      const bool ok = key < ctx;
+      if (early ? key >= key_lim : key < early_lim) continue;
+      const bool ok = early || key < ctx;                      // early keys all exist
       const size_t off = (size_t)(ok ? key : 0) * ATT_HD + c * 8;
       cp_async16(swz(sk, r, c), kb + off, ok);
       cp_async16(swz(sv, r, c), vb + off, ok);
     }
   };
-  const int pre = n < DEC_STAGES - 1 ? n : DEC_STAGES - 1;
-  for (int i = 0; i < pre; ++i) {
-    load_sub(i, 0);
+  const int pre_early = n_early < DEC_STAGES - 1 ? n_early : DEC_STAGES - 1;
+  for (int i = 0; i < pre_early; ++i) {
+    load_sub(i, true, early_keys, 0);
     cp_async_commit();
   }
   pdl_wait();                                                  // q and the newest K/V row
+  if (pos_dev) ctx = pos_dev[b] + 1;
+  const int klo = window > 0 ? max(0, ctx - window) : 0;     // the first key inside the window
+  const int s_first = klo / DEC_SUB;
+  c_begin = s_first + grp * group;
+  const int nsub = (ctx + DEC_SUB - 1) / DEC_SUB;
+  const int ngroups = (nsub - s_first + group - 1) / group;
+  const int n = max(0, min(group, nsub - c_begin));
+  const int pre = n < DEC_STAGES - 1 ? n : DEC_STAGES - 1;
   for (int e = tid; e < 16 * 16; e += DEC_THREADS) {
     const int r = e >> 4, c = e & 15;
-    const bool ok = r < n_head;
-    cp_async16(swz(sQ, r, c), Q + (size_t)b * ldq + (ok ? r : 0) * ATT_HD + c * 8, ok);
+    const bool ok = r < nq;
+    cp_async16(swz(sQ, r, c), Q + (size_t)b * ldq + (h0 + (ok ? r : 0)) * ATT_HD + c * 8, ok);
   }
-  for (int i = 0; i < pre; ++i) load_sub(i, 1);
+  // the keys of the first `pre` sub-chunks not loaded early (sub-chunks the
+  // early pass did not start are loaded whole)
+  for (int i = 0; i < pre; ++i) load_sub(i, false, 0, i < pre_early ? early_keys : 0);
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
@@ -147,7 +169,7 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
   for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
   for (int i = 0; i < n; ++i) {
-    if (i + DEC_STAGES - 1 < n) load_sub(i + DEC_STAGES - 1, 2);
+    if (i + DEC_STAGES - 1 < n) load_sub(i + DEC_STAGES - 1, false, 0, 0);
     cp_async_commit();
     cp_async_wait<DEC_STAGES - 1>();
     __syncthreads();
@@ -173,7 +195,7 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int key = k0 + wk + j * 8 + (lane & 3) * 2 + e;
-        const bool ok = key < ctx;
+        const bool ok = key < ctx && key >= klo;
         s[j][e] = ok ? s[j][e] * scale_log2 : -INFINITY;
         s[j][2 + e] = ok ? s[j][2 + e] * scale_log2 : -INFINITY;
         mx_lo = fmaxf(mx_lo, s[j][e]);
@@ -253,7 +275,7 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
   __syncthreads();
   // per head row: the CTA's max and sum over its warps
   float cm = -INFINITY, cl = 0.f;
-  if (tid < n_head) {
+  if (tid < nq) {
     for (int w = 0; w < DEC_WARPS; ++w) cm = fmaxf(cm, red[(w * 16 + tid) * 2]);
     for (int w = 0; w < DEC_WARPS; ++w) {
       const float mw = red[(w * 16 + tid) * 2];
@@ -265,14 +287,14 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
     // CTA of the cluster waits on a cluster barrier in this case)
     if (grp != 0) return;
     float* inv_l1 = reinterpret_cast<float*>(att_smem);         // the Q tile is in registers
-    if (tid < n_head) inv_l1[tid] = 1.f / cl;
+    if (tid < nq) inv_l1[tid] = 1.f / cl;
     __syncthreads();
     // thread = output column of every other head row
-    for (int r = tid >> 7; r < n_head; r += DEC_THREADS / 128) {
+    for (int r = tid >> 7; r < nq; r += DEC_THREADS / 128) {
       float acc = 0.f;
 #pragma unroll
       for (int w = 0; w < DEC_WARPS; ++w) acc += ored[(w * 16 + r) * 128 + ocol];
-      O[((size_t)b * n_head + r) * ATT_HD + ocol] = f2bf(acc * inv_l1[r]);
+      O[((size_t)b * n_head + h0 + r) * ATT_HD + ocol] = f2bf(acc * inv_l1[r]);
     }
     return;
   }
@@ -282,20 +304,20 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
   // every rank in rank order (the result does not depend on timing)
   float* po = reinterpret_cast<float*>(att_smem + 16 * 256 + DEC_WARPS * 16 * 128 * 4);  // [16][128]
   float* pml = po + 16 * 128;                                                            // [16][2]
-  for (int r = tid >> 7; r < n_head; r += DEC_THREADS / 128) {
+  for (int r = tid >> 7; r < nq; r += DEC_THREADS / 128) {
     float acc = 0.f;
 #pragma unroll
     for (int w = 0; w < DEC_WARPS; ++w) acc += ored[(w * 16 + r) * 128 + ocol];
     po[r * 128 + ocol] = acc;
   }
-  if (tid < n_head) {
+  if (tid < nq) {
     pml[tid * 2 + 0] = cm;
     pml[tid * 2 + 1] = cl;
   }
   cluster_sync_all();
   const int G = (int)gridDim.x;
   const uint32_t po_s = smem_u32(po), pml_s = smem_u32(pml);
-  for (int r = grp + G * (tid >> 7); r < n_head; r += G * (DEC_THREADS / 128)) {
+  for (int r = grp + G * (tid >> 7); r < nq; r += G * (DEC_THREADS / 128)) {
     float mg[DEC_MAX_GROUPS], lg[DEC_MAX_GROUPS], og[DEC_MAX_GROUPS];
 #pragma unroll
     for (int g = 0; g < DEC_MAX_GROUPS; ++g) {
@@ -315,7 +337,7 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
       l += lg[g] * f;
       acc += og[g] * f;
     }
-    O[((size_t)b * n_head + r) * ATT_HD + ocol] = f2bf(acc * (1.f / l));
+    O[((size_t)b * n_head + h0 + r) * ATT_HD + ocol] = f2bf(acc * (1.f / l));
   }
   cluster_sync_all();                                          // remote reads done before any CTA exits
 }

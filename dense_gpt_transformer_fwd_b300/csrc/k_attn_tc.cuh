@@ -7,9 +7,18 @@
 // 1/sqrt(head_dim) as in SDPA (apidog.com/th "train your own ChatGPT", "how
 // nanochat works" item 5); query t attends to keys 0..t.
 //
+// Grouped-query attention with sliding windows (apidog.com/th item 1): query
+// head h reads K/V head h / G, G = n_head / n_kv (G = n_head is multi-query
+// attention), and a layer with a window sees only the last `window` keys.
+//
 // One CTA = one batch row, one tile of 128 query positions and TWO query
-// heads (tiles "A" and "B"), which share every K and V tile it loads.  Per
-// 128-key block j:
+// heads of one K/V group (tiles "A" and "B"), which share every K and V tile
+// it loads (with G odd, the last pair of a group repeats its one head in tile
+// B and does not store it).  The
+// queries of row b of a prefill chunk sit at positions p0 .. p0 + T - 1,
+// p0 = pos0[b], and read the keys 0 .. p0 + T - 1 of the cache (p0 = 0 for a
+// whole prompt; a later chunk continues each row's cache).  Per 128-key
+// block j:
 //   S_t   = Q_t K_j^T          tcgen05.mma M=128 N=128 K=128   (TMEM, fp32)
 //   P_t   = exp2(S_t * c - m)  softmax threads, bf16, into shared memory
 //   O_t  += P_t V_j            tcgen05.mma M=128 N=128 K=128   (TMEM, fp32)
@@ -21,8 +30,8 @@
 //
 // Operands (all K-major bf16 tiles with the 128-byte swizzle, boxes of 64
 // columns x 128 rows): Q from the query buffer viewed as [B][T][n_head*128];
-// K from this layer's cache [B_max][S][128]; V from a transposed copy
-// V^T [B_max][128][S_vt] that the QKV epilogue writes during the prefill, so
+// K from this layer's cache [B_max * n_kv][S][128]; V from a transposed copy
+// V^T [B_max * n_kv][128][S_vt] that the QKV epilogue writes during the prefill, so
 // that P V is again an A * B^T product with B = V^T.  O is staged in the P
 // buffer and written by a TMA store into the attention output
 // [B][T][n_head*128]; the tensor maps clip rows t >= T.
@@ -41,6 +50,9 @@ namespace nc {
 
 struct AttnTcArgs {
   int B, T, n_head, n_qt;          // n_qt = ceil(T / 128)
+  int n_kv;                        // K/V heads; query head h reads K/V head h / (n_head / n_kv)
+  int window;                      // sliding window (keys p - window + 1 .. p); 0 = unrestricted
+  const int* pos0;                 // [B] position of each row's first query (its cache length before the chunk)
   float scale_log2;                // log2(e) / sqrt(head_dim)
   int* err;
   unsigned long long wait_limit_ns;
@@ -119,14 +131,26 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
             DRAIN = 15;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pairs = args.n_head >> 1;
-  // heavy query tiles first: item -> (query tile, batch row, head pair)
+  const int G = args.n_head / args.n_kv;             // query heads per K/V head
+  const int pg_n = (G + 1) >> 1;                     // head pairs per group
+  const int pairs = args.n_kv * pg_n;
+  // heavy query tiles first: item -> (query tile, batch row, K/V group, pair)
   const int per_qt = args.B * pairs;
   const int qt = args.n_qt - 1 - (int)(blockIdx.x / per_qt);
   const int rest = (int)(blockIdx.x % per_qt);
   const int b = rest / pairs, hp = rest % pairs;
+  const int g = hp / pg_n;
+  const int h0 = g * G + 2 * (hp % pg_n);            // tile A's head
+  const int h1 = min(h0 + 1, g * G + G - 1);         // tile B's head (== h0: not stored)
+  const int bkv = b * args.n_kv + g;                 // K/V cache sequence of this CTA
   const int q0 = qt * 128;
-  const int nb = qt + 1;                             // key blocks 0 .. qt
+  // query row r sits at position qpos0 + r and sees keys max(0, qpos0 + r -
+  // window + 1) .. qpos0 + r; the keys of the cache end at pos0 + T - 1
+  const int p0 = args.pos0[b];
+  const int qpos0 = p0 + q0;
+  const int last_key = min(qpos0 + 127, p0 + args.T - 1);
+  const int jfirst = args.window > 0 ? max(0, qpos0 - args.window + 1) / 128 : 0;
+  const int nb = last_key / 128 + 1 - jfirst;        // key blocks jfirst .. jfirst + nb - 1
   const uint64_t limit = args.wait_limit_ns;
 
   if (threadIdx.x == 0) {
@@ -167,6 +191,12 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     fail();
     return false;
   };
+  // the softmax warps read TMEM with warp-collective loads: a wait they take
+  // ends the same way for every lane of the warp
+  auto wait_warp = [&](int i, uint32_t parity) -> bool {
+    const bool r = wait(i, parity);
+    return __all_sync(0xffffffffu, r);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -180,17 +210,17 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
       for (int t = 0; t < 2; ++t)
         for (int h = 0; h < 2; ++h)
           tma_load_3d(s0 + ATC_OFF_Q + t * ATC_TILE + h * ATC_HALF, &tmQ, bar(QFULL),
-                      (2 * hp + t) * 128 + 64 * h, q0, b);
+                      (t == 0 ? h0 : h1) * 128 + 64 * h, q0, b);
       for (int i = 0; ok && i < 2 * nb; ++i) {
-        const int slot = i % 3, round = i / 3, j = i >> 1;
+        const int slot = i % 3, round = i / 3, j = jfirst + (i >> 1);
         if (!wait(KVFREE + slot, (round & 1) ^ 1)) { ok = false; break; }
         mbar_arrive_expect_tx(bar(KVFULL + slot), ATC_TILE);
         const uint32_t dst = s0 + ATC_OFF_KV + slot * ATC_TILE;
         for (int h = 0; h < 2; ++h) {
           if ((i & 1) == 0)
-            tma_load_3d(dst + h * ATC_HALF, &tmK, bar(KVFULL + slot), 64 * h, j * 128, b);
+            tma_load_3d(dst + h * ATC_HALF, &tmK, bar(KVFULL + slot), 64 * h, j * 128, bkv);
           else
-            tma_load_3d(dst + h * ATC_HALF, &tmVt, bar(KVFULL + slot), j * 128 + 64 * h, 0, b);
+            tma_load_3d(dst + h * ATC_HALF, &tmVt, bar(KVFULL + slot), j * 128 + 64 * h, 0, bkv);
         }
         inflight[slot] = round & 1;
       }
@@ -263,7 +293,7 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------- softmax
-    const int t = (warp - 2) >> 2;                  // tile: 0 = head 2hp, 1 = head 2hp+1
+    const int t = (warp - 2) >> 2;                  // tile: 0 = head h0, 1 = head h1
     const int qd = warp & 3;                        // TMEM lane quarter
     const int r = 32 * qd + lane;                   // row of the tile = query q0 + r
     const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
@@ -275,16 +305,26 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     float l = 0.f;                                  // running sum of exp2((s - m) * sl2)
     bool ok = true;
     for (int j = 0; ok && j < nb; ++j) {
-      if (!wait(SFULL + t, j & 1)) { ok = false; break; }
+      if (!wait_warp(SFULL + t, j & 1)) { ok = false; break; }
       tc_fence_after();
       float v[128];
       tmem_ld128(tS, v);                            // the whole row of S_t
       tc_fence_before();
       mbar_arrive(bar(SFREE + t));                  // S_t may be overwritten
-      if (j == qt) {                                // diagonal block: keys c > r are in the future
+      const int jb = jfirst + j;                    // the key block
+      const int lim = qpos0 + r - jb * 128;         // last key of the block this row may see
+      if (lim < 127) {                              // a diagonal block: later keys are in the future
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (c > r) v[c] = -INFINITY;
+          if (c > lim) v[c] = -INFINITY;
+      }
+      if (args.window > 0) {
+        const int lo = lim - args.window + 1;       // first key of the block inside the window
+        if (lo > 0) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c < lo) v[c] = -INFINITY;
+        }
       }
       // row max as a tree (8 independent chains) to keep the latency short
       float mk[8];
@@ -304,9 +344,10 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
         m = mx;
         rescale = j > 0;
       }
-      const float mb = m * sl2;
+      // no key seen yet (a window can mask a whole block of a row): P = 0
+      const float mb = m == -INFINITY ? 0.f : m * sl2;
       // P_t of the previous block must have been consumed (and O_t written)
-      if (j > 0 && !wait(PVDONE + t, (j - 1) & 1)) { ok = false; break; }
+      if (j > 0 && !wait_warp(PVDONE + t, (j - 1) & 1)) { ok = false; break; }
       tc_fence_after();
       // P = exp2(s * sl2 - m * sl2) in bf16, 8 columns (one 16-byte chunk) at
       // a time straight into shared memory; row sum in 8 partial sums
@@ -323,13 +364,17 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
                       pack_bf16_2(p[4], p[5]), pack_bf16_2(p[6], p[7]));
       }
       l += ((lk[0] + lk[1]) + (lk[2] + lk[3])) + ((lk[4] + lk[5]) + (lk[6] + lk[7]));
-      if (rescale) {
+      // tcgen05.ld / tcgen05.st are warp-collective: the whole warp takes the
+      // rescale path when any of its rows needs it, each row with its own
+      // factor (1 for rows that keep their reference max)
+      if (__any_sync(0xffffffffu, rescale)) {
+        const float f = rescale ? factor : 1.f;
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
           float o[32];
           tmem_ld32(tO + c, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= factor;
+          for (int i = 0; i < 32; ++i) o[i] *= f;
           tmem_st32(tO + c, o);
         }
         tmem_wait_st();
@@ -339,7 +384,7 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
       mbar_arrive(bar(PFULL + t));
     }
     // ---- epilogue: O / l -> bf16 -> P buffer -> TMA store
-    if (ok && !wait(PVDONE + t, (nb - 1) & 1)) ok = false;
+    if (ok && !wait_warp(PVDONE + t, (nb - 1) & 1)) ok = false;
     if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;
@@ -356,8 +401,8 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     // every thread of the tile reaches this barrier exactly once
     named_bar_sync(1 + t, 128);
     if (threadIdx.x == 64 + 128 * t) {
-      if (ok && !*abort_flag) {
-        const int head = 2 * hp + t;
+      if (ok && !*abort_flag && (t == 0 || h1 != h0)) {
+        const int head = t == 0 ? h0 : h1;
         tma_store_3d(&tmO, pbuf, head * 128, q0, b);
         tma_store_3d(&tmO, pbuf + ATC_HALF, head * 128 + 64, q0, b);
         bulk_commit();
@@ -370,6 +415,40 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+// V^T[s][dim][p] = V[s][p][dim] for the K/V sequences s = b * n_kv + g
+// (s < gridDim.y) and p in [0, P_b), P_b = pos0[b]: the transposed value
+// operand of the prefill attention for the positions written before the
+// current chunk (by an earlier chunk or by decode steps).  One CTA per (64
+// positions, sequence): 64 cache rows of 256 B through shared memory, read
+// and written with coalesced accesses.  Positions >= P_b are not touched.
+__global__ void __launch_bounds__(256) vt_fill_kernel(const __nv_bfloat16* __restrict__ V,
+                                                      __nv_bfloat16* __restrict__ vt, int cache_S, int vt_S,
+                                                      const int* __restrict__ pos0, int n_kv) {
+  __shared__ __align__(16) __nv_bfloat16 tile[64][128 + 8];
+  const int b = blockIdx.y, p0 = blockIdx.x * 64;   // b: the K/V sequence
+  const int P = pos0[b / n_kv];
+  if (p0 >= P) return;
+  for (int e = threadIdx.x; e < 64 * 16; e += 256) {
+    const int r = e >> 4, c = e & 15;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (p0 + r < P) v = *reinterpret_cast<const uint4*>(V + ((size_t)b * cache_S + p0 + r) * 128 + c * 8);
+    *reinterpret_cast<uint4*>(&tile[r][c * 8]) = v;
+  }
+  __syncthreads();
+  __nv_bfloat16* dst = vt + (size_t)b * 128 * vt_S + p0;
+  for (int e = threadIdx.x; e < 128 * 32; e += 256) {
+    const int d = e >> 5, j = (e & 31) * 2;
+    if (p0 + j + 1 < P) {
+      __nv_bfloat162 pr;
+      pr.x = tile[j][d];
+      pr.y = tile[j + 1][d];
+      *reinterpret_cast<__nv_bfloat162*>(dst + (size_t)d * vt_S + j) = pr;
+    } else if (p0 + j < P) {
+      dst[(size_t)d * vt_S + j] = tile[j][d];
+    }
+  }
 }
 
 }  // namespace nc

@@ -44,12 +44,12 @@ struct SkinnyArgs {
   // epilogue outputs
   float* x;                       // EPI_RESID: [B][N] fp32, += ; EPI_LOGITS: [B][N] fp32 out
   __nv_bfloat16* out_bf;          // EPI_RELU2: [B][N]; EPI_QKV: Q [B][n_head*128]
-  __nv_bfloat16* k_cache;         // EPI_QKV: this layer's K [B_max][S][128]
+  __nv_bfloat16* k_cache;         // EPI_QKV: this layer's K [B_max][n_kv][S][128]
   __nv_bfloat16* v_cache;
   const float* rope_cos;          // [S][64]
   const float* rope_sin;
-  const int* pos_dev;             // EPI_QKV: position of the new token (device)
-  int n_head, cache_S;
+  const int* pos_dev;             // EPI_QKV: [B] position of each row's new token (device)
+  int n_head, n_kv, cache_S;
   float eps, softcap;
   int* err;
   unsigned long long wait_limit_ns;
@@ -62,7 +62,7 @@ struct SkinnyArgs {
   float* ss_out;
   const float* ss_in;
   int n_ss, ss_ld;
-  int* len_inc;                   // EPI_LOGITS: the step's final kernel advances the cache length
+  int* len_inc;                   // EPI_LOGITS: the step's final kernel advances every row's cache length
 };
 
 // column blocks of 128 in a folded RMSNorm (d_model <= 2048)
@@ -75,7 +75,7 @@ struct SkCfg {
   static constexpr uint32_t STAGE_BYTES = W_BYTES + A_BYTES;
   static constexpr int STAGES = (int)(98304 / STAGE_BYTES) < 2 ? 2 : (int)(98304 / STAGE_BYTES);
   static constexpr uint32_t TMEM_COLS = NB < 32 ? 32 : NB;
-  // + row scales [NB], RoPE row [128] and position
+  // + barriers and flags (256 B), row scales [NB], slack
   static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + NB * 4 + 512 + 16;
   static_assert((size_t)STAGES * STAGE_BYTES >= (size_t)NB * 128 * 4, "partial tile must fit the ring");
 };
@@ -98,21 +98,15 @@ __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_addr, uint32_t rank
 // round trips instead of one per row.
 template <int S, int EPI>
 __device__ __forceinline__ void sk_reduce_epilogue(const SkinnyArgs& args, uint32_t psm, const float* r_s,
-                                                   const float* rope_s, const int* pos_s, int rank, int warp,
-                                                   int lane, int tile, float inv_cap) {
+                                                   int rank, int warp, int lane, int tile, float inv_cap) {
   constexpr int RPB = 16 / S > 8 ? 8 : 16 / S;
   const int c = 4 * lane;
   const int n0 = tile * 128;
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  // EPI_QKV: the tile is one head; rope row of the new token's position
-  const bool is_v = EPI == EPI_QKV && tile == args.n_head + 1;
-  float4 cs = zero, sn = zero;
-  int pos = 0;
-  if constexpr (EPI == EPI_QKV) {
-    pos = *pos_s;
-    cs = *reinterpret_cast<const float4*>(rope_s + 4 * (lane & 15));
-    sn = *reinterpret_cast<const float4*>(rope_s + 64 + 4 * (lane & 15));
-  }
+  // EPI_QKV: the tile is one head: a query head, one of the n_kv key heads,
+  // or one of the n_kv value heads (K/V head g)
+  const bool is_v = EPI == EPI_QKV && tile >= args.n_head + args.n_kv;
+  const int g = tile < args.n_head ? 0 : (is_v ? tile - args.n_head - args.n_kv : tile - args.n_head);
   for (int b0 = rank + S * warp; b0 < args.B; b0 += 4 * S * RPB) {
     float4 part[RPB][S], xo[RPB];
 #pragma unroll
@@ -142,7 +136,11 @@ __device__ __forceinline__ void sk_reduce_epilogue(const SkinnyArgs& args, uint3
         for (int k = 0; k < 4; ++k) v[k] *= rb;
       }
       if constexpr (EPI == EPI_QKV) {
+        // the row's new token sits at its own position (per-row cache lengths)
+        const int pos = args.pos_dev[b];
         if (!is_v) {
+          const float4 cs = __ldg(reinterpret_cast<const float4*>(args.rope_cos + (size_t)pos * 64 + 4 * (lane & 15)));
+          const float4 sn = __ldg(reinterpret_cast<const float4*>(args.rope_sin + (size_t)pos * 64 + 4 * (lane & 15)));
           // QK norm over the head's 128 dims, then RoPE on pairs (j, j + 64):
           // lanes 0..15 hold j = 4l..4l+3, lanes 16..31 their partners
           float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
@@ -160,7 +158,7 @@ __device__ __forceinline__ void sk_reduce_epilogue(const SkinnyArgs& args, uint3
         if (tile < args.n_head)
           dst = args.out_bf + (size_t)b * args.n_head * 128 + tile * 128;
         else
-          dst = (is_v ? args.v_cache : args.k_cache) + ((size_t)b * args.cache_S + pos) * 128;
+          dst = (is_v ? args.v_cache : args.k_cache) + (((size_t)b * args.n_kv + g) * args.cache_S + pos) * 128;
         uint2 pk;
         pk.x = pack_bf16(v[0], v[1]);
         pk.y = pack_bf16(v[2], v[3]);
@@ -214,8 +212,6 @@ __global__ void __launch_bounds__(128)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);   // [0] abort
   float* r_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);   // [NB] row scales
-  float* rope_s = r_s + NB;                                  // EPI_QKV: cos [64], sin [64] at pos
-  int* pos_s = reinterpret_cast<int*>(rope_s + 128);
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int FULL = 0, EMPTY = STAGES, DONE = 2 * STAGES;
 
@@ -310,8 +306,8 @@ __global__ void __launch_bounds__(128)
 
   // ------------------------------------------------------------- epilogue
   pdl_wait();                                        // x / positions of the previous kernels
-  // row scales (all n_ss loads in flight, summed in block order) and the
-  // RoPE row, while the MMAs run
+  // row scales (all n_ss loads in flight, summed in block order), while the
+  // MMAs run
   if (threadIdx.x < NB) {
     float r = 1.f;
     if (args.ss_in && threadIdx.x < args.B) {
@@ -326,21 +322,15 @@ __global__ void __launch_bounds__(128)
     }
     r_s[threadIdx.x] = r;
   }
-  if (EPI == EPI_QKV && threadIdx.x >= 64) {
-    const int pos = *args.pos_dev, j = threadIdx.x - 64;
-    rope_s[j] = args.rope_cos[(size_t)pos * 64 + j];
-    rope_s[64 + j] = args.rope_sin[(size_t)pos * 64 + j];
-    if (j == 0) *pos_s = pos;
-  }
-  if (EPI == EPI_LOGITS && args.len_inc && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
-    *args.len_inc += 1;                              // every reader of the length has finished
+  if (EPI == EPI_LOGITS && args.len_inc && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < args.B)
+    args.len_inc[threadIdx.x] += 1;                  // every reader of the lengths has finished
   const bool done_ok = mbar_wait(bar(DONE), 0, limit);
-  if (!done_ok && threadIdx.x == 0) fail();
+  if (!done_ok) fail();
   tc_fence_after();
   const int row = 32 * warp + lane;                  // weight row n0 + row
   const uint32_t taddr = tmem_base + ((uint32_t)(32 * warp) << 16);
-  __syncthreads();
-  const bool run = done_ok && !flags[0];
+  // the same decision in every thread: the TMEM loads below are warp-collective
+  const bool run = __syncthreads_and(done_ok) && !flags[0];
   const float inv_cap = 1.f / args.softcap;
 
   if (args.splits == 1 && EPI == EPI_LOGITS) {
@@ -373,14 +363,14 @@ __global__ void __launch_bounds__(128)
     if (run) {
       const int rank = (int)cluster_ctarank();
       switch (args.splits) {
-        case 1: sk_reduce_epilogue<1, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
-        case 2: sk_reduce_epilogue<2, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
-        case 3: sk_reduce_epilogue<3, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
-        case 4: sk_reduce_epilogue<4, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
-        case 5: sk_reduce_epilogue<5, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
-        case 6: sk_reduce_epilogue<6, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
-        case 7: sk_reduce_epilogue<7, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
-        default: sk_reduce_epilogue<8, EPI>(args, psm, r_s, rope_s, pos_s, rank, warp, lane, tile, inv_cap); break;
+        case 1: sk_reduce_epilogue<1, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 2: sk_reduce_epilogue<2, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 3: sk_reduce_epilogue<3, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 4: sk_reduce_epilogue<4, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 5: sk_reduce_epilogue<5, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 6: sk_reduce_epilogue<6, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 7: sk_reduce_epilogue<7, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        default: sk_reduce_epilogue<8, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
       }
     }
     cluster_sync_all();                              // remote reads done before any CTA exits

@@ -41,19 +41,20 @@ enum GemmEpi : int {
 struct GemmArgs {
   int M, N, K;
   // EPI_QKV
-  __nv_bfloat16* k_cache;         // this layer's K: [B_max][S][128]
-  __nv_bfloat16* v_cache;         // this layer's V: [B_max][S][128]
+  __nv_bfloat16* k_cache;         // this layer's K: [B_max][n_kv][S][128]
+  __nv_bfloat16* v_cache;         // this layer's V: [B_max][n_kv][S][128]
   const float* rope_cos;          // [S][64]
   const float* rope_sin;          // [S][64]
   const float* rope_cos_t;        // the same tables dim-major: [64][S]
   const float* rope_sin_t;
   // K and V caches of all layers as [rows][128] bf16 tensor maps in device
-  // memory ([0] K, [1] V; 32 x 64 boxes); this layer's cache row (b, pos) is
-  // kv_row0 + b * cache_S + pos
+  // memory ([0] K, [1] V; 32 x 64 boxes); this layer's cache row (b, g, pos)
+  // of K/V head g is kv_row0 + (b * n_kv + g) * cache_S + pos
   const CUtensorMap* tm_kv;
   long long kv_row0;
-  int n_head, T, pos0, cache_S;
-  __nv_bfloat16* vt;              // optional V^T [B_max][128][vt_S] for the prefill attention
+  int n_head, n_kv, T, cache_S;
+  const int* pos0;                // [B] each row's first position (its cache length before the call)
+  __nv_bfloat16* vt;              // optional V^T [B_max * n_kv][128][vt_S] for the prefill attention
   int vt_S;
   float eps;
   // EPI_LOGITS
@@ -387,7 +388,10 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
     int local = 0;
     for (int u = unit0; u < num_units; u += ustride, ++local) {
       const int acc = local & 1;
-      if (*abort_flag || !mbar_wait(bar(TFULL + acc), (local >> 1) & 1, limit)) {
+      // the epilogue reads TMEM with warp-collective loads: every lane of the
+      // warp leaves or stays together
+      const bool full = !*abort_flag && mbar_wait(bar(TFULL + acc), (local >> 1) & 1, limit);
+      if (!__all_sync(0xffffffffu, full)) {
         if (!*abort_flag) fail();
         break;
       }
@@ -451,11 +455,12 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
         }
       } else if constexpr (EPI == EPI_QKV) {
         // BN covers BN/128 whole heads (head_dim 128); each warp owns HALF/128
-        // heads.  Columns [0, n_head*128) are query heads, then the key head,
-        // then the value head.  The two halves of a head (dims 0..63, 64..127)
-        // go to the warp's two staging buffers.
-        const int b = my_row / args.T;
-        const int pos = args.pos0 + (my_row - b * args.T);
+        // heads.  Columns [0, n_head*128) are query heads, then the n_kv key
+        // heads, then the n_kv value heads.  The two halves of a head (dims
+        // 0..63, 64..127) go to the warp's two staging buffers.
+        const int b_last = (args.M - 1) / args.T;
+        const int b = min(my_row / args.T, b_last);     // rows >= M use the last row's start
+        const int pos = args.pos0[b] + (my_row - b * args.T);
         const int pos_c = pos < args.cache_S ? pos : args.cache_S - 1;   // rows >= M only
         const uint32_t bufA = buf0, bufB = buf0 + C::EP_BUF;
         // the warp's 32 rows are consecutive positions of one sequence (then
@@ -465,7 +470,9 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
 #pragma unroll 1
         for (int hh = 0; hh < HALF / 128; ++hh) {
           const int head = ((n0 + ch0) >> 7) + hh;
-          const bool is_v = head == args.n_head + 1;
+          const bool is_v = head >= args.n_head + args.n_kv;
+          // K/V head of a key or value column block
+          const int g = head < args.n_head ? 0 : (is_v ? head - args.n_head - args.n_kv : head - args.n_head);
           const uint32_t hbase = taddr + hh * 128;
           // RoPE factors of dims c..c+31 at this row's position from the
           // dim-major tables: for each dim the warp reads 32 consecutive
@@ -511,7 +518,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
             if (is_v && args.vt != nullptr && my_row < args.M) {
               // transposed copy V^T[b][dim][pos]: lanes (consecutive positions)
               // write consecutive addresses for each dim
-              __nv_bfloat16* vt = args.vt + (size_t)b * 128 * args.vt_S + pos;
+              __nv_bfloat16* vt = args.vt + (size_t)(b * args.n_kv + g) * 128 * args.vt_S + pos;
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 vt[(size_t)(c + j) * args.vt_S] = f2bf(a[j]);
@@ -543,7 +550,8 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
             __syncwarp();
             if (lane == 0) {
               const CUtensorMap* tkv = args.tm_kv + (is_v ? 1 : 0);
-              const int crow = (int)(args.kv_row0 + (long long)b0w * args.cache_S + args.pos0 + (row0 - b0w * args.T));
+              const int crow = (int)(args.kv_row0 + ((long long)b0w * args.n_kv + g) * args.cache_S +
+                                     args.pos0[b0w] + (row0 - b0w * args.T));
               tma_store_2d(tkv, bufA, 0, crow);
               tma_store_2d(tkv, bufB, 64, crow);
               bulk_commit();
@@ -557,9 +565,9 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
               const int m = row0 + r;
               if (m < args.M) {
                 const int rb = m / args.T;
-                const int rp = args.pos0 + (m - rb * args.T);
+                const int rp = args.pos0[rb] + (m - rb * args.T);
                 uint32_t* dst = reinterpret_cast<uint32_t*>(
-                    (is_v ? args.v_cache : args.k_cache) + ((size_t)rb * args.cache_S + rp) * 128);
+                    (is_v ? args.v_cache : args.k_cache) + (((size_t)rb * args.n_kv + g) * args.cache_S + rp) * 128);
                 const uint32_t off = ((lane >> 2) ^ (r & 7)) * 16 + (lane & 3) * 4;
                 dst[lane] = ld_shared_u32(bufA + r * 128 + off);
                 dst[lane + 32] = ld_shared_u32(bufB + r * 128 + off);

@@ -22,13 +22,10 @@ namespace nc {
 template <typename TW, typename TA>
 __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tok, const TW* __restrict__ E,
                                      float* __restrict__ x, TA* __restrict__ h, int M, int d,
-                                     int vocab, float eps, int* err, int* len_set, int len_val,
-                                     float* __restrict__ ss_out, int ss_ld) {
+                                     int vocab, float eps, int* err, float* __restrict__ ss_out, int ss_ld) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
   pdl_wait();
-  // the prefill records the cache length on the device for the decode steps
-  if (len_set && blockIdx.x == 0 && threadIdx.x == 0) *len_set = len_val;
   if (warp >= M) return;
   int t = tok[warp];
   if (t < 0 || t >= vocab) {
@@ -69,20 +66,24 @@ __global__ void embed_rmsnorm_kernel(const int32_t* __restrict__ tok, const TW* 
   for (int j = lane; j < d; j += 32) h[(size_t)warp * d + j] = from_f<TA>(x[(size_t)warp * d + j] * r1);
 }
 
-// One warp per output row: h[i] = TA(rms(x[src_row(i)])), src_row(i) = i*stride + offset
-// (stride 1, offset 0 for all rows; stride T, offset T-1 for the last position of each row).
+// One warp per output row: h[i] = TA(rms(x[src_row(i)])), src_row(i) =
+// i*stride + (last ? last[i] : 0): stride 1 and no `last` for all rows;
+// stride T and last[i] = the index of row i's last token for the last
+// position of each row.
 template <typename TA>
 __global__ void rmsnorm_kernel(const float* __restrict__ x, TA* __restrict__ h, int rows, int d,
-                               int stride, int offset, float eps, int* len_inc) {
+                               int stride, const int* __restrict__ last, float eps, int* len_inc) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
   pdl_wait();
   // the final norm of a decode step on the generic path (fp32 models, or a
-  // batch wider than the decode GEMMs) advances the device-side cache length;
-  // every kernel of the step that reads it has finished (stream order)
-  if (len_inc && blockIdx.x == 0 && threadIdx.x == 0) *len_inc += 1;
+  // batch wider than the decode GEMMs) advances every row's device-side
+  // cache length; every kernel of the step that reads them has finished
+  // (stream order)
+  if (len_inc && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < rows; i += blockDim.x) len_inc[i] += 1;
   if (warp >= rows) return;
-  const float* xr = x + ((size_t)warp * stride + offset) * d;
+  const float* xr = x + ((size_t)warp * stride + (last ? last[warp] : 0)) * d;
   float ss = 0.f;
   if ((d & 127) == 0) {
     for (int j = lane * 4; j < d; j += 128) {
@@ -153,26 +154,28 @@ __global__ void __launch_bounds__(256) gemm_simt_f32_kernel(const float* __restr
   }
 }
 
-// One warp per (row m, head slot): slots [0, n_head) are query heads, n_head
-// the key head, n_head + 1 the value head.  q and k: RoPE at the row's
-// position, then RMSNorm over head_dim; v: copied.  q goes to Q [M, n_head*hd],
-// k and v to the cache row (b, pos).  Each lane holds elements lane + 32 i, so
-// both members of a rotation pair (j, j + hd/2) sit in the same lane.
+// One warp per (row m, head slot): slots [0, n_head) are query heads, then
+// n_kv key heads, then n_kv value heads.  q and k: RoPE at the row's
+// position pos0[b] + t, then RMSNorm over head_dim; v: copied.  q goes to
+// Q [M, n_head*hd], k and v of K/V head g to the cache row (b, g, pos).  Each lane holds
+// elements lane + 32 i, so both members of a rotation pair (j, j + hd/2) sit
+// in the same lane.
 template <typename TA, typename TC>
 __global__ void qkv_post_kernel(const float* __restrict__ qkv, TA* __restrict__ q_out,
                                 TC* __restrict__ k_cache, TC* __restrict__ v_cache,
                                 const float* __restrict__ rope_cos, const float* __restrict__ rope_sin,
-                                int M, int n_head, int hd, int T, int pos0, int cache_S, float eps) {
+                                int M, int n_head, int n_kv, int hd, int T, const int* __restrict__ pos0,
+                                int cache_S, float eps) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  const int slots = n_head + 2;
+  const int slots = n_head + 2 * n_kv;
   if (warp >= M * slots) return;
   const int m = warp / slots, head = warp % slots;
-  const int b = m / T, pos = pos0 + (m % T);
+  const int b = m / T, pos = pos0[b] + (m % T);
   const int per = hd / 32, half = hd / 2;     // hd in {64, 128}
   const float* src = qkv + (size_t)m * (slots * hd) + head * hd;
   float v[4];
   for (int i = 0; i < per; ++i) v[i] = src[lane + 32 * i];
-  if (head <= n_head) {
+  if (head < n_head + n_kv) {                   // query or key: RoPE + QK-norm
     float ss = 0.f;
     for (int i = 0; i < per; ++i) ss = fmaf(v[i], v[i], ss);
     ss = warp_sum(ss);
@@ -189,8 +192,32 @@ __global__ void qkv_post_kernel(const float* __restrict__ qkv, TA* __restrict__ 
     TA* dst = q_out + (size_t)m * (n_head * hd) + head * hd;
     for (int i = 0; i < per; ++i) dst[lane + 32 * i] = from_f<TA>(v[i]);
   } else {
-    TC* dst = (head == n_head ? k_cache : v_cache) + ((size_t)b * cache_S + pos) * hd;
+    const bool is_v = head >= n_head + n_kv;
+    const int g = is_v ? head - n_head - n_kv : head - n_head;
+    TC* dst = (is_v ? v_cache : k_cache) + (((size_t)b * n_kv + g) * cache_S + pos) * hd;
     for (int i = 0; i < per; ++i) dst[lane + 32 * i] = from_f<TC>(v[i]);
+  }
+}
+
+// Per-row cache bookkeeping of one call, written on the device in stream
+// order for rows base .. base + n - 1: pos0[b] = the row's cache length
+// before the call (the position of its first new token), len[b] = its length
+// after the call, last[b] = the index of its last token in the call's
+// [B][T] token array.  The values travel in the kernel's parameters, so the
+// host may reuse its buffers at once.
+constexpr int ROWSET_MAX = 256;
+struct RowSet {
+  int n, base;
+  int32_t pos0[ROWSET_MAX], len[ROWSET_MAX], last[ROWSET_MAX];
+};
+__global__ void set_rows_kernel(const RowSet rs, int* __restrict__ pos0, int* __restrict__ len,
+                                int* __restrict__ last) {
+  pdl_trigger();
+  pdl_wait();
+  for (int i = threadIdx.x; i < rs.n; i += blockDim.x) {
+    pos0[rs.base + i] = rs.pos0[i];
+    len[rs.base + i] = rs.len[i];
+    last[rs.base + i] = rs.last[i];
   }
 }
 

@@ -16,10 +16,12 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <utility>
 #include <vector>
@@ -30,6 +32,7 @@
 #include "k_gemm_skinny.cuh"
 #include "k_gemm_tc.cuh"
 #include "k_rowops.cuh"
+#include "k_sample.cuh"
 #include "nc_common.cuh"
 
 using namespace nc;
@@ -126,6 +129,61 @@ inline unsigned blocks_for_warps(int64_t warps, int threads = 256) {
   return (unsigned)((warps * 32 + threads - 1) / threads);
 }
 
+// The intermediates of one decode step on the decode GEMMs: the fp32
+// residual x [rows][d], h = bf16(x) [rows][d], per-128-column sums of squares
+// of x ss [d/128][ss_ld], the query q and attention output att [rows][n_head*128],
+// the MLP hidden u [rows][d_mlp], and the tensor maps the decode GEMMs read
+// h, att and u through (boxes of NB rows x 64 columns).
+struct DecodeBufs {
+  float* x = nullptr;
+  void* h = nullptr;
+  void* q = nullptr;
+  void* att = nullptr;
+  void* u = nullptr;
+  float* ss = nullptr;
+  int ss_ld = 0;
+  CUtensorMap tm_h_nb{}, tm_att_nb{}, tm_u_nb{};
+};
+
+// ------------------------------------------------ no-allocation decode scratch
+// nc_decode_step_noalloc keeps the decode step's intermediates (a DecodeBufs
+// set) in this file-scope device array instead of model memory, so that a
+// decode step can run for callers that may not allocate.  Limits: at most
+// kNaRows rows, d_model <= kNaD, n_head * 128 <= kNaNQ, d_mlp <= kNaF; the
+// array is 4.5 MiB and every GPU that loads the library holds it until the
+// process exits.
+constexpr int kNaRows = 128, kNaD = 2048, kNaNQ = 2048, kNaF = 8192;
+constexpr size_t na_round(size_t b) { return (b + 255) / 256 * 256; }
+constexpr size_t kNaOffX = 0;
+constexpr size_t kNaOffH = kNaOffX + na_round((size_t)kNaRows * kNaD * 4);
+constexpr size_t kNaOffQ = kNaOffH + na_round((size_t)kNaRows * kNaD * 2);
+constexpr size_t kNaOffAtt = kNaOffQ + na_round((size_t)kNaRows * kNaNQ * 2);
+constexpr size_t kNaOffU = kNaOffAtt + na_round((size_t)kNaRows * kNaNQ * 2);
+constexpr size_t kNaOffSS = kNaOffU + na_round((size_t)kNaRows * kNaF * 2);
+constexpr size_t kNaBytes = kNaOffSS + na_round((size_t)(kNaD / 128) * kNaRows * 4);
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaBytes];
+
+// Device address of the scratch on device `dev`, which must be current.  In
+// host code the array's name is a host-side stand-in, not a device address:
+// the address is looked up with cudaGetSymbolAddress once per device (at the
+// creation of the first model on it) and cached.
+constexpr int kNaMaxDevices = 64;
+std::mutex g_na_mutex;
+void* g_na_addr[kNaMaxDevices] = {};
+
+cudaError_t noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= kNaMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_na_mutex);
+  if (!g_na_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_na_addr[dev] = p;
+  }
+  *out = g_na_addr[dev];
+  return cudaSuccess;
+}
+
 }  // namespace
 
 struct nc_model {
@@ -171,12 +229,21 @@ struct nc_model {
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_used = 0;
   std::vector<ProfRec> recs;
-  int* d_len = nullptr;                // device copy of the cache length (decode reads it)
+  // per-row cache lengths: host mirror, and device arrays [max_batch] that the
+  // kernels read: the length (decode), the start position of the current
+  // call's tokens (prefill) and the index of each row's last token
+  std::vector<int32_t> lens;
+  int* d_len = nullptr;
+  int* d_pos0 = nullptr;
+  int* d_last = nullptr;
   // decode-step skinny GEMMs (bf16, B <= sk_nb)
   int sk_nb = 0;                       // padded batch of the MMA N operand: 32, 64 or 128 (0 = off)
   int sk_splits[4] = {1, 1, 1, 1};     // K splits of QKV, O-proj, FC, PROJ
   std::vector<CUtensorMap> tm_w128;    // per layer Wqkv, Wo, Wfc, Wproj, box 64 x 128 rows
-  CUtensorMap tm_wu128{}, tm_h_nb{}, tm_att_nb{}, tm_u_nb{};
+  CUtensorMap tm_wu128{};
+  DecodeBufs dbuf;                     // the decode step's intermediates in the workspace above
+  DecodeBufs dbuf_na;                  // the same in the no-allocation scratch (nc_decode_step_noalloc)
+  bool noalloc_ok = false;             // the model's shape fits the no-allocation scratch
   // captured decode step
   cudaStream_t cap_stream = nullptr;
   cudaGraphExec_t g_exec = nullptr;
@@ -206,7 +273,7 @@ void free_model(nc_model* m) {
   void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->rope_cos_t, m->rope_sin_t, m->d_tm_kv,
                   m->k_alloc, m->v_alloc, m->x,
                   m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
-                  m->tok_stage, m->logit_stage, m->err, m->vt, m->d_len, m->ss_part};
+                  m->tok_stage, m->logit_stage, m->err, m->vt, m->d_len, m->d_pos0, m->d_last, m->ss_part};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete m;
@@ -250,10 +317,11 @@ nc_status validate(const nc_config* c) {
       c->vocab < 1 || c->max_batch < 1 || c->max_seq < 1 || !(c->rope_base > 0.f) ||
       !(c->softcap > 0.f) || !(c->rms_eps >= 0.f) || (c->dtype != NC_F32 && c->dtype != NC_BF16))
     return NC_ERR_INVALID_ARG;
-  if (c->n_kv_head != 1) return NC_ERR_UNSUPPORTED;
+  if (c->n_kv_head < 1 || c->n_head % c->n_kv_head || c->window < 0) return NC_ERR_INVALID_ARG;
+  if (c->window > 0 && c->n_layer > 64) return NC_ERR_UNSUPPORTED;   // one bit per layer
   if (c->dtype == NC_BF16) {
     if (c->head_dim != 128 || c->d_model % 256 || c->d_mlp % 256 || c->vocab % 256 ||
-        ((c->n_head + 2) * 128) % 256 || c->n_head > 16 || c->n_head % 2)
+        ((c->n_head + 2 * c->n_kv_head) * 128) % 256 || c->n_head > 16 || c->n_head % 2)
       return NC_ERR_UNSUPPORTED;
   } else {
     if ((c->head_dim != 64 && c->head_dim != 128) || c->d_model % 32) return NC_ERR_UNSUPPORTED;
@@ -370,9 +438,11 @@ int choose_splits(int tiles, int kb, int sms) {
 // DEC_MAX_GROUPS groups (one cluster) per row; grid.x covers max_seq.  A batch
 // of num_sms / 2 rows or more gets one CTA per row, which writes its output
 // without a merge.
-void decode_attn_shape(const nc_model* m, int B, int* group, int* grid_x) {
-  const int max_sub = (m->cfg.max_seq + DEC_SUB - 1) / DEC_SUB;
-  int target = m->num_sms / B;
+void decode_attn_shape(const nc_model* m, int B, int window, int* group, int* grid_x) {
+  int max_sub = (m->cfg.max_seq + DEC_SUB - 1) / DEC_SUB;
+  // a window of W keys spans at most ceil(W / DEC_SUB) + 1 sub-chunks
+  if (window > 0) max_sub = std::min(max_sub, (window + DEC_SUB - 1) / DEC_SUB + 1);
+  int target = m->num_sms / (B * m->cfg.n_kv_head);    // one CTA per SM over the K/V sequences
   if (target < 1) target = 1;
   if (target > DEC_MAX_GROUPS) target = DEC_MAX_GROUPS;
   int g = (max_sub + target - 1) / target;
@@ -380,6 +450,13 @@ void decode_attn_shape(const nc_model* m, int B, int* group, int* grid_x) {
   if (g < min_g) g = min_g;
   *group = g;
   *grid_x = (max_sub + g - 1) / g;
+}
+
+// Sliding window of layer l: the config's window where bit l of
+// window_layers is set, else 0 (the whole causal context).
+int layer_window(const nc_model* m, int l) {
+  const nc_config& c = m->cfg;
+  return (c.window > 0 && l < 64 && ((c.window_layers >> l) & 1ull)) ? c.window : 0;
 }
 
 GemmArgs base_args(nc_model* m, int M, int N, int K) {
@@ -405,19 +482,26 @@ cudaError_t launch_simt_gemm(nc_model* m, const float* A, const float* W, float*
   return cudaGetLastError();
 }
 
-// The whole forward pass over M = B*T rows at positions pos0 .. pos0+T-1.
-nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float* logits,
-                  bool last_only, cudaStream_t s) {
+// The whole forward pass over M = B*T rows; row b's tokens sit at positions
+// p0_b .. p0_b + T - 1.  A prefill (p0_b = 0 for new sequences, or a later
+// chunk continuing each row's cache) reads p0_b from d_pos0 and, for
+// last_only, each row's last token index from d_last (both written by
+// set_rows before the call); `max_p0` is the largest p0_b.  With `decode`, one
+// generic decode step (T = 1, p0_b = the row's length, read from d_len).
+nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, float* logits,
+                  bool last_only, cudaStream_t s, bool decode = false) {
   const nc_config& c = m->cfg;
   const int M = B * T, d = c.d_model, hd = c.head_dim, nh = c.n_head, F = c.d_mlp, V = c.vocab;
-  const int NQKV = (nh + 2) * hd, NQ = nh * hd;
+  const int nkv = c.n_kv_head;
+  const int NQKV = (nh + 2 * nkv) * hd, NQ = nh * hd;
   const float eps = c.rms_eps;
   const int out_rows = last_only ? B : M;
   const bool bf = m->bf16;
+  const int* pos0 = decode ? m->d_len : m->d_pos0;    // [B] first position of each row's tokens
   using bf16 = __nv_bfloat16;
 
   CUtensorMap tm_qa[2];  // q and att viewed as [B][T][n_head*128], box 64 x 128 rows
-  if (bf && pos0 == 0 && T > 1) {
+  if (bf && T > 1) {
     const uint64_t dims[3] = {(uint64_t)NQ, (uint64_t)T, (uint64_t)B};
     const uint64_t strides[2] = {(uint64_t)NQ * 2, (uint64_t)T * NQ * 2};
     const uint32_t box[3] = {64, 128, 1};
@@ -426,19 +510,27 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
   }
   {  // x = rms(E[tok]); h = rms(x)
     KScope ks(m, NC_K_EMBED, s);
-    int* len_set = pos0 == 0 ? m->d_len : nullptr;   // prefill: device length := T
     if (bf)
       embed_rmsnorm_kernel<bf16, bf16><<<blocks_for_warps(M), 256, 0, s>>>(
           tok, static_cast<const bf16*>(m->E), m->x, static_cast<bf16*>(m->h), M, d, V, eps, m->err,
-          len_set, T, (float*)nullptr, 0);
+          (float*)nullptr, 0);
     else
       embed_rmsnorm_kernel<float, float><<<blocks_for_warps(M), 256, 0, s>>>(
           tok, static_cast<const float*>(m->E), m->x, static_cast<float*>(m->h), M, d, V, eps, m->err,
-          len_set, T, (float*)nullptr, 0);
+          (float*)nullptr, 0);
     m->launches++;
     NC_TRY(cudaGetLastError());
   }
   for (int l = 0; l < c.n_layer; ++l) {
+    if (bf && T > 1 && max_p0 > 0) {
+      // a later prefill chunk: the attention's V^T operand of the positions
+      // cached before it (the QKV epilogue below writes the chunk's own)
+      KScope ks(m, NC_K_ATTN, s);
+      vt_fill_kernel<<<dim3((max_p0 + 63) / 64, B * nkv), 256, 0, s>>>(
+          static_cast<const bf16*>(m->vc(l)), static_cast<bf16*>(m->vt), c.max_seq, m->vt_S, m->d_pos0, nkv);
+      m->launches++;
+      NC_TRY(cudaGetLastError());
+    }
     {  // [q;k;v] = h Wqkv^T; RoPE + QK-norm; q -> Q, k/v -> cache
       KScope ks(m, NC_K_QKV, s);
       if (bf) {
@@ -450,12 +542,13 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
         a.rope_cos_t = m->rope_cos_t;
         a.rope_sin_t = m->rope_sin_t;
         a.tm_kv = m->d_tm_kv;
-        a.kv_row0 = kGuardElems / 128 + (long long)l * c.max_batch * c.max_seq;
+        a.kv_row0 = kGuardElems / 128 + (long long)l * c.max_batch * nkv * c.max_seq;
         a.n_head = nh;
+        a.n_kv = nkv;
         a.T = T;
         a.pos0 = pos0;
         a.cache_S = c.max_seq;
-        if (pos0 == 0 && T > 1) {
+        if (T > 1) {
           a.vt = static_cast<bf16*>(m->vt);
           a.vt_S = m->vt_S;
         }
@@ -464,9 +557,9 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
         NC_TRY(launch_simt_gemm<SEPI_STORE>(m, static_cast<const float*>(m->h),
                                             static_cast<const float*>(m->wqkv[l]), m->c32, M, NQKV,
                                             d, NQKV, s));
-        qkv_post_kernel<float, float><<<blocks_for_warps((int64_t)M * (nh + 2)), 256, 0, s>>>(
+        qkv_post_kernel<float, float><<<blocks_for_warps((int64_t)M * (nh + 2 * nkv)), 256, 0, s>>>(
             m->c32, static_cast<float*>(m->q), static_cast<float*>(m->kc(l)),
-            static_cast<float*>(m->vc(l)), m->rope_cos, m->rope_sin, M, nh, hd, T, pos0, c.max_seq,
+            static_cast<float*>(m->vc(l)), m->rope_cos, m->rope_sin, M, nh, nkv, hd, T, pos0, c.max_seq,
             eps);
         m->launches++;
         NC_TRY(cudaGetLastError());
@@ -474,33 +567,38 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
     }
     {  // causal MQA attention over the cache
       KScope ks(m, NC_K_ATTN, s);
-      if (bf && pos0 == 0 && T > 1) {
+      if (bf && T > 1) {
         AttnTcArgs aa;
         aa.B = B;
         aa.T = T;
+        aa.pos0 = pos0;
         aa.n_head = nh;
+        aa.n_kv = nkv;
+        aa.window = layer_window(m, l);
         aa.n_qt = (T + 127) / 128;
         aa.scale_log2 = kAttnScaleLog2;
         aa.err = m->err;
         aa.wait_limit_ns = m->wait_limit_ns;
-        attn_prefill_tc_kernel<<<aa.n_qt * B * (nh / 2), ATC_THREADS, ATC_SMEM, s>>>(
+        // CTAs: query tiles x rows x K/V heads x head pairs of a group
+        attn_prefill_tc_kernel<<<aa.n_qt * B * nkv * ((nh / nkv + 1) / 2), ATC_THREADS, ATC_SMEM, s>>>(
             tm_qa[0], m->tm_kc[l], m->tm_vt, tm_qa[1], aa);
         m->launches++;
         NC_TRY(cudaGetLastError());
       } else if (bf) {
-        const int ctx = pos0 + 1;                     // decode: T == 1
+        // one position per row (T == 1): row b's context is pos0[b] + 1
         int group = 2, gx = 1;
-        decode_attn_shape(m, B, &group, &gx);
-        NC_TRY(launch_attn_decode(false, dim3(gx, B), s, static_cast<const bf16*>(m->q),
+        const int win = layer_window(m, l);
+        decode_attn_shape(m, B, win, &group, &gx);
+        NC_TRY(launch_attn_decode(false, dim3(gx, B * nkv), s, static_cast<const bf16*>(m->q),
                                   static_cast<const bf16*>(m->kc(l)), static_cast<const bf16*>(m->vc(l)),
-                                  static_cast<bf16*>(m->att), nh, (int)c.max_seq, ctx, (const int*)nullptr,
-                                  kAttnScaleLog2, group));
+                                  static_cast<bf16*>(m->att), nh, (int)c.max_seq, 0, pos0, kAttnScaleLog2,
+                                  group, nkv, win));
         m->launches++;
       } else {
         attn_simt_kernel<float, float><<<blocks_for_warps((int64_t)M * nh), 256, 0, s>>>(
             static_cast<const float*>(m->q), static_cast<const float*>(m->kc(l)),
-            static_cast<const float*>(m->vc(l)), static_cast<float*>(m->att), M, nh, hd, T, pos0,
-            c.max_seq);
+            static_cast<const float*>(m->vc(l)), static_cast<float*>(m->att), M, nh, nkv, hd, T, pos0,
+            c.max_seq, layer_window(m, l));
         m->launches++;
         NC_TRY(cudaGetLastError());
       }
@@ -518,11 +616,11 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
     {  // h = rms(x)
       KScope ks(m, NC_K_NORM, s);
       if (bf)
-        rmsnorm_kernel<bf16><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<bf16*>(m->h), M, d, 1, 0,
-                                                                 eps, nullptr);
+        rmsnorm_kernel<bf16><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<bf16*>(m->h), M, d, 1,
+                                                                 nullptr, eps, nullptr);
       else
-        rmsnorm_kernel<float><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<float*>(m->h), M, d, 1, 0,
-                                                                  eps, nullptr);
+        rmsnorm_kernel<float><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<float*>(m->h), M, d, 1,
+                                                                  nullptr, eps, nullptr);
       m->launches++;
       NC_TRY(cudaGetLastError());
     }
@@ -552,15 +650,16 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int pos0, float
       const bool final_last = last_only && l == c.n_layer - 1;
       const int rows = final_last ? B : M;
       void* dst = final_last ? m->h_last : m->h;
-      // a decode step on this generic path (pos0 > 0) advances the device-side
-      // length in its final norm
-      int* len_inc = (pos0 > 0 && l == c.n_layer - 1) ? m->d_len : nullptr;
+      // a decode step on this generic path advances the device-side length in
+      // its final norm
+      int* len_inc = (decode && l == c.n_layer - 1) ? m->d_len : nullptr;
+      const int* last = final_last ? m->d_last : nullptr;
       if (bf)
         rmsnorm_kernel<bf16><<<blocks_for_warps(rows), 256, 0, s>>>(
-            m->x, static_cast<bf16*>(dst), rows, d, final_last ? T : 1, final_last ? T - 1 : 0, eps, len_inc);
+            m->x, static_cast<bf16*>(dst), rows, d, final_last ? T : 1, last, eps, len_inc);
       else
         rmsnorm_kernel<float><<<blocks_for_warps(rows), 256, 0, s>>>(
-            m->x, static_cast<float*>(dst), rows, d, final_last ? T : 1, final_last ? T - 1 : 0, eps, len_inc);
+            m->x, static_cast<float*>(dst), rows, d, final_last ? T : 1, last, eps, len_inc);
       m->launches++;
       NC_TRY(cudaGetLastError());
     }
@@ -623,31 +722,32 @@ SkinnyArgs skinny_args(nc_model* m, int B, int N, int K, int splits) {
 // Every kernel takes the position from the device-side length, so the
 // sequence is the same at every step and can be replayed as a CUDA graph.
 template <int NB>
-nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logits, cudaStream_t s) {
+nc_status forward_decode_nb(nc_model* m, const DecodeBufs& db, const int32_t* tok, int B, float* logits,
+                            cudaStream_t s) {
   const nc_config& c = m->cfg;
   const int d = c.d_model, nh = c.n_head, F = c.d_mlp, V = c.vocab;
-  const int NQKV = (nh + 2) * 128, NQ = nh * 128;
+  const int nkv = c.n_kv_head;
+  const int NQKV = (nh + 2 * nkv) * 128, NQ = nh * 128;
   const float eps = c.rms_eps;
   using bf16 = __nv_bfloat16;
   // RMSNorm folded into the projections: every residual update writes
   // h = bf16(x) and per-block sums of squares; QKV, MLP up and lm_head scale
   // their rows by 1/rms(x) (r (x W^T) = (r x) W^T)
-  const int ss_ld = c.max_batch, n_ss = d / 128;
+  const int ss_ld = db.ss_ld, n_ss = d / 128;
   auto fold_in = [&](SkinnyArgs& a) {
-    a.ss_in = m->ss_part;
+    a.ss_in = db.ss;
     a.n_ss = n_ss;
     a.ss_ld = ss_ld;
   };
   auto fold_out = [&](SkinnyArgs& a) {
-    a.h_out = static_cast<bf16*>(m->h);
-    a.ss_out = m->ss_part;
+    a.h_out = static_cast<bf16*>(db.h);
+    a.ss_out = db.ss;
     a.ss_ld = ss_ld;
   };
   {
     KScope ks(m, NC_K_EMBED, s);
     embed_rmsnorm_kernel<bf16, bf16><<<blocks_for_warps(B), 256, 0, s>>>(
-        tok, static_cast<const bf16*>(m->E), m->x, static_cast<bf16*>(m->h), B, d, V, eps, m->err, nullptr, 0,
-        m->ss_part, ss_ld);
+        tok, static_cast<const bf16*>(m->E), db.x, static_cast<bf16*>(db.h), B, d, V, eps, m->err, db.ss, ss_ld);
     m->launches++;
     NC_TRY(cudaGetLastError());
   }
@@ -655,47 +755,49 @@ nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logit
     {
       KScope ks(m, NC_K_QKV, s);
       SkinnyArgs a = skinny_args(m, B, NQKV, d, m->sk_splits[0]);
-      a.out_bf = static_cast<bf16*>(m->q);
+      a.out_bf = static_cast<bf16*>(db.q);
       a.k_cache = static_cast<bf16*>(m->kc(l));
       a.v_cache = static_cast<bf16*>(m->vc(l));
       a.rope_cos = m->rope_cos;
       a.rope_sin = m->rope_sin;
       a.pos_dev = m->d_len;
       a.n_head = nh;
+      a.n_kv = nkv;
       a.cache_S = c.max_seq;
       fold_in(a);
-      NC_TRY((launch_skinny<NB, EPI_QKV>(m, m->tm_w128[4 * l + 0], m->tm_h_nb, a, NQKV / 128, s)));
+      NC_TRY((launch_skinny<NB, EPI_QKV>(m, m->tm_w128[4 * l + 0], db.tm_h_nb, a, NQKV / 128, s)));
     }
     {
       KScope ks(m, NC_K_ATTN, s);
       int group = 2, gx = 1;
-      decode_attn_shape(m, B, &group, &gx);
-      NC_TRY(launch_attn_decode(true, dim3(gx, B), s, static_cast<const bf16*>(m->q),
+      const int win = layer_window(m, l);
+      decode_attn_shape(m, B, win, &group, &gx);
+      NC_TRY(launch_attn_decode(true, dim3(gx, B * nkv), s, static_cast<const bf16*>(db.q),
                                 static_cast<const bf16*>(m->kc(l)), static_cast<const bf16*>(m->vc(l)),
-                                static_cast<bf16*>(m->att), nh, (int)c.max_seq, 0,
-                                static_cast<const int*>(m->d_len), kAttnScaleLog2, group));
+                                static_cast<bf16*>(db.att), nh, (int)c.max_seq, 0,
+                                static_cast<const int*>(m->d_len), kAttnScaleLog2, group, nkv, win));
       m->launches++;
     }
     {
       KScope ks(m, NC_K_OPROJ, s);
       SkinnyArgs a = skinny_args(m, B, d, NQ, m->sk_splits[1]);
-      a.x = m->x;
+      a.x = db.x;
       fold_out(a);
-      NC_TRY((launch_skinny<NB, EPI_RESID>(m, m->tm_w128[4 * l + 1], m->tm_att_nb, a, d / 128, s)));
+      NC_TRY((launch_skinny<NB, EPI_RESID>(m, m->tm_w128[4 * l + 1], db.tm_att_nb, a, d / 128, s)));
     }
     {
       KScope ks(m, NC_K_FC, s);
       SkinnyArgs a = skinny_args(m, B, F, d, m->sk_splits[2]);
-      a.out_bf = static_cast<bf16*>(m->u);
+      a.out_bf = static_cast<bf16*>(db.u);
       fold_in(a);
-      NC_TRY((launch_skinny<NB, EPI_RELU2>(m, m->tm_w128[4 * l + 2], m->tm_h_nb, a, F / 128, s)));
+      NC_TRY((launch_skinny<NB, EPI_RELU2>(m, m->tm_w128[4 * l + 2], db.tm_h_nb, a, F / 128, s)));
     }
     {
       KScope ks(m, NC_K_PROJ, s);
       SkinnyArgs a = skinny_args(m, B, d, F, m->sk_splits[3]);
-      a.x = m->x;
+      a.x = db.x;
       fold_out(a);
-      NC_TRY((launch_skinny<NB, EPI_RESID>(m, m->tm_w128[4 * l + 3], m->tm_u_nb, a, d / 128, s)));
+      NC_TRY((launch_skinny<NB, EPI_RESID>(m, m->tm_w128[4 * l + 3], db.tm_u_nb, a, d / 128, s)));
     }
   }
   {
@@ -704,7 +806,7 @@ nc_status forward_decode_nb(nc_model* m, const int32_t* tok, int B, float* logit
     a.x = logits;
     fold_in(a);
     a.len_inc = m->d_len;                            // the step's last kernel
-    NC_TRY((launch_skinny<NB, EPI_LOGITS>(m, m->tm_wu128, m->tm_h_nb, a, V / 128, s)));
+    NC_TRY((launch_skinny<NB, EPI_LOGITS>(m, m->tm_wu128, db.tm_h_nb, a, V / 128, s)));
   }
   return NC_OK;
 }
@@ -756,6 +858,8 @@ cudaError_t configure_kernels(const nc_model* m) {
                               (int)ATT_DECODE_SMEM));
     step(load_kernel(embed_rmsnorm_kernel<bf16, bf16>));
     step(load_kernel(rmsnorm_kernel<bf16>));
+    step(load_kernel(vt_fill_kernel));
+    step(load_kernel(set_rows_kernel));
   } else {
     step(load_kernel(gemm_simt_f32_kernel<SEPI_STORE>));
     step(load_kernel(gemm_simt_f32_kernel<SEPI_RESID>));
@@ -765,18 +869,23 @@ cudaError_t configure_kernels(const nc_model* m) {
     step(load_kernel(attn_simt_kernel<float, float>));
     step(load_kernel(embed_rmsnorm_kernel<float, float>));
     step(load_kernel(rmsnorm_kernel<float>));
+    step(load_kernel(set_rows_kernel));
   }
+  step(load_kernel(sample_kernel));
+  step(load_kernel(kv_clone_kernel));
   return e;
 }
 
 bool decode_on_skinny(const nc_model* m, int B) { return m->bf16 && m->sk_nb > 0 && B <= m->sk_nb; }
 
-nc_status forward_decode(nc_model* m, const int32_t* tok, int B, float* logits, cudaStream_t s) {
-  if (!decode_on_skinny(m, B)) return forward(m, tok, B, 1, m->length, logits, false, s);
+nc_status forward_decode(nc_model* m, const int32_t* tok, int B, float* logits, cudaStream_t s,
+                         const DecodeBufs* db = nullptr) {
+  if (!decode_on_skinny(m, B)) return forward(m, tok, B, 1, 0, logits, false, s, true);
+  const DecodeBufs& b = db ? *db : m->dbuf;
   switch (m->sk_nb) {
-    case 32: return forward_decode_nb<32>(m, tok, B, logits, s);
-    case 64: return forward_decode_nb<64>(m, tok, B, logits, s);
-    default: return forward_decode_nb<128>(m, tok, B, logits, s);
+    case 32: return forward_decode_nb<32>(m, b, tok, B, logits, s);
+    case 64: return forward_decode_nb<64>(m, b, tok, B, logits, s);
+    default: return forward_decode_nb<128>(m, b, tok, B, logits, s);
   }
 }
 
@@ -829,8 +938,8 @@ nc_status decode_graph(nc_model* m, const int32_t* tok, int B, float* logits, cu
 }
 
 // Resolve the token and logit buffers to device memory, staging host buffers.
-nc_status run_call(nc_model* m, const int32_t* tokens, int B, int T, int pos0, float* logits,
-                   bool last_only, cudaStream_t s) {
+nc_status run_call(nc_model* m, const int32_t* tokens, int B, int T, int max_p0, float* logits,
+                   bool last_only, cudaStream_t s, bool decode) {
   const int M = B * T;
   const PtrKind tk = ptr_kind(tokens, m->device), lk = ptr_kind(logits, m->device);
   if (tk == PTR_OTHER_DEVICE || lk == PTR_OTHER_DEVICE) return NC_ERR_INVALID_ARG;
@@ -853,8 +962,8 @@ nc_status run_call(nc_model* m, const int32_t* tokens, int B, int T, int pos0, f
     }
     out_dev = m->logit_stage;
   }
-  nc_status st = pos0 > 0 ? decode_graph(m, tok_dev, B, out_dev, s)
-                          : forward(m, tok_dev, B, T, pos0, out_dev, last_only, s);
+  nc_status st = decode ? decode_graph(m, tok_dev, B, out_dev, s)
+                        : forward(m, tok_dev, B, T, max_p0, out_dev, last_only, s);
   if (st != NC_OK) return st;
   if (host_out) NC_TRY(cudaMemcpyAsync(logits, out_dev, out_bytes, cudaMemcpyDeviceToHost, s));
   return NC_OK;
@@ -889,7 +998,7 @@ const char* nc_status_string(nc_status s) {
     case NC_ERR_TOKEN: return "token id out of range";
     case NC_ERR_TIMEOUT: return "device wait timed out";
     case NC_ERR_CUDA: return "CUDA error";
-    case NC_ERR_SCRATCH_LIMIT: return "reserved (not returned by this version)";
+    case NC_ERR_SCRATCH_LIMIT: return "beyond the no-allocation decode scratch (rows, widths or model type)";
   }
   return "unknown status";
 }
@@ -907,7 +1016,8 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   m->wbytes = m->bf16 ? 2 : 4;
   const nc_config& c = m->cfg;
   const int64_t d = c.d_model, hd = c.head_dim, nh = c.n_head, F = c.d_mlp, V = c.vocab;
-  const int64_t NQKV = (nh + 2) * hd, NQ = nh * hd;
+  const int64_t nkv = c.n_kv_head;
+  const int64_t NQKV = (nh + 2 * nkv) * hd, NQ = nh * hd;
   const int64_t layer_params = NQKV * d + d * NQ + F * d + d * F;
   const int64_t n_params = 2 * V * d + c.n_layer * layer_params;
 
@@ -996,7 +1106,7 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   }
 
   // KV cache with sentinel guards
-  m->layer_elems = (int64_t)c.max_batch * c.max_seq * hd;
+  m->layer_elems = (int64_t)c.max_batch * nkv * c.max_seq * hd;
   m->kv_elems = 2 * kGuardElems + c.n_layer * m->layer_elems;
   CREATE_TRY(cudaMalloc(&m->k_alloc, m->kv_elems * m->wbytes));
   CREATE_TRY(cudaMalloc(&m->v_alloc, m->kv_elems * m->wbytes));
@@ -1017,13 +1127,18 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   CREATE_TRY(cudaMalloc(&m->tok_stage, R * 4));
   if (m->bf16) {
     m->vt_S = (c.max_seq + 127) / 128 * 128;
-    CREATE_TRY(cudaMalloc(&m->vt, (int64_t)c.max_batch * 128 * m->vt_S * 2));
-    CREATE_TRY(cudaMemset(m->vt, 0, (int64_t)c.max_batch * 128 * m->vt_S * 2));
+    CREATE_TRY(cudaMalloc(&m->vt, (int64_t)c.max_batch * nkv * 128 * m->vt_S * 2));
+    CREATE_TRY(cudaMemset(m->vt, 0, (int64_t)c.max_batch * nkv * 128 * m->vt_S * 2));
   }
   CREATE_TRY(configure_kernels(m));
   CREATE_TRY(cudaMalloc(&m->err, sizeof(int)));
-  CREATE_TRY(cudaMalloc(&m->d_len, sizeof(int)));
-  CREATE_TRY(cudaMemset(m->d_len, 0, sizeof(int)));
+  CREATE_TRY(cudaMalloc(&m->d_len, (size_t)c.max_batch * sizeof(int)));
+  CREATE_TRY(cudaMalloc(&m->d_pos0, (size_t)c.max_batch * sizeof(int)));
+  CREATE_TRY(cudaMalloc(&m->d_last, (size_t)c.max_batch * sizeof(int)));
+  CREATE_TRY(cudaMemset(m->d_len, 0, (size_t)c.max_batch * sizeof(int)));
+  CREATE_TRY(cudaMemset(m->d_pos0, 0, (size_t)c.max_batch * sizeof(int)));
+  CREATE_TRY(cudaMemset(m->d_last, 0, (size_t)c.max_batch * sizeof(int)));
+  m->lens.assign(c.max_batch, 0);
   if (m->bf16 && d <= SK_MAX_SS * 128) {
     // decode-step skinny GEMMs: batch padded to 32, 64 or 128 columns
     m->sk_nb = c.max_batch <= 32 ? 32 : (c.max_batch <= 64 ? 64 : 128);
@@ -1044,13 +1159,41 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
               make_tmap(&m->tm_q_st, m->q, R, NQ, 32) && make_tmap(&m->tm_u_st, m->u, R, F, 32) &&
               make_tmap(&m->tm_x_st, m->x, R, d, 32, true);
     {
-      const uint64_t dims[3] = {(uint64_t)m->vt_S, 128, (uint64_t)c.max_batch};
+      const uint64_t dims[3] = {(uint64_t)m->vt_S, 128, (uint64_t)(c.max_batch * nkv)};
       const uint64_t strides[2] = {(uint64_t)m->vt_S * 2, (uint64_t)m->vt_S * 256};
       const uint32_t box[3] = {64, 128, 1};
       ok = ok && make_tmap3(&m->tm_vt, m->vt, dims, strides, box);
     }
-    ok = ok && make_tmap(&m->tm_wu128, m->Wu, V, d, 128) && make_tmap(&m->tm_h_nb, m->h, R, d, m->sk_nb) &&
-         make_tmap(&m->tm_att_nb, m->att, R, NQ, m->sk_nb) && make_tmap(&m->tm_u_nb, m->u, R, F, m->sk_nb);
+    ok = ok && make_tmap(&m->tm_wu128, m->Wu, V, d, 128);
+    // the decode step's intermediates in the workspace
+    DecodeBufs& db = m->dbuf;
+    db.x = m->x;
+    db.h = m->h;
+    db.q = m->q;
+    db.att = m->att;
+    db.u = m->u;
+    db.ss = m->ss_part;
+    db.ss_ld = c.max_batch;
+    if (m->sk_nb > 0)
+      ok = ok && make_tmap(&db.tm_h_nb, db.h, R, d, m->sk_nb) && make_tmap(&db.tm_att_nb, db.att, R, NQ, m->sk_nb) &&
+           make_tmap(&db.tm_u_nb, db.u, R, F, m->sk_nb);
+    // ... and in the no-allocation scratch, when the shape fits it
+    if (ok && m->sk_nb > 0 && d <= kNaD && NQ <= kNaNQ && F <= kNaF) {
+      void* base = nullptr;
+      CREATE_TRY(noalloc_scratch(m->device, &base));
+      char* b0 = static_cast<char*>(base);
+      DecodeBufs& na = m->dbuf_na;
+      na.x = reinterpret_cast<float*>(b0 + kNaOffX);
+      na.h = b0 + kNaOffH;
+      na.q = b0 + kNaOffQ;
+      na.att = b0 + kNaOffAtt;
+      na.u = b0 + kNaOffU;
+      na.ss = reinterpret_cast<float*>(b0 + kNaOffSS);
+      na.ss_ld = kNaRows;
+      ok = make_tmap(&na.tm_h_nb, na.h, kNaRows, d, m->sk_nb) && make_tmap(&na.tm_att_nb, na.att, kNaRows, NQ, m->sk_nb) &&
+           make_tmap(&na.tm_u_nb, na.u, kNaRows, F, m->sk_nb);
+      m->noalloc_ok = ok;
+    }
     m->tm_w128.resize(4 * c.n_layer);
     for (int l = 0; ok && l < c.n_layer; ++l)
       ok = make_tmap(&m->tm_w128[4 * l + 0], m->wqkv[l], NQKV, d, 128) &&
@@ -1059,7 +1202,7 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
            make_tmap(&m->tm_w128[4 * l + 3], m->wproj[l], d, F, 128);
     m->tm_kc.resize(c.n_layer);
     for (int l = 0; ok && l < c.n_layer; ++l) {
-      const uint64_t dims[3] = {128, (uint64_t)c.max_seq, (uint64_t)c.max_batch};
+      const uint64_t dims[3] = {128, (uint64_t)c.max_seq, (uint64_t)(c.max_batch * nkv)};
       const uint64_t strides[2] = {256, (uint64_t)c.max_seq * 256};
       const uint32_t box[3] = {64, 128, 1};
       ok = make_tmap3(&m->tm_kc[l], m->kc(l), dims, strides, box);
@@ -1094,19 +1237,54 @@ nc_status nc_kv_reset(nc_model* m, nc_stream_t) {
   if (!m) return NC_ERR_INVALID_ARG;
   m->length = 0;
   m->batch = 0;
+  std::fill(m->lens.begin(), m->lens.end(), 0);
+  return NC_OK;
+}
+
+nc_status nc_prefill_rows(nc_model* m, const int32_t* tokens, int32_t B, int32_t T, const int32_t* row_len,
+                          float* logits, int32_t last_only, nc_stream_t stream) {
+  if (!m || !tokens || !logits) return NC_ERR_INVALID_ARG;
+  if (B < 1 || B > m->cfg.max_batch || T < 1 || T > m->cfg.max_seq) return NC_ERR_INVALID_ARG;
+  const bool fresh = m->length == 0;
+  // a later chunk of the same rows continues the cache
+  if (!fresh && B != m->batch) return NC_ERR_INVALID_ARG;
+  std::vector<int32_t> p0(B), len(B), last(B);
+  int max_p0 = 0;
+  for (int b = 0; b < B; ++b) {
+    const int n = row_len ? row_len[b] : T;
+    if (n < 1 || n > T) return NC_ERR_INVALID_ARG;
+    p0[b] = fresh ? 0 : m->lens[b];
+    // the padded tokens of a shorter row are computed too: every row needs
+    // room for T positions
+    if (T > m->cfg.max_seq - p0[b]) return NC_ERR_CAPACITY;
+    len[b] = p0[b] + n;
+    last[b] = n - 1;
+    max_p0 = std::max(max_p0, (int)p0[b]);
+  }
+  for (int base = 0; base < B; base += ROWSET_MAX) {
+    RowSet rs;
+    rs.base = base;
+    rs.n = std::min(ROWSET_MAX, B - base);
+    for (int i = 0; i < rs.n; ++i) {
+      rs.pos0[i] = p0[base + i];
+      rs.len[i] = len[base + i];
+      rs.last[i] = last[base + i];
+    }
+    set_rows_kernel<<<1, 256, 0, stream>>>(rs, m->d_pos0, m->d_len, m->d_last);
+    m->launches++;
+    NC_TRY(cudaGetLastError());
+  }
+  nc_status st = run_call(m, tokens, B, T, max_p0, logits, last_only != 0, stream, false);
+  if (st != NC_OK) return st;
+  for (int b = 0; b < B; ++b) m->lens[b] = len[b];
+  m->length = *std::max_element(len.begin(), len.end());
+  m->batch = B;
   return NC_OK;
 }
 
 nc_status nc_prefill(nc_model* m, const int32_t* tokens, int32_t B, int32_t T, float* logits,
                      int32_t last_only, nc_stream_t stream) {
-  if (!m || !tokens || !logits) return NC_ERR_INVALID_ARG;
-  if (B < 1 || B > m->cfg.max_batch || T < 1 || T > m->cfg.max_seq) return NC_ERR_INVALID_ARG;
-  if (m->length != 0) return NC_ERR_STATE;
-  nc_status st = run_call(m, tokens, B, T, 0, logits, last_only != 0, stream);
-  if (st != NC_OK) return st;
-  m->length = T;
-  m->batch = B;
-  return NC_OK;
+  return nc_prefill_rows(m, tokens, B, T, nullptr, logits, last_only, stream);
 }
 
 nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, float* logits,
@@ -1114,9 +1292,10 @@ nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, float* l
   if (!m || !tokens || !logits) return NC_ERR_INVALID_ARG;
   if (m->length == 0) return NC_ERR_STATE;
   if (B != m->batch) return NC_ERR_INVALID_ARG;
-  if (m->length >= m->cfg.max_seq) return NC_ERR_CAPACITY;
-  nc_status st = run_call(m, tokens, B, 1, m->length, logits, false, stream);
+  if (m->length >= m->cfg.max_seq) return NC_ERR_CAPACITY;   // the longest row is full
+  nc_status st = run_call(m, tokens, B, 1, 0, logits, false, stream, true);
   if (st != NC_OK) return st;
+  for (int b = 0; b < B; ++b) m->lens[b] += 1;
   m->length += 1;
   return NC_OK;
 }
@@ -1128,15 +1307,60 @@ nc_status nc_decode_step_noalloc(nc_model* m, const int32_t* tokens, int32_t B, 
   if (m->length == 0) return NC_ERR_STATE;
   if (B != m->batch) return NC_ERR_INVALID_ARG;
   if (m->length >= m->cfg.max_seq) return NC_ERR_CAPACITY;
-  if (ptr_kind(tokens, m->device) != PTR_DEVICE || ptr_kind(logits, m->device) != PTR_DEVICE)
-    return NC_ERR_INVALID_ARG;
+  if (!m->noalloc_ok || B > kNaRows || !decode_on_skinny(m, B)) return NC_ERR_SCRATCH_LIMIT;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != m->device) return NC_ERR_INVALID_ARG;
-  // every buffer of the step is model-owned and sized at creation; the eager
-  // launch sequence (no graph instantiation) allocates nothing
-  const nc_status st = forward_decode(m, tokens, B, logits, stream);
+  if (ptr_kind(tokens, m->device) != PTR_DEVICE || ptr_kind(logits, m->device) != PTR_DEVICE)
+    return NC_ERR_INVALID_ARG;
+  // the step's intermediates live in the file-scope scratch (its device
+  // address was looked up when the model was created); the kernels were
+  // loaded and configured then too, and the step is launched kernel by
+  // kernel: nothing here allocates.  Per-kernel profiling events are not
+  // recorded for this call.
+  const bool prof = m->profiling;
+  m->profiling = false;
+  const nc_status st = forward_decode(m, tokens, B, logits, stream, &m->dbuf_na);
+  m->profiling = prof;
   if (st != NC_OK) return st;
+  for (int b = 0; b < B; ++b) m->lens[b] += 1;
   m->length += 1;
+  return NC_OK;
+}
+
+nc_status nc_kv_clone(nc_model* m, int32_t src, int32_t n, nc_stream_t stream) {
+  if (!m) return NC_ERR_INVALID_ARG;
+  if (m->length == 0) return NC_ERR_STATE;
+  if (src < 0 || src >= m->batch || n < 1 || n > m->cfg.max_batch) return NC_ERR_INVALID_ARG;
+  const size_t wb = m->wbytes, hd = (size_t)m->cfg.head_dim;
+  char* k0 = static_cast<char*>(m->k_alloc) + kGuardElems * wb;
+  char* v0 = static_cast<char*>(m->v_alloc) + kGuardElems * wb;
+  const int len = m->lens[src];
+  const int nkv = m->cfg.n_kv_head;
+  kv_clone_kernel<<<dim3(n, m->cfg.n_layer, 2 * nkv), 256, 0, stream>>>(
+      k0, v0, (size_t)m->layer_elems * wb, (size_t)m->cfg.max_seq * hd * wb, nkv, src, (size_t)len * hd * wb,
+      m->d_len, len);
+  m->launches++;
+  NC_TRY(cudaGetLastError());
+  for (int b = 0; b < n; ++b) m->lens[b] = len;
+  m->length = len;
+  m->batch = n;
+  return NC_OK;
+}
+
+nc_status nc_sample(nc_model* m, const float* logits, int32_t B, double temperature, int32_t top_k,
+                    const double* u, int32_t* tokens, nc_stream_t stream) {
+  if (!m || !logits || !tokens || B < 1 || B > m->cfg.max_batch) return NC_ERR_INVALID_ARG;
+  if (!(temperature >= 0.0) || !std::isfinite(temperature)) return NC_ERR_INVALID_ARG;
+  if (temperature > 0.0 && !u) return NC_ERR_INVALID_ARG;
+  const int V = m->cfg.vocab;
+  const int kept = (top_k <= 0 || top_k > V) ? V : top_k;
+  if (temperature > 0.0 && kept > SAMPLE_MAX_KEEP) return NC_ERR_UNSUPPORTED;
+  if (ptr_kind(logits, m->device) != PTR_DEVICE || ptr_kind(tokens, m->device) != PTR_DEVICE ||
+      (temperature > 0.0 && ptr_kind(u, m->device) != PTR_DEVICE))
+    return NC_ERR_INVALID_ARG;
+  sample_kernel<<<B, SAMPLE_THREADS, 0, stream>>>(logits, V, V, temperature, top_k, u, tokens);
+  m->launches++;
+  NC_TRY(cudaGetLastError());
   return NC_OK;
 }
 
@@ -1157,6 +1381,12 @@ nc_status nc_kv_length(const nc_model* m, int32_t* length, int32_t* batch) {
   if (!m) return NC_ERR_INVALID_ARG;
   if (length) *length = m->length;
   if (batch) *batch = m->batch;
+  return NC_OK;
+}
+
+nc_status nc_kv_row_lengths(const nc_model* m, int32_t* lengths) {
+  if (!m || !lengths) return NC_ERR_INVALID_ARG;
+  for (int b = 0; b < m->batch; ++b) lengths[b] = m->lens[b];
   return NC_OK;
 }
 

@@ -34,7 +34,8 @@ class NcConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("n_layer", "d_model", "n_head", "n_kv_head", "head_dim", "d_mlp", "vocab")] + \
                [(n, ctypes.c_float) for n in ("rope_base", "softcap", "rms_eps")] + \
-               [(n, ctypes.c_int32) for n in ("dtype", "max_batch", "max_seq")]
+               [(n, ctypes.c_int32) for n in ("dtype", "max_batch", "max_seq", "window", "reserved")] + \
+               [("window_layers", ctypes.c_uint64)]
 
 
 _lib = None
@@ -63,8 +64,12 @@ def lib() -> ctypes.CDLL:
         "nc_kv_reset": ([P, P], S),
         "nc_prefill": ([P, P, I32, I32, P, I32, P], S),
         "nc_decode_step": ([P, P, I32, P, P], S),
+        "nc_prefill_rows": ([P, P, I32, I32, P, P, I32, P], S),
+        "nc_kv_row_lengths": ([P, P], S),
         "nc_decode_step_noalloc": ([P, P, I32, P, P], S),
         "nc_sync_status": ([P, P], S),
+        "nc_kv_clone": ([P, I32, I32, P], S),
+        "nc_sample": ([P, P, I32, ctypes.c_double, I32, P, P, P], S),
         "nc_kv_length": ([P, ctypes.POINTER(I32), ctypes.POINTER(I32)], S),
         "nc_kv_layout": ([P, ctypes.POINTER(I64), ctypes.POINTER(I64), ctypes.POINTER(I32)], S),
         "nc_kv_read": ([P, P, P, P], S),
@@ -113,11 +118,22 @@ def _ptr(t):
     raise TypeError(type(t))
 
 
+def window_layers(pattern: str, n_layer: int) -> int:
+    """Bit l set where the sliding-window pattern (e.g. "SSSL", repeated over
+    the layers) has an "S" at layer l."""
+    if not pattern:
+        return 0
+    return sum(1 << l for l in range(n_layer) if pattern[l % len(pattern)] == "S")
+
+
 def make_config(shape, max_batch: int, max_seq: int) -> NcConfig:
     """nc_config from a shape object with the nc_inputs.ModelShape fields."""
+    window = int(getattr(shape, "window", 0) or 0)
+    pattern = getattr(shape, "window_pattern", "") or ""
     return NcConfig(shape.n_layer, shape.d_model, shape.n_head, shape.n_kv_head, shape.head_dim,
                     shape.d_mlp, shape.vocab, shape.rope_base, shape.softcap, shape.rms_eps,
-                    NC_BF16 if shape.dtype == "bf16" else NC_F32, max_batch, max_seq)
+                    NC_BF16 if shape.dtype == "bf16" else NC_F32, max_batch, max_seq,
+                    window if pattern else 0, 0, window_layers(pattern, shape.n_layer) if window else 0)
 
 
 class Model:
@@ -171,6 +187,26 @@ class Model:
                                   _stream(stream)), "nc_prefill")
         return out.view(B, self.cfg.vocab) if last_only else out.view(B, T, self.cfg.vocab)
 
+    def prefill_rows(self, tokens, row_len, last_only: bool = False, out=None, stream=None):
+        """nc_prefill_rows: tokens [B, T] with row_len[b] real tokens at the
+        start of row b (host int sequence); each row keeps its own length."""
+        import torch
+        tokens = tokens.to(torch.int32).contiguous()
+        B, T = tokens.shape
+        lens = np.ascontiguousarray(np.asarray(row_len, dtype=np.int32).reshape(B))
+        if out is None:
+            out = self._out(tokens, B if last_only else B * T)
+        _check(self._L.nc_prefill_rows(self._h, _ptr(tokens), B, T, _ptr(lens), _ptr(out), int(last_only),
+                                       _stream(stream)), "nc_prefill_rows")
+        return out.view(B, self.cfg.vocab) if last_only else out.view(B, T, self.cfg.vocab)
+
+    def row_lengths(self):
+        """Each cached row's length (host list)."""
+        n, b = self.kv_length()
+        out = np.zeros(max(b, 1), dtype=np.int32)
+        _check(self._L.nc_kv_row_lengths(self._h, _ptr(out)), "nc_kv_row_lengths")
+        return out[:b].tolist()
+
     def decode_step(self, tokens, out=None, stream=None):
         import torch
         tokens = tokens.to(torch.int32).contiguous()
@@ -188,6 +224,22 @@ class Model:
         _check(self._L.nc_decode_step_noalloc(self._h, _ptr(tokens), B, _ptr(out), _stream(stream)),
                "nc_decode_step_noalloc")
         return out.view(B, self.cfg.vocab)
+
+    def kv_clone(self, src: int, n: int, stream=None):
+        """nc_kv_clone: rows [0, n) of the cache become copies of row src."""
+        _check(self._L.nc_kv_clone(self._h, int(src), int(n), _stream(stream)), "nc_kv_clone")
+
+    def sample(self, logits, temperature: float = 0.0, top_k: int = 0, u=None, out=None, stream=None):
+        """nc_sample: next tokens [B] int32 (device) from device logits [B, V]
+        fp32; u: device fp64 draws [B] (needed when temperature > 0)."""
+        import torch
+        B = logits.shape[0]
+        if out is None:
+            out = torch.empty(B, dtype=torch.int32, device=logits.device)
+        up = _ptr(u) if u is not None else ctypes.c_void_p()
+        _check(self._L.nc_sample(self._h, _ptr(logits), B, float(temperature), int(top_k), up, _ptr(out),
+                                 _stream(stream)), "nc_sample")
+        return out
 
     def kv_reset(self, stream=None):
         _check(self._L.nc_kv_reset(self._h, _stream(stream)), "nc_kv_reset")

@@ -55,7 +55,7 @@ typedef enum {
   NC_ERR_TOKEN = 6,       /* (device) a token id outside [0, vocab) was seen */
   NC_ERR_TIMEOUT = 7,     /* (device) a bounded pipeline wait expired */
   NC_ERR_CUDA = 8,        /* a CUDA runtime error */
-  NC_ERR_SCRATCH_LIMIT = 9 /* reserved: earlier versions of nc_decode_step_noalloc returned it */
+  NC_ERR_SCRATCH_LIMIT = 9 /* nc_decode_step_noalloc: the batch or the model is beyond its fixed scratch */
 } nc_status;
 
 typedef enum { NC_F32 = 0, NC_BF16 = 1 } nc_dtype;
@@ -65,14 +65,21 @@ typedef enum { NC_F32 = 0, NC_BF16 = 1 } nc_dtype;
  * 1280, 10 heads of dim 128 (szyisi.cn, "pre-training"); d12/d24 follow the
  * same depth rule (d_model = 64 * depth, heads of 128, MLP = 4 * d_model);
  * vocab 65536 = 2**16 (szyisi.cn, tokenizer section).
- *   n_kv_head must be 1 (multi-query attention).
+ *   n_kv_head: K/V heads, dividing n_head; query head h reads K/V head
+ *            h / (n_head / n_kv_head).  1 is multi-query attention (yelogs.com
+ *            architecture answer); more is grouped-query attention
+ *            (apidog.com/th "how nanochat works" item 1).
+ *   window / window_layers: sliding-window attention (apidog.com/th item 1,
+ *            a pattern such as "SSSL" of short and long windows): a layer
+ *            whose bit is set lets a query at position p see only the keys
+ *            p - window + 1 .. p.
  *   NC_BF16: weights, activations and the KV cache in bf16 with fp32
  *            accumulation and an fp32 residual stream; needs head_dim == 128,
  *            d_model, d_mlp and n_head*head_dim multiples of 256, vocab a
  *            multiple of 256.
  *   NC_F32:  everything fp32 (SIMT kernels); head_dim 64 or 128.
  *   rms_eps sits inside the square root: x / sqrt(mean(x^2) + eps).
- *   max_batch / max_seq size the KV cache [n_layer][max_batch][max_seq][head_dim]
+ *   max_batch / max_seq size the KV cache [n_layer][max_batch][n_kv_head][max_seq][head_dim]
  *   (K and V each) and the activation workspace (max_batch * max_seq rows).
  */
 typedef struct {
@@ -80,6 +87,9 @@ typedef struct {
   float rope_base, softcap, rms_eps;
   int32_t dtype; /* nc_dtype */
   int32_t max_batch, max_seq;
+  int32_t window;          /* sliding window in positions; 0 = every layer sees its whole causal context */
+  int32_t reserved;        /* 0 */
+  uint64_t window_layers;  /* bit l set: layer l uses the sliding window (n_layer <= 64 when window > 0) */
 } nc_config;
 
 typedef struct nc_model nc_model;
@@ -101,52 +111,143 @@ NC_API nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_
 /* Free everything the model owns.  NULL is ignored.  Synchronizes the device. */
 NC_API void nc_model_destroy(nc_model* m);
 
-/* Empty the KV cache (length := 0).  Cache contents are left as they are. */
+/*
+ * Empty the KV cache (length := 0, no prefill batch), so that the next call
+ * must be a prefill.  The inference engine's KV cache is filled by the prefill
+ * and extended by each decode step (szyisi.cn "$100 ... ChatGPT clone",
+ * inference engine paragraph; apidog.com/th "how nanochat works" item 6);
+ * this call starts a new sequence.  Host-side bookkeeping only: `stream` is
+ * not used, nothing is enqueued, and the cache contents and the device copy
+ * of the length are left as they are (the next prefill's embedding kernel
+ * rewrites the device length before any kernel reads it).
+ */
 NC_API nc_status nc_kv_reset(nc_model* m, nc_stream_t stream);
 
 /*
- * Prefill: run the full forward pass over tokens[B][T] from an empty cache,
- * write K/V for positions [0, T) of rows [0, B), set the cache length to T.
+ * Prefill (szyisi.cn inference engine paragraph: the prompt is processed in
+ * one pass that fills the KV cache; apidog.com/th "how nanochat works" item 6;
+ * yelogs.com architecture answer for the forward pass itself): the full
+ * forward pass over tokens[B][T] at positions p0 .. p0 + T - 1, where p0 is
+ * the cache length before the call.
+ *  - On an empty cache (p0 = 0) it starts B new sequences.
+ *  - On a non-empty cache it is the next chunk of the same B rows (chunked
+ *    prefill): each chunk attends to every cached position and to its own
+ *    earlier positions, so prefilling a prompt in chunks gives the logits of
+ *    prefilling it at once.  Decode steps may come between chunks.
+ * K/V of the T positions are written to rows [0, B) of the cache and the
+ * cache length becomes p0 + T.
  *   tokens:    int32 [B][T], ids in [0, vocab).
- *   logits:    fp32 [B][T][vocab], or [B][vocab] (position T-1) if last_only.
- * Errors: NC_ERR_STATE if the cache is not empty; NC_ERR_INVALID_ARG if B is
- * outside [1, max_batch] or T outside [1, max_seq].
+ *   logits:    fp32 [B][T][vocab], or [B][vocab] (position p0 + T - 1) if last_only.
+ * Errors: NC_ERR_INVALID_ARG if B is outside [1, max_batch], T outside
+ * [1, max_seq], or (non-empty cache) B differs from the cached batch;
+ * NC_ERR_CAPACITY if p0 + T > max_seq.
  */
 NC_API nc_status nc_prefill(nc_model* m, const int32_t* tokens, int32_t B, int32_t T, float* logits,
                      int32_t last_only, nc_stream_t stream);
 
 /*
- * Decode step: one new token per row at position p = current length, attending
- * to cached positions 0..p; appends K/V at p; length := p + 1.
+ * Prefill with a length per row: as nc_prefill, but row b holds row_len[b]
+ * tokens (1 <= row_len[b] <= T) at the start of its T-token slot, the rest of
+ * the slot being padding.  Each row has its own cache length: row b's tokens
+ * sit at positions p_b .. p_b + row_len[b] - 1, p_b being its length before
+ * the call, and its length becomes p_b + row_len[b].  A batch of prompts of
+ * different lengths is prefilled in one call this way, and decode steps then
+ * append each row's token at its own position.  (The engine serves a batch of
+ * sequences from one KV cache: apidog.com/th "how nanochat works" item 6.)
+ *   row_len: int32 [B] in host memory; NULL means T for every row.
+ *   logits:  fp32 [B][T][vocab] (the padding positions hold unspecified
+ *            values), or [B][vocab] at each row's last token if last_only.
+ * The padding tokens are computed and their K/V written past the row's
+ * length (a later call overwrites them), so every row needs room for T
+ * positions: NC_ERR_CAPACITY if p_b + T > max_seq for some row.  Other errors
+ * as nc_prefill; NC_ERR_INVALID_ARG for a row_len outside [1, T].
+ */
+NC_API nc_status nc_prefill_rows(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
+                                 const int32_t* row_len, float* logits, int32_t last_only, nc_stream_t stream);
+
+/*
+ * Decode step (szyisi.cn inference engine paragraph and geoz.com.cn
+ * "development tricks": each new token attends to the cached keys and values
+ * instead of recomputing the prefix): one new token per row at position
+ * p = the row's current length, attending to its cached positions 0..p;
+ * appends K/V at p; the row's length := p + 1.
  *   tokens: int32 [B]; logits: fp32 [B][vocab].
  * Errors: NC_ERR_STATE before any prefill; NC_ERR_INVALID_ARG if B differs from
- * the prefill's B; NC_ERR_CAPACITY if length == max_seq.
+ * the prefill's B; NC_ERR_CAPACITY if the longest row's length == max_seq.
  */
 NC_API nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, float* logits,
                          nc_stream_t stream);
 
 /*
  * Decode step that allocates nothing.  The pages have no counterpart to this
- * call; it exists for callers that must not allocate device memory while they
- * decode: for example a serving loop that has handed all free device memory to
- * other models' KV caches, or a host framework that owns the device allocator
- * and forbids allocations outside it.  nc_decode_step itself may allocate (it
- * grows a staging buffer the first time it is given host logits); this call
- * never calls cudaMalloc, cudaFree or any allocating routine.
+ * call.  It is for callers that cannot allocate device memory while they
+ * decode: a serving loop that has handed every free byte to other models'
+ * KV caches, a host framework that owns the device allocator and forbids
+ * allocations outside it, or code running where an allocation would
+ * synchronise the device.  nc_decode_step may allocate: it grows a staging
+ * buffer the first time it is given host logits, and it instantiates a CUDA
+ * graph of the step.  This call never calls cudaMalloc, cudaFree or any other
+ * allocating routine.
  *
- * Same arguments, state rules and results as nc_decode_step, except that
- * tokens and logits must be device pointers (host buffers would need staging
- * memory): otherwise NC_ERR_INVALID_ARG.  Every intermediate of the step lives
- * in buffers the model allocated at creation (the split-context attention
- * merges its partial results in on-chip shared memory), and the step is
- * launched kernel by kernel rather than through a CUDA graph (whose
- * instantiation would allocate).  Calls on different models do not share any
- * memory.
- * Only bf16 models (NC_ERR_UNSUPPORTED otherwise); the current device must be
- * the model's device (NC_ERR_INVALID_ARG otherwise).
+ * Same arguments, state rules and results as nc_decode_step, except:
+ *  - tokens and logits must be device pointers on the model's device (host
+ *    buffers would need staging memory), and the current device must be the
+ *    model's device: otherwise NC_ERR_INVALID_ARG;
+ *  - the step's intermediates (residual, activations, queries, attention
+ *    output, MLP hidden, norm partial sums) live in one fixed scratch array in
+ *    device memory, a static part of the library of 4.5 MiB that every GPU
+ *    loading the library holds until the process exits.  It serves at most
+ *    128 rows of a bf16 model with d_model <= 2048, n_head * 128 <= 2048 and
+ *    d_mlp <= 8192; anything larger (or an fp32 model) returns
+ *    NC_ERR_SCRATCH_LIMIT with nothing enqueued;
+ *  - the scratch's device address is looked up when the first model is
+ *    created on a device, and every kernel the step uses is loaded and
+ *    configured at model creation, so the call itself does no set-up;
+ *  - the step is launched kernel by kernel, not through a CUDA graph.
+ * Every call of every model on a device shares the one scratch array, which
+ * keeps the last call's contents.  No value in it has to start at zero: each
+ * value a step reads was written earlier in the same step, and rows past the
+ * batch only feed results that are discarded.  Calls that can overlap on the
+ * GPU (on different streams, or on different models) race on the scratch:
+ * order them, for example by issuing them on one stream.
  */
 NC_API nc_status nc_decode_step_noalloc(nc_model* m, const int32_t* tokens, int32_t B,
                                         float* logits, nc_stream_t stream);
+
+/*
+ * Batch generation (apidog.com/th "how nanochat works" item 6: the engine
+ * clones the KV cache to sample several continuations of one prompt in
+ * parallel): rows [0, n) of the cache become copies of row `src` for every
+ * position it holds, every row's length becomes src's, and the batch
+ * becomes n.  Typical use: prefill a prompt
+ * with B = 1, clone it to n rows, then decode the n rows with different
+ * sampled tokens.  Asynchronous on `stream`.
+ * Errors: NC_ERR_STATE on an empty cache; NC_ERR_INVALID_ARG if src is not a
+ * cached row or n is outside [1, max_batch].
+ */
+NC_API nc_status nc_kv_clone(nc_model* m, int32_t src, int32_t n, nc_stream_t stream);
+
+/*
+ * Next tokens from logits on the device (apidog.com/th item 6 and szyisi.cn
+ * inference engine paragraph name sampling but give no rule; this is the
+ * plainest reading):
+ *  - temperature == 0: the argmax of each row, the lowest index among equal
+ *    maxima (u and top_k are not used; u may be NULL);
+ *  - temperature > 0: the candidates in the order (logit descending, index
+ *    ascending), the first top_k of them (top_k <= 0 keeps all), weights
+ *    w_i = exp((l_i - l_0) / temperature) in fp64, cumulative sums
+ *    C_j = w_0 + ... + w_j in that order, and the first candidate with
+ *    C_j > u[b] * C_last.
+ *   logits: fp32 [B][vocab] (device); u: fp64 [B] draws in [0, 1) (device);
+ *   tokens: int32 [B] (device), written on `stream`; they may be passed
+ *           straight to the next nc_decode_step.
+ * At most 1024 candidates are kept with temperature > 0 (top_k <= 1024, or
+ * vocab <= 1024): otherwise NC_ERR_UNSUPPORTED.  NC_ERR_INVALID_ARG for null
+ * or host pointers, B outside [1, max_batch], a negative or non-finite
+ * temperature.
+ */
+NC_API nc_status nc_sample(nc_model* m, const float* logits, int32_t B, double temperature, int32_t top_k,
+                           const double* u, int32_t* tokens, nc_stream_t stream);
 
 /*
  * Synchronize `stream`, then report (and clear) the device error word:
@@ -154,13 +255,19 @@ NC_API nc_status nc_decode_step_noalloc(nc_model* m, const int32_t* tokens, int3
  */
 NC_API nc_status nc_sync_status(nc_model* m, nc_stream_t stream);
 
-/* Current cache length and the prefill batch (0 before the first prefill). */
+/*
+ * The cache length (the longest row's, when rows differ) and the batch
+ * (0 before the first prefill).
+ */
 NC_API nc_status nc_kv_length(const nc_model* m, int32_t* length, int32_t* batch);
+
+/* Each cached row's length: lengths[b] for b < batch (host memory). */
+NC_API nc_status nc_kv_row_lengths(const nc_model* m, int32_t* lengths);
 
 /*
  * Test hook: copy the whole K and V caches, guard regions included, into
  * k_dst / v_dst (device or host), each `nc_kv_bytes` bytes.  Layout of each:
- * [guard][n_layer][max_batch][max_seq][head_dim][guard], elements of
+ * [guard][n_layer][max_batch][n_kv_head][max_seq][head_dim][guard], elements of
  * `elem_bytes` (2 for NC_BF16, 4 for NC_F32); guards are `guard_elems`
  * elements.  At creation the whole buffer holds the sentinel byte 0xFF; a
  * position is written only when prefill or decode computes it.

@@ -4,6 +4,8 @@ of rows, and the acceptance tolerances.
 Tolerances (logits): bf16 models max |dlogit| <= 3e-2 and mean |dlogit| <= 5e-3;
 fp32 model max |dlogit| <= 1e-4.
 """
+import re
+
 import numpy as np
 import torch
 
@@ -18,14 +20,34 @@ def small_bf16_shape(n_layer=2, vocab=4096):
     return nc_inputs.D12.with_(name="d12_small", n_layer=n_layer, vocab=vocab)
 
 
-def check_close(got, want, dtype, what=""):
+# worst margins per check group, printed at the end of the session (conftest)
+MARGINS = {}
+
+
+def _record(group, mx, mean, tmax, tmean):
+    old = MARGINS.get(group)
+    if old is None:
+        MARGINS[group] = (mx, mean, tmax, tmean, 1)
+    else:
+        MARGINS[group] = (max(old[0], mx), max(old[1], mean), tmax, tmean, old[4] + 1)
+
+
+def check_close(got, want, dtype, what="", group=None, tol=None):
+    """max and mean |got - want| within the tolerance of `dtype` (or `tol`);
+    the margins are recorded under `group` (default: `what` without a
+    trailing step number) for the end-of-session summary."""
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite GPU values"
     err = np.abs(got - want)
     mx, mean = float(err.max()), float(err.mean())
-    tmax, tmean = TOL[dtype]
+    tmax, tmean = tol if tol is not None else TOL[dtype]
+    if group is None:
+        group = re.sub(r"\s*\d+$", "", what) or what      # "d12 decode step 5" -> "d12 decode step"
+        if tol is None:
+            group += f" [{dtype}]"
+    _record(group, mx, mean, tmax, tmean)
     assert mx <= tmax and mean <= tmean, f"{what}: max {mx:.3e} (tol {tmax}), mean {mean:.3e} (tol {tmean})"
     return mx, mean
 

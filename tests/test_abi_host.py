@@ -48,7 +48,8 @@ def _create(L, cfg, weights_ptr=ctypes.c_void_p(1)):
 @pytest.mark.parametrize("field,value,want", [
     ("n_layer", 0, 1), ("d_model", 0, 1), ("n_head", 0, 1), ("vocab", 0, 1),
     ("max_batch", 0, 1), ("max_seq", 0, 1), ("dtype", 7, 1), ("softcap", 0.0, 1),
-    ("rope_base", -1.0, 1), ("n_kv_head", 2, 2), ("head_dim", 96, 2),
+    ("rope_base", -1.0, 1), ("n_kv_head", 3, 1), ("n_kv_head", 0, 1), ("window", -1, 1),
+    ("head_dim", 96, 2),
 ])
 def test_create_rejects_bad_config_without_gpu(L, field, value, want):
     st, h = _create(L, _cfg(**{field: value}))

@@ -230,9 +230,9 @@ def test_state_and_capacity_errors():
         m.decode_step(tok[:, 0])
     assert e.value.name == "NC_ERR_STATE"
     m.prefill(tok)
-    with pytest.raises(ncp.NcError) as e:
+    with pytest.raises(ncp.NcError) as e:           # a second chunk of 8 would pass max_seq
         m.prefill(tok)
-    assert e.value.name == "NC_ERR_STATE"
+    assert e.value.name == "NC_ERR_CAPACITY"
     with pytest.raises(ncp.NcError) as e:
         m.decode_step(tok[:1, 0])
     assert e.value.name == "NC_ERR_INVALID_ARG"
