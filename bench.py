@@ -63,7 +63,7 @@ def prefill_flops(s, B, T, last_only=False):
     M = B * T
     d, hd, nh, F, V, L = s.d_model, s.head_dim, s.n_head, s.d_mlp, s.vocab, s.n_layer
     return {
-        "qkv": 2.0 * M * d * (nh + 2) * hd * L,
+        "qkv": 2.0 * M * d * (nh + 2 * s.n_kv_head) * hd * L,
         "attn": 4.0 * nh * hd * (T * (T + 1) / 2) * B * L,
         "oproj": 2.0 * M * nh * hd * d * L,
         "fc": 2.0 * M * d * F * L,
@@ -75,18 +75,20 @@ def prefill_flops(s, B, T, last_only=False):
 def decode_bytes_by_class(s, B, ctx):
     """Algorithmic HBM bytes of one decode step at context length ctx (keys
     0..ctx-1 read, one new K/V row written), split by the kernel class that
-    moves them: bf16 weights once (QKV, O, FC, PROJ, unembedding), the K/V
-    read (attention), the new K/V row (QKV), the embedding rows and the fp32
-    logits."""
+    moves them: the projection weights once (QKV, O, FC, PROJ, unembedding;
+    2 bytes each, 1 with FP8 weights), the K/V read (attention), the new K/V
+    rows (QKV), the embedding rows and the fp32 logits."""
     d, hd, nh, F, V, L = s.d_model, s.head_dim, s.n_head, s.d_mlp, s.vocab, s.n_layer
+    nkv = s.n_kv_head
+    wb = 1.0 if s.dtype == "fp8" else 2.0
     return {
         "embed": B * d * 2.0,
-        "qkv": 2.0 * L * (nh + 2) * hd * d + L * B * 2 * hd * 2.0,
-        "attn": L * B * 2.0 * ctx * hd * 2,
-        "oproj": 2.0 * L * d * nh * hd,
-        "fc": 2.0 * L * F * d,
-        "proj": 2.0 * L * d * F,
-        "lm_head": 2.0 * V * d + B * V * 4.0,
+        "qkv": wb * L * (nh + 2 * nkv) * hd * d + L * B * nkv * 2 * hd * 2.0,
+        "attn": L * B * nkv * 2.0 * ctx * hd * 2,
+        "oproj": wb * L * d * nh * hd,
+        "fc": wb * L * F * d,
+        "proj": wb * L * d * F,
+        "lm_head": wb * V * d + B * V * 4.0,
     }
 
 
@@ -95,8 +97,11 @@ def decode_bytes(s, B, ctx):
     return sum(decode_bytes_by_class(s, B, ctx).values())
 
 
-def weight_bytes(s, elem=2):
-    return elem * nc_inputs.param_count(s)
+def weight_bytes(s):
+    """Bytes of the weights a decode step streams (bf16; FP8 projections)."""
+    if s.dtype == "fp8":
+        return 2 * s.vocab * s.d_model + (nc_inputs.param_count(s) - s.vocab * s.d_model)
+    return 2 * nc_inputs.param_count(s)
 
 
 # --------------------------------------------------------------------------- #
@@ -717,6 +722,14 @@ def main():
         extra["decode"] = {k: e[k] for k in ("workload", "value", "ms_per_step", "step_gbs",
                                              "step_frac_of_hbm", "roofline", "e2e")}
         line["d12"] = extra
+        if w.shape.name == "d24":
+            # the same decode workload with FP8 projection weights
+            w8 = nc_inputs.WORKLOADS["d24_decode_fp8"]
+            f8 = nc_inputs.gen_weights(w8.shape, w8.weight_seed)
+            p8, n8 = _tokens(w8)
+            _, e = decode_leg(args, world, local, w8, f8, p8, n8, peaks, peak_src)
+            line["decode_fp8"] = {k: e[k] for k in ("workload", "value", "ms_per_step", "step_gbs",
+                                                    "step_frac_of_hbm", "roofline", "kernels", "e2e")}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         pre, dec = oracle_baselines(w, wd, flat, prompt if w.decode_steps == 0 else pd, nd)

@@ -80,9 +80,11 @@ constexpr uint32_t DEC_STAGE_BYTES = 2 * DEC_SUB * 256;   // K and V rows of a s
 static_assert(DEC_KPW == 16, "the score tile loop assumes 16 keys per warp");
 static_assert(DEC_CHUNK % DEC_SUB == 0 || DEC_SUB % DEC_CHUNK == 0, "partial buffers sized by DEC_CHUNK");
 
+// TO: the output type (bf16, or f16 when the next projection's activations are f16)
+template <typename TO>
 __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ Kc,
-    const __nv_bfloat16* __restrict__ Vc, __nv_bfloat16* __restrict__ O, int n_head, int cache_S, int ctx_arg,
+    const __nv_bfloat16* __restrict__ Vc, TO* __restrict__ O, int n_head, int cache_S, int ctx_arg,
     const int* __restrict__ pos_dev, float scale_log2, int group, int n_kv, int window) {
   pdl_trigger();
   const int grp = blockIdx.x, bs = blockIdx.y;                 // K/V sequence bs = b * n_kv + g
@@ -294,7 +296,7 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
       float acc = 0.f;
 #pragma unroll
       for (int w = 0; w < DEC_WARPS; ++w) acc += ored[(w * 16 + r) * 128 + ocol];
-      O[((size_t)b * n_head + h0 + r) * ATT_HD + ocol] = f2bf(acc * inv_l1[r]);
+      O[((size_t)b * n_head + h0 + r) * ATT_HD + ocol] = from_f<TO>(acc * inv_l1[r]);
     }
     return;
   }
@@ -337,7 +339,7 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_mma_kernel(
       l += lg[g] * f;
       acc += og[g] * f;
     }
-    O[((size_t)b * n_head + h0 + r) * ATT_HD + ocol] = f2bf(acc * (1.f / l));
+    O[((size_t)b * n_head + h0 + r) * ATT_HD + ocol] = from_f<TO>(acc * (1.f / l));
   }
   cluster_sync_all();                                          // remote reads done before any CTA exits
 }

@@ -29,9 +29,19 @@
 // epilogue.  Every mbarrier wait is bounded.  Launched as a programmatic
 // dependent of the previous kernel, the CTA streams its first weight blocks
 // into shared memory before it waits for that kernel's results.
+//
+// FP8 weights (FP8 = true; the FP8 training path of apidog.com/th "how
+// nanochat works" item 3, here for inference): each weight matrix is stored
+// as FP8 E4M3 values times one power-of-two scale, so a step streams one
+// byte per weight instead of two.  The TMA brings 128 x 64 E4M3 tiles (64-byte
+// swizzle); four more warps (256 threads) widen each tile exactly to f16 in a
+// 128-byte-swizzled tile, which the tensor core reads as the A operand of a
+// kind::f16 MMA with f16 activations; the scale multiplies the accumulated
+// sums in the epilogue, whose activation outputs are then f16.
 #pragma once
 
 #include <cuda.h>
+#include <type_traits>
 #include "k_gemm_tc.cuh"
 #include "nc_common.cuh"
 
@@ -43,7 +53,9 @@ struct SkinnyArgs {
                                   // (the cluster size along grid y)
   // epilogue outputs
   float* x;                       // EPI_RESID: [B][N] fp32, += ; EPI_LOGITS: [B][N] fp32 out
-  __nv_bfloat16* out_bf;          // EPI_RELU2: [B][N]; EPI_QKV: Q [B][n_head*128]
+  __nv_bfloat16* out_bf;          // EPI_QKV: Q [B][n_head*128]
+  void* out_act;                  // EPI_RELU2: [B][N] activations (bf16, or f16 with FP8 weights)
+  float w_scale;                  // the weight matrix's scale (1 for bf16 weights)
   __nv_bfloat16* k_cache;         // EPI_QKV: this layer's K [B_max][n_kv][S][128]
   __nv_bfloat16* v_cache;
   const float* rope_cos;          // [S][64]
@@ -58,7 +70,7 @@ struct SkinnyArgs {
   // columns to ss_out[tile * ss_ld + b]; a consumer of h (QKV, MLP up, logits)
   // scales row b of its result by r_b = 1 / sqrt(sum_t ss_in[t * ss_ld + b] / K
   // + eps), summed over the n_ss column blocks in order.  Null: no folding.
-  __nv_bfloat16* h_out;
+  void* h_out;                    // activations (bf16, or f16 with FP8 weights)
   float* ss_out;
   const float* ss_in;
   int n_ss, ss_ld;
@@ -68,11 +80,14 @@ struct SkinnyArgs {
 // column blocks of 128 in a folded RMSNorm (d_model <= 2048)
 constexpr int SK_MAX_SS = 16;
 
-template <int NB>
+template <int NB, bool FP8 = false>
 struct SkCfg {
-  static constexpr uint32_t W_BYTES = 128 * 64 * 2;      // 16 KB
+  static constexpr int THREADS = FP8 ? 256 : 128;         // FP8: four converter warps more
+  static constexpr uint32_t W_BYTES = 128 * 64 * 2;      // 16 KB: the MMA's 16-bit weight tile
+  static constexpr uint32_t W8_BYTES = FP8 ? 128 * 64 : 0;   // 8 KB: the E4M3 tile the TMA brings
   static constexpr uint32_t A_BYTES = NB * 64 * 2;
-  static constexpr uint32_t STAGE_BYTES = W_BYTES + A_BYTES;
+  static constexpr uint32_t STAGE_BYTES = W_BYTES + A_BYTES + W8_BYTES;
+  static constexpr uint32_t TMA_BYTES = (FP8 ? W8_BYTES : W_BYTES) + A_BYTES;   // per stage
   static constexpr int STAGES = (int)(98304 / STAGE_BYTES) < 2 ? 2 : (int)(98304 / STAGE_BYTES);
   static constexpr uint32_t TMEM_COLS = NB < 32 ? 32 : NB;
   // + barriers and flags (256 B), row scales [NB], slack
@@ -96,7 +111,7 @@ __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t local_addr, uint32_t rank
 // contiguous bytes.  RPB rows per warp are in flight at once (RPB x S reads,
 // plus the residual for EPI_RESID), which makes the reduction one or two
 // round trips instead of one per row.
-template <int S, int EPI>
+template <int S, int EPI, typename TA>
 __device__ __forceinline__ void sk_reduce_epilogue(const SkinnyArgs& args, uint32_t psm, const float* r_s,
                                                    int rank, int warp, int lane, int tile, float inv_cap) {
   constexpr int RPB = 16 / S > 8 ? 8 : 16 / S;
@@ -130,6 +145,8 @@ __device__ __forceinline__ void sk_reduce_epilogue(const SkinnyArgs& args, uint3
         v[2] += part[i][q].z;
         v[3] += part[i][q].w;
       }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] *= args.w_scale;    // 1 for bf16 weights (exact)
       if constexpr (EPI != EPI_RESID) {
         const float rb = r_s[b];                     // folded RMSNorm of the input row
 #pragma unroll
@@ -170,9 +187,9 @@ __device__ __forceinline__ void sk_reduce_epilogue(const SkinnyArgs& args, uint3
           *reinterpret_cast<float4*>(args.x + o) = xn;
           if (args.h_out) {
             uint2 pk;
-            pk.x = pack_bf16(xn.x, xn.y);
-            pk.y = pack_bf16(xn.z, xn.w);
-            *reinterpret_cast<uint2*>(args.h_out + o) = pk;
+            pk.x = pack2<TA>(xn.x, xn.y);
+            pk.y = pack2<TA>(xn.z, xn.w);
+            *reinterpret_cast<uint2*>(static_cast<TA*>(args.h_out) + o) = pk;
             const float ss = warp_sum(xn.x * xn.x + xn.y * xn.y + xn.z * xn.z + xn.w * xn.w);
             if (lane == 0) args.ss_out[(size_t)tile * args.ss_ld + b] = ss;
           }
@@ -184,9 +201,9 @@ __device__ __forceinline__ void sk_reduce_epilogue(const SkinnyArgs& args, uint3
             r[k] = t * t;
           }
           uint2 pk;
-          pk.x = pack_bf16(r[0], r[1]);
-          pk.y = pack_bf16(r[2], r[3]);
-          *reinterpret_cast<uint2*>(args.out_bf + o) = pk;
+          pk.x = pack2<TA>(r[0], r[1]);
+          pk.y = pack2<TA>(r[2], r[3]);
+          *reinterpret_cast<uint2*>(static_cast<TA*>(args.out_act) + o) = pk;
         } else {
           *reinterpret_cast<float4*>(args.x + o) =
               make_float4(softcap_f(v[0], inv_cap, args.softcap), softcap_f(v[1], inv_cap, args.softcap),
@@ -197,23 +214,44 @@ __device__ __forceinline__ void sk_reduce_epilogue(const SkinnyArgs& args, uint3
   }
 }
 
-template <int NB, int EPI>
-__global__ void __launch_bounds__(128)
+// 16 E4M3 values (one 16-byte chunk) -> 16 f16 values, exactly (every E4M3
+// value is an f16 value)
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4 v, uint32_t (&h)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFFu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
+    h[2 * i] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+    h[2 * i + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+  }
+}
+__device__ __forceinline__ uint4 ld_shared_v4u(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
+template <int NB, int EPI, bool FP8>
+__global__ void __launch_bounds__(SkCfg<NB, FP8>::THREADS)
     gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                        const SkinnyArgs args) {
-  using C = SkCfg<NB>;
+  using C = SkCfg<NB, FP8>;
+  using TA = typename std::conditional<FP8, __half, __nv_bfloat16>::type;   // activation type
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t sk_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sk_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sW = smem;
-  uint8_t* sA = smem + STAGES * C::W_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + STAGES * C::A_BYTES);
-  // bars: full[STAGES], empty[STAGES], done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  uint8_t* sW = smem;                                // MMA weight tiles (16-bit)
+  uint8_t* sA = smem + STAGES * C::W_BYTES;          // activation tiles
+  uint8_t* sW8 = sA + STAGES * C::A_BYTES;           // FP8: E4M3 tiles from the TMA
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sW8 + STAGES * C::W8_BYTES);
+  // bars: full[STAGES], empty[STAGES], converted[STAGES], done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);   // [0] abort
   float* r_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);   // [NB] row scales
   auto bar = [&](int i) { return smem_u32(bars + i); };
-  const int FULL = 0, EMPTY = STAGES, DONE = 2 * STAGES;
+  const int FULL = 0, EMPTY = STAGES, CONV = 2 * STAGES, DONE = 3 * STAGES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, split = blockIdx.y;
@@ -226,6 +264,7 @@ __global__ void __launch_bounds__(128)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar(FULL + s), 1);
       mbar_init(bar(EMPTY + s), 1);
+      mbar_init(bar(CONV + s), 4);                   // one arrival per converter warp
     }
     mbar_init(bar(DONE), 1);
     flags[0] = 0;
@@ -244,6 +283,8 @@ __global__ void __launch_bounds__(128)
     atomicOr(args.err, NC_DEVFLAG_TIMEOUT);
     flags[0] = 1;
   };
+  // the weight tile of a stage as the TMA writes it
+  auto w_dst = [&](int s) { return smem_u32(FP8 ? sW8 + s * C::W8_BYTES : sW + s * C::W_BYTES); };
 
   pdl_trigger();
   if (warp == 0 && lane == 0) {
@@ -254,8 +295,8 @@ __global__ void __launch_bounds__(128)
     for (int s = 0; s < STAGES; ++s) issued[s] = -1;
     const int pre = nkb < STAGES ? nkb : STAGES;
     for (int kb = 0; kb < pre; ++kb) {
-      mbar_arrive_expect_tx(bar(FULL + kb), C::STAGE_BYTES);
-      tma_load_2d(smem_u32(sW + kb * C::W_BYTES), &tmW, bar(FULL + kb), (kb0 + kb) * 64, n0);
+      mbar_arrive_expect_tx(bar(FULL + kb), C::TMA_BYTES);
+      tma_load_2d(w_dst(kb), &tmW, bar(FULL + kb), (kb0 + kb) * 64, n0);
       issued[kb] = 0;
     }
     pdl_wait();
@@ -269,8 +310,8 @@ __global__ void __launch_bounds__(128)
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(bar(FULL + stage), C::STAGE_BYTES);
-      tma_load_2d(smem_u32(sW + stage * C::W_BYTES), &tmW, bar(FULL + stage), (kb0 + kb) * 64, n0);
+      mbar_arrive_expect_tx(bar(FULL + stage), C::TMA_BYTES);
+      tma_load_2d(w_dst(stage), &tmW, bar(FULL + stage), (kb0 + kb) * 64, n0);
       tma_load_2d(smem_u32(sA + stage * C::A_BYTES), &tmA, bar(FULL + stage), (kb0 + kb) * 64, 0);
       issued[stage] = (int)phase;
       if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -280,11 +321,14 @@ __global__ void __launch_bounds__(128)
         if (issued[s] >= 0) mbar_wait(bar(FULL + s), (uint32_t)issued[s], limit);
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(128, NB);
+    constexpr uint32_t idesc = FP8 ? idesc_f16_f32(128, NB) : idesc_bf16_f32(128, NB);
     uint32_t stage = 0, phase = 0;
     bool any = false;
     for (int kb = 0; kb < nkb; ++kb) {
-      if (flags[0] || !mbar_wait(bar(FULL + stage), phase, limit)) {
+      // FP8: the converter warps have widened the stage's weights (they
+      // waited for its copies first)
+      if (flags[0] || !mbar_wait(bar(FULL + stage), phase, limit) ||
+          (FP8 && !mbar_wait(bar(CONV + stage), phase, limit))) {
         if (!flags[0]) fail();
         break;
       }
@@ -301,6 +345,32 @@ __global__ void __launch_bounds__(128)
     // completion of every issued MMA (also the drain on the abort path)
     if (any) tc_commit(bar(DONE));
     else mbar_arrive(bar(DONE));
+  } else if (FP8 && warp >= 4) {
+    // ------------------------------------------------------- FP8 converters
+    // thread = weight row r: its 64 E4M3 bytes (64-byte swizzle: chunk c at
+    // c ^ ((r >> 1) & 3)) become 64 f16 (128-byte swizzle: chunk c at c ^ (r & 7))
+    const int r = 32 * (warp - 4) + lane;
+    uint32_t stage = 0, phase = 0;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const bool ok = !flags[0] && mbar_wait(bar(FULL + stage), phase, limit);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (!flags[0]) fail();
+        break;
+      }
+      const uint32_t w8 = smem_u32(sW8 + stage * C::W8_BYTES) + r * 64;
+      const uint32_t w16 = smem_u32(sW + stage * C::W_BYTES) + r * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        uint32_t h[8];
+        e4m3x16_to_f16(ld_shared_v4u(w8 + ((c8 ^ ((r >> 1) & 3)) << 4)), h);
+        st_shared_v4u(w16 + (((2 * c8) ^ (r & 7)) << 4), h[0], h[1], h[2], h[3]);
+        st_shared_v4u(w16 + (((2 * c8 + 1) ^ (r & 7)) << 4), h[4], h[5], h[6], h[7]);
+      }
+      fence_async_smem();                            // the tensor core reads what was written
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(CONV + stage));
+      if (++stage == STAGES) { stage = 0; phase ^= 1; }
+    }
   }
   __syncwarp();
 
@@ -327,14 +397,16 @@ __global__ void __launch_bounds__(128)
   const bool done_ok = mbar_wait(bar(DONE), 0, limit);
   if (!done_ok) fail();
   tc_fence_after();
-  const int row = 32 * warp + lane;                  // weight row n0 + row
-  const uint32_t taddr = tmem_base + ((uint32_t)(32 * warp) << 16);
-  // the same decision in every thread: the TMEM loads below are warp-collective
+  const int row = 32 * (warp & 3) + lane;            // weight row n0 + row (warps 0..3)
+  const uint32_t taddr = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16);
+  // the same decision in every thread: the TMEM loads below are warp-collective;
+  // only warps 0..3 (one per TMEM lane quarter) run the epilogue
   const bool run = __syncthreads_and(done_ok) && !flags[0];
+  const bool epi = run && warp < 4;
   const float inv_cap = 1.f / args.softcap;
 
   if (args.splits == 1 && EPI == EPI_LOGITS) {
-    if (run) {
+    if (epi) {
 #pragma unroll 1
       for (int c = 0; c < NB; c += 32) {
         float v[32];
@@ -342,14 +414,15 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (c + j < args.B)
-            args.x[(size_t)(c + j) * args.N + n0 + row] = softcap_f(v[j] * r_s[c + j], inv_cap, args.softcap);
+            args.x[(size_t)(c + j) * args.N + n0 + row] =
+                softcap_f(v[j] * args.w_scale * r_s[c + j], inv_cap, args.softcap);
       }
     }
   } else {
     // this CTA's partial D[n][b] -> own shared memory as P[b][n] (the ring is
     // free: every load has landed and every MMA has read it)
     const uint32_t psm = smem_u32(smem);
-    if (run) {
+    if (epi) {
 #pragma unroll 1
       for (int c = 0; c < NB; c += 32) {
         float v[32];
@@ -360,17 +433,17 @@ __global__ void __launch_bounds__(128)
       }
     }
     cluster_sync_all();                              // every CTA of the tile reaches it once
-    if (run) {
+    if (epi) {
       const int rank = (int)cluster_ctarank();
       switch (args.splits) {
-        case 1: sk_reduce_epilogue<1, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
-        case 2: sk_reduce_epilogue<2, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
-        case 3: sk_reduce_epilogue<3, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
-        case 4: sk_reduce_epilogue<4, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
-        case 5: sk_reduce_epilogue<5, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
-        case 6: sk_reduce_epilogue<6, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
-        case 7: sk_reduce_epilogue<7, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
-        default: sk_reduce_epilogue<8, EPI>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 1: sk_reduce_epilogue<1, EPI, TA>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 2: sk_reduce_epilogue<2, EPI, TA>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 3: sk_reduce_epilogue<3, EPI, TA>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 4: sk_reduce_epilogue<4, EPI, TA>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 5: sk_reduce_epilogue<5, EPI, TA>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 6: sk_reduce_epilogue<6, EPI, TA>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        case 7: sk_reduce_epilogue<7, EPI, TA>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
+        default: sk_reduce_epilogue<8, EPI, TA>(args, psm, r_s, rank, warp, lane, tile, inv_cap); break;
       }
     }
     cluster_sync_all();                              // remote reads done before any CTA exits

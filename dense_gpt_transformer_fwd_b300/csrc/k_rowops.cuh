@@ -221,6 +221,31 @@ __global__ void set_rows_kernel(const RowSet rs, int* __restrict__ pos0, int* __
   }
 }
 
+// max |src[i]| over n values, as the bit pattern of a non-negative float
+// (those order like unsigned integers): atomicMax into *amax (zeroed before)
+__global__ void absmax_kernel(const float* __restrict__ src, size_t n, unsigned int* amax) {
+  float m = 0.f;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    m = fmaxf(m, fabsf(src[i]));
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) atomicMax(amax, __float_as_uint(m));
+}
+
+// FP8 weights (FP8 E4M3 values times one power-of-two scale per matrix):
+// q[i] = e4m3(src[i] / scale) (round to nearest even, saturating at 448), and
+// deq[i] = bf16(e4m3 value * scale), the exact 16-bit image the prefill GEMMs
+// use (an E4M3 value has 3 mantissa bits; times a power of two it is a bf16
+// value).  inv_scale = 1 / scale, both powers of two: the products are exact.
+__global__ void quantize_e4m3_kernel(const float* __restrict__ src, size_t n, float inv_scale, float scale,
+                                     uint8_t* __restrict__ q, __nv_bfloat16* __restrict__ deq) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(src[i] * inv_scale, __NV_SATFINITE, __NV_E4M3);
+    q[i] = c;
+    const __half h(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3));
+    deq[i] = __float2bfloat16_rn(__half2float(h) * scale);
+  }
+}
+
 // fp32 -> bf16 (round to nearest even) weight conversion
 __global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
                                    size_t n) {

@@ -23,6 +23,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <type_traits>
 #include <utility>
 #include <vector>
 
@@ -75,6 +76,21 @@ bool make_tmap(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, u
   CUresult r = g_encode(tm, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         2, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 2-D map over a row-major [rows][cols] byte matrix (FP8 E4M3 weights): box
+// 64 bytes x box_rows, 64-byte swizzle (chunk c of row r at c ^ ((r >> 1) & 3)).
+bool make_tmap8(CUtensorMap* tm, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  if (!load_encode()) return false;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || cols % 16) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -241,6 +257,14 @@ struct nc_model {
   int sk_splits[4] = {1, 1, 1, 1};     // K splits of QKV, O-proj, FC, PROJ
   std::vector<CUtensorMap> tm_w128;    // per layer Wqkv, Wo, Wfc, Wproj, box 64 x 128 rows
   CUtensorMap tm_wu128{};
+  // FP8 models: the projection weights as E4M3 bytes (per layer Wqkv, Wo, Wfc,
+  // Wproj, then Wu), one power-of-two scale per matrix, and their tensor maps
+  // (box 64 bytes x 128 rows, 64-byte swizzle) for the decode GEMMs; the bf16
+  // buffer above holds their exact dequantized image for the prefill
+  bool fp8 = false;
+  void* w8 = nullptr;
+  std::vector<float> w8_scale;
+  std::vector<CUtensorMap> tm_w8;
   DecodeBufs dbuf;                     // the decode step's intermediates in the workspace above
   DecodeBufs dbuf_na;                  // the same in the no-allocation scratch (nc_decode_step_noalloc)
   bool noalloc_ok = false;             // the model's shape fits the no-allocation scratch
@@ -273,10 +297,65 @@ void free_model(nc_model* m) {
   void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->rope_cos_t, m->rope_sin_t, m->d_tm_kv,
                   m->k_alloc, m->v_alloc, m->x,
                   m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
-                  m->tok_stage, m->logit_stage, m->err, m->vt, m->d_len, m->d_pos0, m->d_last, m->ss_part};
+                  m->tok_stage, m->logit_stage, m->err, m->vt, m->d_len, m->d_pos0, m->d_last, m->ss_part,
+                  m->w8};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete m;
+}
+
+// FP8 models: every projection matrix (per layer Wqkv, Wo, Wfc, Wproj, then
+// Wu) of the fp32 weights `src` (device, canonical order) becomes E4M3 bytes
+// in m->w8 with one power-of-two scale per matrix, 2**ceil(log2(amax / 448)),
+// and its exact dequantized image replaces the matrix in the bf16 buffer.
+cudaError_t quantize_fp8_weights(nc_model* m, const float* src) {
+  const nc_config& c = m->cfg;
+  const int64_t d = c.d_model, nh = c.n_head, nkv = c.n_kv_head, F = c.d_mlp, V = c.vocab;
+  const int64_t NQKV = (nh + 2 * nkv) * 128, NQ = nh * 128;
+  std::vector<std::pair<int64_t, int64_t>> mats;         // (element offset, count)
+  int64_t off = V * d;                                    // after E
+  for (int l = 0; l < c.n_layer; ++l)
+    for (int64_t n : {NQKV * d, d * NQ, F * d, d * F}) {
+      mats.push_back({off, n});
+      off += n;
+    }
+  mats.push_back({off, V * d});                           // Wu
+  int64_t total = 0;
+  for (auto& mt : mats) total += mt.second;
+  cudaError_t e = cudaMalloc(&m->w8, total);
+  if (e != cudaSuccess) return e;
+  unsigned int* d_amax = nullptr;
+  e = cudaMalloc(&d_amax, mats.size() * sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  std::vector<unsigned int> amax(mats.size());
+  e = cudaMemset(d_amax, 0, mats.size() * sizeof(unsigned int));
+  for (size_t i = 0; e == cudaSuccess && i < mats.size(); ++i) {
+    absmax_kernel<<<2 * m->num_sms, 256>>>(src + mats[i].first, (size_t)mats[i].second, d_amax + i);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaMemcpy(amax.data(), d_amax, mats.size() * sizeof(unsigned int), cudaMemcpyDeviceToHost);
+  cudaFree(d_amax);
+  if (e != cudaSuccess) return e;
+  uint8_t* q = static_cast<uint8_t*>(m->w8);
+  __nv_bfloat16* img = static_cast<__nv_bfloat16*>(m->weights);
+  m->w8_scale.clear();
+  for (size_t i = 0; i < mats.size(); ++i) {
+    float a;
+    std::memcpy(&a, &amax[i], sizeof(a));
+    double scale = 1.0;
+    if (a > 0.f) {
+      int ex = 0;
+      const double mant = std::frexp((double)a / 448.0, &ex);   // a / 448 = mant * 2^ex, mant in [0.5, 1)
+      scale = std::ldexp(1.0, mant == 0.5 ? ex - 1 : ex);
+    }
+    m->w8_scale.push_back((float)scale);
+    quantize_e4m3_kernel<<<4 * m->num_sms, 256>>>(src + mats[i].first, (size_t)mats[i].second,
+                                                  (float)(1.0 / scale), (float)scale, q, img + mats[i].first);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    q += mats[i].second;
+  }
+  return cudaSuccess;
 }
 
 cudaEvent_t next_event(nc_model* m) {
@@ -315,11 +394,12 @@ nc_status validate(const nc_config* c) {
   if (!c) return NC_ERR_INVALID_ARG;
   if (c->n_layer < 1 || c->d_model < 32 || c->n_head < 1 || c->head_dim < 32 || c->d_mlp < 1 ||
       c->vocab < 1 || c->max_batch < 1 || c->max_seq < 1 || !(c->rope_base > 0.f) ||
-      !(c->softcap > 0.f) || !(c->rms_eps >= 0.f) || (c->dtype != NC_F32 && c->dtype != NC_BF16))
+      !(c->softcap > 0.f) || !(c->rms_eps >= 0.f) ||
+      (c->dtype != NC_F32 && c->dtype != NC_BF16 && c->dtype != NC_FP8))
     return NC_ERR_INVALID_ARG;
   if (c->n_kv_head < 1 || c->n_head % c->n_kv_head || c->window < 0) return NC_ERR_INVALID_ARG;
   if (c->window > 0 && c->n_layer > 64) return NC_ERR_UNSUPPORTED;   // one bit per layer
-  if (c->dtype == NC_BF16) {
+  if (c->dtype == NC_BF16 || c->dtype == NC_FP8) {
     if (c->head_dim != 128 || c->d_model % 256 || c->d_mlp % 256 || c->vocab % 256 ||
         ((c->n_head + 2 * c->n_kv_head) * 128) % 256 || c->n_head > 16 || c->n_head % 2)
       return NC_ERR_UNSUPPORTED;
@@ -349,8 +429,9 @@ cudaError_t launch_k(bool pdl, void (*k)(KArgs...), dim3 grid, dim3 block, size_
 }
 
 // Decode attention: the grid.x groups of a row form one thread-block cluster
-// (they merge through distributed shared memory); `pdl` as for launch_k.
-template <typename... Args>
+// (they merge through distributed shared memory); `pdl` as for launch_k.  TO
+// is the output (activation) type.
+template <typename TO = __nv_bfloat16, typename... Args>
 cudaError_t launch_attn_decode(bool pdl, dim3 grid, cudaStream_t s, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -366,7 +447,7 @@ cudaError_t launch_attn_decode(bool pdl, dim3 grid, cudaStream_t s, Args&&... ar
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, attn_decode_mma_kernel, std::forward<Args>(args)...);
+  return cudaLaunchKernelEx(&cfg, attn_decode_mma_kernel<TO>, std::forward<Args>(args)...);
 }
 
 // Prefill GEMM; tb is a weight map with a box of BN/2 rows.  cl selects the
@@ -680,13 +761,13 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
   return NC_OK;
 }
 
-template <int NB, int EPI>
+template <int NB, int EPI, bool FP8>
 cudaError_t launch_skinny(nc_model* m, const CUtensorMap& tw, const CUtensorMap& ta, SkinnyArgs a, int tiles,
                           cudaStream_t s) {
-  using C = SkCfg<NB>;
+  using C = SkCfg<NB, FP8>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles, a.splits, 1);
-  cfg.blockDim = dim3(128, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -698,7 +779,7 @@ cudaError_t launch_skinny(nc_model* m, const CUtensorMap& tw, const CUtensorMap&
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<NB, EPI>, tw, ta, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<NB, EPI, FP8>, tw, ta, a);
   m->launches++;
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -715,13 +796,14 @@ SkinnyArgs skinny_args(nc_model* m, int B, int N, int K, int splits) {
   a.softcap = m->cfg.softcap;
   a.err = m->err;
   a.wait_limit_ns = m->wait_limit_ns;
+  a.w_scale = 1.f;
   return a;
 }
 
 // One decode step of the bf16 model for B <= NB rows on the skinny GEMMs.
 // Every kernel takes the position from the device-side length, so the
 // sequence is the same at every step and can be replayed as a CUDA graph.
-template <int NB>
+template <int NB, bool FP8>
 nc_status forward_decode_nb(nc_model* m, const DecodeBufs& db, const int32_t* tok, int B, float* logits,
                             cudaStream_t s) {
   const nc_config& c = m->cfg;
@@ -730,8 +812,14 @@ nc_status forward_decode_nb(nc_model* m, const DecodeBufs& db, const int32_t* to
   const int NQKV = (nh + 2 * nkv) * 128, NQ = nh * 128;
   const float eps = c.rms_eps;
   using bf16 = __nv_bfloat16;
+  // the decode GEMMs' activations: bf16, or f16 with FP8 weights (the tensor
+  // core takes the same type for both operands)
+  using TA = typename std::conditional<FP8, __half, bf16>::type;
+  // weight map and scale of matrix g (0 Wqkv, 1 Wo, 2 Wfc, 3 Wproj) of layer l
+  auto wmap = [&](int l, int g) -> const CUtensorMap& { return FP8 ? m->tm_w8[4 * l + g] : m->tm_w128[4 * l + g]; };
+  auto wscale = [&](int l, int g) { return FP8 ? m->w8_scale[4 * l + g] : 1.f; };
   // RMSNorm folded into the projections: every residual update writes
-  // h = bf16(x) and per-block sums of squares; QKV, MLP up and lm_head scale
+  // h = TA(x) and per-block sums of squares; QKV, MLP up and lm_head scale
   // their rows by 1/rms(x) (r (x W^T) = (r x) W^T)
   const int ss_ld = db.ss_ld, n_ss = d / 128;
   auto fold_in = [&](SkinnyArgs& a) {
@@ -740,14 +828,14 @@ nc_status forward_decode_nb(nc_model* m, const DecodeBufs& db, const int32_t* to
     a.ss_ld = ss_ld;
   };
   auto fold_out = [&](SkinnyArgs& a) {
-    a.h_out = static_cast<bf16*>(db.h);
+    a.h_out = db.h;
     a.ss_out = db.ss;
     a.ss_ld = ss_ld;
   };
   {
     KScope ks(m, NC_K_EMBED, s);
-    embed_rmsnorm_kernel<bf16, bf16><<<blocks_for_warps(B), 256, 0, s>>>(
-        tok, static_cast<const bf16*>(m->E), db.x, static_cast<bf16*>(db.h), B, d, V, eps, m->err, db.ss, ss_ld);
+    embed_rmsnorm_kernel<bf16, TA><<<blocks_for_warps(B), 256, 0, s>>>(
+        tok, static_cast<const bf16*>(m->E), db.x, static_cast<TA*>(db.h), B, d, V, eps, m->err, db.ss, ss_ld);
     m->launches++;
     NC_TRY(cudaGetLastError());
   }
@@ -764,40 +852,44 @@ nc_status forward_decode_nb(nc_model* m, const DecodeBufs& db, const int32_t* to
       a.n_head = nh;
       a.n_kv = nkv;
       a.cache_S = c.max_seq;
+      a.w_scale = wscale(l, 0);
       fold_in(a);
-      NC_TRY((launch_skinny<NB, EPI_QKV>(m, m->tm_w128[4 * l + 0], db.tm_h_nb, a, NQKV / 128, s)));
+      NC_TRY((launch_skinny<NB, EPI_QKV, FP8>(m, wmap(l, 0), db.tm_h_nb, a, NQKV / 128, s)));
     }
     {
       KScope ks(m, NC_K_ATTN, s);
       int group = 2, gx = 1;
       const int win = layer_window(m, l);
       decode_attn_shape(m, B, win, &group, &gx);
-      NC_TRY(launch_attn_decode(true, dim3(gx, B * nkv), s, static_cast<const bf16*>(db.q),
-                                static_cast<const bf16*>(m->kc(l)), static_cast<const bf16*>(m->vc(l)),
-                                static_cast<bf16*>(db.att), nh, (int)c.max_seq, 0,
-                                static_cast<const int*>(m->d_len), kAttnScaleLog2, group, nkv, win));
+      NC_TRY(launch_attn_decode<TA>(true, dim3(gx, B * nkv), s, static_cast<const bf16*>(db.q),
+                                    static_cast<const bf16*>(m->kc(l)), static_cast<const bf16*>(m->vc(l)),
+                                    static_cast<TA*>(db.att), nh, (int)c.max_seq, 0,
+                                    static_cast<const int*>(m->d_len), kAttnScaleLog2, group, nkv, win));
       m->launches++;
     }
     {
       KScope ks(m, NC_K_OPROJ, s);
       SkinnyArgs a = skinny_args(m, B, d, NQ, m->sk_splits[1]);
       a.x = db.x;
+      a.w_scale = wscale(l, 1);
       fold_out(a);
-      NC_TRY((launch_skinny<NB, EPI_RESID>(m, m->tm_w128[4 * l + 1], db.tm_att_nb, a, d / 128, s)));
+      NC_TRY((launch_skinny<NB, EPI_RESID, FP8>(m, wmap(l, 1), db.tm_att_nb, a, d / 128, s)));
     }
     {
       KScope ks(m, NC_K_FC, s);
       SkinnyArgs a = skinny_args(m, B, F, d, m->sk_splits[2]);
-      a.out_bf = static_cast<bf16*>(db.u);
+      a.out_act = db.u;
+      a.w_scale = wscale(l, 2);
       fold_in(a);
-      NC_TRY((launch_skinny<NB, EPI_RELU2>(m, m->tm_w128[4 * l + 2], db.tm_h_nb, a, F / 128, s)));
+      NC_TRY((launch_skinny<NB, EPI_RELU2, FP8>(m, wmap(l, 2), db.tm_h_nb, a, F / 128, s)));
     }
     {
       KScope ks(m, NC_K_PROJ, s);
       SkinnyArgs a = skinny_args(m, B, d, F, m->sk_splits[3]);
       a.x = db.x;
+      a.w_scale = wscale(l, 3);
       fold_out(a);
-      NC_TRY((launch_skinny<NB, EPI_RESID>(m, m->tm_w128[4 * l + 3], db.tm_u_nb, a, d / 128, s)));
+      NC_TRY((launch_skinny<NB, EPI_RESID, FP8>(m, wmap(l, 3), db.tm_u_nb, a, d / 128, s)));
     }
   }
   {
@@ -806,7 +898,9 @@ nc_status forward_decode_nb(nc_model* m, const DecodeBufs& db, const int32_t* to
     a.x = logits;
     fold_in(a);
     a.len_inc = m->d_len;                            // the step's last kernel
-    NC_TRY((launch_skinny<NB, EPI_LOGITS>(m, m->tm_wu128, db.tm_h_nb, a, V / 128, s)));
+    a.w_scale = FP8 ? m->w8_scale[4 * c.n_layer] : 1.f;
+    NC_TRY((launch_skinny<NB, EPI_LOGITS, FP8>(m, FP8 ? m->tm_w8[4 * c.n_layer] : m->tm_wu128, db.tm_h_nb, a,
+                                               V / 128, s)));
   }
   return NC_OK;
 }
@@ -821,14 +915,14 @@ cudaError_t configure_gemm_tc() {
   cudaError_t e = set_gemm_smem<256, EPI, 0>();
   return e != cudaSuccess ? e : set_gemm_smem<256, EPI, 2>();
 }
-template <int NB>
+template <int NB, bool FP8>
 cudaError_t configure_skinny() {
-  const int sm = (int)SkCfg<NB>::SMEM;
+  const int sm = (int)SkCfg<NB, FP8>::SMEM;
   const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI_QKV>, a, sm);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI_RESID>, a, sm);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI_RELU2>, a, sm);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI_LOGITS>, a, sm);
+  cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI_QKV, FP8>, a, sm);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI_RESID, FP8>, a, sm);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI_RELU2, FP8>, a, sm);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_skinny_kernel<NB, EPI_LOGITS, FP8>, a, sm);
   return e;
 }
 template <typename K>
@@ -849,12 +943,22 @@ cudaError_t configure_kernels(const nc_model* m) {
     step(configure_gemm_tc<EPI_RELU2>());
     step(configure_gemm_tc<EPI_LOGITS>());
     step(configure_gemm_tc<EPI_STORE>());
-    step(configure_skinny<32>());
-    step(configure_skinny<64>());
-    step(configure_skinny<128>());
+    if (m->fp8) {
+      step(configure_skinny<32, true>());
+      step(configure_skinny<64, true>());
+      step(configure_skinny<128, true>());
+      step(cudaFuncSetAttribute(attn_decode_mma_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)ATT_DECODE_SMEM));
+      step(load_kernel(embed_rmsnorm_kernel<bf16, __half>));
+      step(load_kernel(absmax_kernel));
+      step(load_kernel(quantize_e4m3_kernel));
+    }
+    step(configure_skinny<32, false>());
+    step(configure_skinny<64, false>());
+    step(configure_skinny<128, false>());
     step(cudaFuncSetAttribute(attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)ATC_SMEM));
-    step(cudaFuncSetAttribute(attn_decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    step(cudaFuncSetAttribute(attn_decode_mma_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)ATT_DECODE_SMEM));
     step(load_kernel(embed_rmsnorm_kernel<bf16, bf16>));
     step(load_kernel(rmsnorm_kernel<bf16>));
@@ -882,10 +986,17 @@ nc_status forward_decode(nc_model* m, const int32_t* tok, int B, float* logits, 
                          const DecodeBufs* db = nullptr) {
   if (!decode_on_skinny(m, B)) return forward(m, tok, B, 1, 0, logits, false, s, true);
   const DecodeBufs& b = db ? *db : m->dbuf;
+  if (m->fp8) {
+    switch (m->sk_nb) {
+      case 32: return forward_decode_nb<32, true>(m, b, tok, B, logits, s);
+      case 64: return forward_decode_nb<64, true>(m, b, tok, B, logits, s);
+      default: return forward_decode_nb<128, true>(m, b, tok, B, logits, s);
+    }
+  }
   switch (m->sk_nb) {
-    case 32: return forward_decode_nb<32>(m, b, tok, B, logits, s);
-    case 64: return forward_decode_nb<64>(m, b, tok, B, logits, s);
-    default: return forward_decode_nb<128>(m, b, tok, B, logits, s);
+    case 32: return forward_decode_nb<32, false>(m, b, tok, B, logits, s);
+    case 64: return forward_decode_nb<64, false>(m, b, tok, B, logits, s);
+    default: return forward_decode_nb<128, false>(m, b, tok, B, logits, s);
   }
 }
 
@@ -1012,7 +1123,8 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   nc_model* m = new (std::nothrow) nc_model();
   if (!m) return NC_ERR_OOM;
   m->cfg = *cfg;
-  m->bf16 = cfg->dtype == NC_BF16;
+  m->bf16 = cfg->dtype == NC_BF16 || cfg->dtype == NC_FP8;   // FP8: bf16 compute, FP8 decode weights
+  m->fp8 = cfg->dtype == NC_FP8;
   m->wbytes = m->bf16 ? 2 : 4;
   const nc_config& c = m->cfg;
   const int64_t d = c.d_model, hd = c.head_dim, nh = c.n_head, F = c.d_mlp, V = c.vocab;
@@ -1054,7 +1166,9 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
     }
     f32_to_bf16_kernel<<<4 * m->num_sms, 256>>>(dev_src ? weights : tmp,
                                                  static_cast<__nv_bfloat16*>(m->weights), n_params);
-    cudaError_t e = cudaDeviceSynchronize();
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess && m->fp8) e = quantize_fp8_weights(m, dev_src ? weights : tmp);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (tmp) cudaFree(tmp);
     CREATE_TRY(e);
   } else {
@@ -1200,6 +1314,18 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
            make_tmap(&m->tm_w128[4 * l + 1], m->wo[l], d, NQ, 128) &&
            make_tmap(&m->tm_w128[4 * l + 2], m->wfc[l], F, d, 128) &&
            make_tmap(&m->tm_w128[4 * l + 3], m->wproj[l], d, F, 128);
+    if (ok && m->fp8) {
+      // E4M3 matrices in the order quantize_fp8_weights wrote them
+      m->tm_w8.resize(4 * c.n_layer + 1);
+      const uint8_t* q = static_cast<const uint8_t*>(m->w8);
+      const int64_t rows[4] = {NQKV, d, F, d}, cols[4] = {d, NQ, d, F};
+      for (int l = 0; ok && l < c.n_layer; ++l)
+        for (int g = 0; ok && g < 4; ++g) {
+          ok = make_tmap8(&m->tm_w8[4 * l + g], q, rows[g], cols[g], 128);
+          q += rows[g] * cols[g];
+        }
+      ok = ok && make_tmap8(&m->tm_w8[4 * c.n_layer], q, V, d, 128);
+    }
     m->tm_kc.resize(c.n_layer);
     for (int l = 0; ok && l < c.n_layer; ++l) {
       const uint64_t dims[3] = {128, (uint64_t)c.max_seq, (uint64_t)(c.max_batch * nkv)};

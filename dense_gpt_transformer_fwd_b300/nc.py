@@ -16,7 +16,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libnc.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "nc.h")
 
-NC_F32, NC_BF16 = 0, 1
+NC_F32, NC_BF16, NC_FP8 = 0, 1, 2
+DTYPES = {"f32": NC_F32, "bf16": NC_BF16, "fp8": NC_FP8}
 KCLASSES = ("embed", "qkv", "attn", "oproj", "norm", "fc", "proj", "lm_head")
 STATUS = {0: "NC_OK", 1: "NC_ERR_INVALID_ARG", 2: "NC_ERR_UNSUPPORTED", 3: "NC_ERR_OOM",
           4: "NC_ERR_STATE", 5: "NC_ERR_CAPACITY", 6: "NC_ERR_TOKEN", 7: "NC_ERR_TIMEOUT",
@@ -132,7 +133,7 @@ def make_config(shape, max_batch: int, max_seq: int) -> NcConfig:
     pattern = getattr(shape, "window_pattern", "") or ""
     return NcConfig(shape.n_layer, shape.d_model, shape.n_head, shape.n_kv_head, shape.head_dim,
                     shape.d_mlp, shape.vocab, shape.rope_base, shape.softcap, shape.rms_eps,
-                    NC_BF16 if shape.dtype == "bf16" else NC_F32, max_batch, max_seq,
+                    DTYPES[shape.dtype], max_batch, max_seq,
                     window if pattern else 0, 0, window_layers(pattern, shape.n_layer) if window else 0)
 
 

@@ -58,7 +58,7 @@ typedef enum {
   NC_ERR_SCRATCH_LIMIT = 9 /* nc_decode_step_noalloc: the batch or the model is beyond its fixed scratch */
 } nc_status;
 
-typedef enum { NC_F32 = 0, NC_BF16 = 1 } nc_dtype;
+typedef enum { NC_F32 = 0, NC_BF16 = 1, NC_FP8 = 2 } nc_dtype;
 
 /*
  * Model shape and capacity.  Shapes of the pages' models: d20 has d_model
@@ -77,6 +77,14 @@ typedef enum { NC_F32 = 0, NC_BF16 = 1 } nc_dtype;
  *            accumulation and an fp32 residual stream; needs head_dim == 128,
  *            d_model, d_mlp and n_head*head_dim multiples of 256, vocab a
  *            multiple of 256.
+ *   NC_FP8:  as NC_BF16, with FP8 projection weights (the FP8 path of
+ *            apidog.com/th "how nanochat works" item 3): each of Wqkv, Wo, Wfc,
+ *            Wproj and Wu is rounded at creation to E4M3 values (nearest
+ *            even, saturating) times one power-of-two scale per matrix,
+ *            2^ceil(log2(amax / 448)).  Decode steps stream the E4M3 bytes
+ *            (half the weight traffic) and widen them exactly to f16, with f16
+ *            activations; prefill runs the bf16 path on the exact bf16 image
+ *            of the same rounded weights.  E stays bf16.
  *   NC_F32:  everything fp32 (SIMT kernels); head_dim 64 or 128.
  *   rms_eps sits inside the square root: x / sqrt(mean(x^2) + eps).
  *   max_batch / max_seq size the KV cache [n_layer][max_batch][n_kv_head][max_seq][head_dim]

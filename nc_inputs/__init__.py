@@ -23,7 +23,11 @@ Random recipe: every matrix entry is N(0, 0.02), drawn in that order from one
 ``numpy.random.default_rng(seed)`` stream as float32 standard normals times
 0.02.  For bf16 workloads each value is then rounded to the nearest bf16
 (ties to even), so both sides consume exactly the same, bf16-representable
-numbers.  Token ids are uniform over ``[0, V)`` from ``default_rng(seed)``.
+numbers.  For fp8 workloads every projection matrix (Wqkv, Wo, Wfc, Wproj,
+Wu) is rounded instead to a multiple of one power-of-two scale per matrix,
+s = 2**ceil(log2(amax / 448)), by an FP8 E4M3 value (round to nearest even,
+saturating at 448), and E to bf16.  Token ids are uniform over ``[0, V)`` from
+``default_rng(seed)``.
 """
 from __future__ import annotations
 
@@ -33,7 +37,8 @@ import numpy as np
 
 __all__ = [
     "ModelShape", "Workload", "SHAPES", "WORKLOADS", "param_count",
-    "layer_param_count", "gen_weights", "gen_tokens", "round_to_bf16",
+    "layer_param_count", "gen_weights", "gen_tokens", "round_to_bf16", "round_to_e4m3",
+    "fp8_scale", "round_to_fp8_tensorwise", "weight_matrices",
 ]
 
 
@@ -50,7 +55,7 @@ class ModelShape:
     rope_base: float = 10000.0
     softcap: float = 15.0
     rms_eps: float = 1e-6
-    dtype: str = "bf16"          # "bf16" or "f32": the precision the model computes in
+    dtype: str = "bf16"          # "bf16", "fp8" (FP8 E4M3 projection weights) or "f32"
     # sliding-window attention: layer l uses `window` (keys p - window + 1 .. p)
     # where window_pattern[l % len] is "S", the whole causal context for "L";
     # an empty pattern (the default) leaves every layer unrestricted
@@ -94,6 +99,8 @@ WORKLOADS = {w.name: w for w in (
     Workload("d20_decode", D20, 64, 1024, 128, 1020, 2120, 3020),
     Workload("d24_prefill", D24, 8, 2048, 0, 1024, 2024, None),
     Workload("d24_decode", D24, 128, 2048, 128, 1024, 2124, 3024),
+    # the d24 decode workload with FP8 projection weights (same seeds)
+    Workload("d24_decode_fp8", D24.with_(name="d24_fp8", dtype="fp8"), 128, 2048, 128, 1024, 2124, 3024),
 )}
 
 
@@ -123,6 +130,53 @@ def round_to_bf16(a: np.ndarray) -> np.ndarray:
     return r.view(np.float32)
 
 
+E4M3_MAX = 448.0          # largest finite FP8 E4M3 value: 1.75 * 2**8
+E4M3_MIN_NORMAL = 2.0 ** -6
+E4M3_QUANTUM_MIN = 2.0 ** -9   # spacing of the subnormals
+
+
+def round_to_e4m3(a: np.ndarray) -> np.ndarray:
+    """Round to the nearest FP8 E4M3 value (ties to even), saturating at
+    +-448; returned as float32.  E4M3: 3 mantissa bits, exponent bias 7,
+    normals from 2**-6, subnormals in steps of 2**-9."""
+    x = np.asarray(a, dtype=np.float64)
+    ax = np.abs(x)
+    _, e2 = np.frexp(np.maximum(ax, E4M3_MIN_NORMAL))      # ax = f * 2**e2, f in [0.5, 1)
+    quantum = np.ldexp(1.0, e2 - 1 - 3)                   # 3 mantissa bits below the leading one
+    q = np.rint(ax / quantum) * quantum                  # np.rint rounds half to even
+    q = np.minimum(q, E4M3_MAX)
+    return (np.sign(x) * q).astype(np.float32)
+
+
+def fp8_scale(a: np.ndarray) -> float:
+    """Power-of-two tensor scale 2**ceil(log2(amax / 448)) (1 for an all-zero matrix)."""
+    amax = float(np.max(np.abs(a))) if a.size else 0.0
+    if amax == 0.0:
+        return 1.0
+    m, e = np.frexp(amax / E4M3_MAX)                      # amax / 448 = m * 2**e, m in [0.5, 1)
+    return float(np.ldexp(1.0, int(e) - 1 if m == 0.5 else int(e)))
+
+
+def round_to_fp8_tensorwise(a: np.ndarray) -> np.ndarray:
+    """a rounded to s * e4m3(a / s) with the matrix's power-of-two scale s."""
+    s = fp8_scale(a)
+    return (round_to_e4m3(np.asarray(a, dtype=np.float64) / s).astype(np.float64) * s).astype(np.float32)
+
+
+def weight_matrices(s: ModelShape):
+    """(name, offset, rows, cols) of every matrix of the packed vector, in order."""
+    d, hd, V, F = s.d_model, s.head_dim, s.vocab, s.d_mlp
+    q, kv = s.n_head * hd, s.n_kv_head * hd
+    out, off = [], 0
+    for name, r, c in ([("E", V, d)] +
+                       [(f"{n}{l}", r, c) for l in range(s.n_layer)
+                        for n, r, c in (("Wqkv", q + 2 * kv, d), ("Wo", d, q), ("Wfc", F, d), ("Wproj", d, F))] +
+                       [("Wu", V, d)]):
+        out.append((name, off, r, c))
+        off += r * c
+    return out
+
+
 def gen_weights(s: ModelShape, seed: int, std: float = 0.02) -> np.ndarray:
     """Packed float32 weight vector in canonical order, N(0, std^2) entries."""
     n = param_count(s)
@@ -134,6 +188,10 @@ def gen_weights(s: ModelShape, seed: int, std: float = 0.02) -> np.ndarray:
         step = 1 << 26
         for i in range(0, n, step):
             w[i:i + step] = round_to_bf16(w[i:i + step])
+    elif s.dtype == "fp8":
+        for name, off, r, c in weight_matrices(s):
+            seg = w[off:off + r * c]
+            w[off:off + r * c] = round_to_bf16(seg) if name == "E" else round_to_fp8_tensorwise(seg)
     return w
 
 
