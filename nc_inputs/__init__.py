@@ -38,7 +38,7 @@ import numpy as np
 __all__ = [
     "ModelShape", "Workload", "SHAPES", "WORKLOADS", "param_count",
     "layer_param_count", "gen_weights", "gen_tokens", "round_to_bf16", "round_to_e4m3",
-    "fp8_scale", "round_to_fp8_tensorwise", "weight_matrices",
+    "fp8_scale", "round_to_fp8_tensorwise", "weight_matrices", "extras_layout", "ve_layers",
 ]
 
 
@@ -61,6 +61,17 @@ class ModelShape:
     # an empty pattern (the default) leaves every layer unrestricted
     window: int = 0
     window_pattern: str = ""
+    # later-architecture extras (off by default): value embeddings on the even
+    # layers with a gate over the first ve_gate_channels channels, per-layer
+    # residual / x0 lambdas, smear over the first smear_channels channels,
+    # backout of the mid-layer residual.  Their parameters follow Wu in the
+    # packed vector (see extras_layout).
+    value_embeds: bool = False
+    resid_lambdas: bool = False
+    smear: bool = False
+    backout: bool = False
+    ve_gate_channels: int = 32
+    smear_channels: int = 24
 
     def with_(self, **kw) -> "ModelShape":
         return replace(self, **kw)
@@ -113,9 +124,33 @@ def layer_param_count(s: ModelShape) -> int:
     return qkv + o + mlp
 
 
+def ve_layers(s: ModelShape) -> list[int]:
+    """Layers with a value embedding: the even ones, 0, 2, 4, ..."""
+    return list(range(0, s.n_layer, 2)) if s.value_embeds else []
+
+
+def extras_layout(s: ModelShape):
+    """(name, count) of the extras' parameters after Wu, in order: the value
+    embedding tables VE_l [V][n_kv * hd] of every even layer, then their gate
+    matrices G_l [n_kv][ve_gate_channels]; resid_lambdas [L], x0_lambdas [L];
+    the smear gate [smear_channels] and smear_lambda [1]; backout_lambda [1]."""
+    out = []
+    for l in ve_layers(s):
+        out.append((f"VE{l}", s.vocab * s.n_kv_head * s.head_dim))
+    for l in ve_layers(s):
+        out.append((f"VEgate{l}", s.n_kv_head * s.ve_gate_channels))
+    if s.resid_lambdas:
+        out += [("resid_lambdas", s.n_layer), ("x0_lambdas", s.n_layer)]
+    if s.smear:
+        out += [("smear_gate", s.smear_channels), ("smear_lambda", 1)]
+    if s.backout:
+        out.append(("backout_lambda", 1))
+    return out
+
+
 def param_count(s: ModelShape) -> int:
-    """Length of the packed weight vector: E, the blocks, Wu."""
-    return 2 * s.vocab * s.d_model + s.n_layer * layer_param_count(s)
+    """Length of the packed weight vector: E, the blocks, Wu, the extras."""
+    return 2 * s.vocab * s.d_model + s.n_layer * layer_param_count(s) + sum(n for _, n in extras_layout(s))
 
 
 def round_to_bf16(a: np.ndarray) -> np.ndarray:
@@ -183,6 +218,16 @@ def gen_weights(s: ModelShape, seed: int, std: float = 0.02) -> np.ndarray:
     rng = np.random.default_rng(seed)
     w = rng.standard_normal(n, dtype=np.float32)
     w *= np.float32(std)
+    # extras: the lambdas near their neutral values (residual 1, the others 0)
+    # with a spread of 0.1, the tables and gates as drawn
+    off = 2 * s.vocab * s.d_model + s.n_layer * layer_param_count(s)
+    for name, cnt in extras_layout(s):
+        seg = w[off:off + cnt]
+        if name == "resid_lambdas":
+            seg[:] = 1.0 + seg * np.float32(0.1 / std)
+        elif name in ("x0_lambdas", "smear_lambda", "backout_lambda"):
+            seg[:] = seg * np.float32(0.1 / std)
+        off += cnt
     if s.dtype == "bf16":
         # chunked to bound the temporary memory on the largest models
         step = 1 << 26

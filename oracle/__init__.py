@@ -8,4 +8,5 @@ module both sides use is ``nc_inputs`` (seeded input generators).
 from .gpt_oracle import (  # noqa: F401
     OracleModel, unpack_weights, rms_norm, rope_tables, apply_rope, causal_attention,
     relu_squared, softcap, block_param_count, total_param_count, sample_tokens, layer_window,
+    unpack_extras, extras_count, sigmoid,
 )

@@ -42,6 +42,17 @@ Readings taken where the pages are silent or garbled (identical in the CUDA path
      the letter pattern[l % len(pattern)]; "S" limits a query at position p to
      the keys p - window + 1 .. p, "L" is the unrestricted causal window.  An
      empty pattern or window 0 leaves every layer unrestricted.
+  R14 later-architecture extras [apidog 1, "performance tricks" and the
+     value-embedding snippet; the autoresearch list names backout and smear]:
+     value embeddings on alternate layers, read as the even layers 0, 2, ...:
+     v += 3 sigmoid(h[:C] G_l^T) * VE_l[tok] per K/V head, h the block's
+     normed input, C = ve_gate_channels (the pages give no width; 32);
+     per-layer residual scaling before block i: x = resid_i x + x0_i x0, x0
+     the residual that enters block 0; smear after the embedding norm:
+     x_t += smear_lambda sigmoid(x_t[:24] . w) x_{t-1}, the previous token's
+     embedding (nothing before the first position); backout after the last
+     block: x -= backout_lambda x_mid, x_mid the residual after the first half
+     of the blocks (block L // 2 - 1).  Each is off unless the shape enables it.
   R11 sampling (the pages name parallel sampling but not its rule; plainest
      reading): temperature 0 is greedy, the lowest index among equal maxima;
      otherwise the candidates are ordered by (logit descending, index
@@ -100,9 +111,59 @@ def unpack_weights(flat, shape):
         layers.append(dict(Wqkv=take(q + 2 * kv, d), Wo=take(d, q),
                            Wfc=take(F, d), Wproj=take(d, F)))
     Wu = take(V, d)
-    if off != flat.size:
-        raise ValueError(f"packed weights: consumed {off} of {flat.size} values")
+    if off + extras_count(shape) != flat.size:
+        raise ValueError(f"packed weights: consumed {off + extras_count(shape)} of {flat.size} values")
     return E, layers, Wu
+
+
+def _ve_layers(s):
+    """Layers with a value embedding (R14): the even ones."""
+    return list(range(0, s.n_layer, 2)) if getattr(s, "value_embeds", False) else []
+
+
+def extras_count(s):
+    """Parameters of the enabled extras (R14), stored after Wu."""
+    n = 0
+    for _ in _ve_layers(s):
+        n += s.vocab * s.n_kv_head * s.head_dim + s.n_kv_head * s.ve_gate_channels
+    if getattr(s, "resid_lambdas", False):
+        n += 2 * s.n_layer
+    if getattr(s, "smear", False):
+        n += s.smear_channels + 1
+    if getattr(s, "backout", False):
+        n += 1
+    return n
+
+
+def unpack_extras(flat, s):
+    """The extras' parameters after Wu (R14), in order: the value-embedding
+    tables of the even layers [V, n_kv * hd], their gates [n_kv, C]; residual
+    and x0 lambdas [L] each; smear gate [24] and lambda; backout lambda."""
+    flat = np.asarray(flat)
+    off = flat.size - extras_count(s)
+
+    def take(n):
+        nonlocal off
+        a = flat[off:off + n].astype(np.float64)
+        off += n
+        return a
+
+    ex = {"ve": {}, "ve_gate": {}}
+    for l in _ve_layers(s):
+        ex["ve"][l] = take(s.vocab * s.n_kv_head * s.head_dim).reshape(s.vocab, s.n_kv_head, s.head_dim)
+    for l in _ve_layers(s):
+        ex["ve_gate"][l] = take(s.n_kv_head * s.ve_gate_channels).reshape(s.n_kv_head, s.ve_gate_channels)
+    if getattr(s, "resid_lambdas", False):
+        ex["resid"], ex["x0"] = take(s.n_layer), take(s.n_layer)
+    if getattr(s, "smear", False):
+        ex["smear_gate"], ex["smear_lambda"] = take(s.smear_channels), take(1)[0]
+    if getattr(s, "backout", False):
+        ex["backout_lambda"] = take(1)[0]
+    return ex
+
+
+def sigmoid(z):
+    return 1.0 / (1.0 + np.exp(-z))
 
 
 # --------------------------------------------------------------------------- #
@@ -199,15 +260,17 @@ class OracleModel:
     def __init__(self, flat_weights, shape):
         self.s = shape
         self.E, self.layers, self.Wu = unpack_weights(flat_weights, shape)
+        self.ex = unpack_extras(flat_weights, shape)
         self.reset()
 
     def reset(self):
         self.k_cache = [None] * self.s.n_layer     # each [B, len, n_kv, hd]
         self.v_cache = [None] * self.s.n_layer
         self.length = 0
+        self.prev_tok = None                       # last token of each row (smear, R14)
 
     # one block over the new positions of every row
-    def _block(self, li, x, positions):
+    def _block(self, li, x, positions, tokens=None):
         s, W = self.s, self.layers[li]
         B, T, _ = x.shape
         hd, nh, nkv = s.head_dim, s.n_head, s.n_kv_head
@@ -218,6 +281,10 @@ class OracleModel:
         q = qkv[..., :nh * hd].reshape(B, T, nh, hd)
         k = qkv[..., nh * hd:(nh + nkv) * hd].reshape(B, T, nkv, hd)
         v = qkv[..., (nh + nkv) * hd:].reshape(B, T, nkv, hd)
+        if li in self.ex["ve"]:                                     # value embedding (R14)
+            C = s.ve_gate_channels
+            gate = 3.0 * sigmoid(h[..., :C] @ self.ex["ve_gate"][li].T)   # [B, T, n_kv]
+            v = v + gate[..., None] * self.ex["ve"][li][tokens]
 
         y = np.empty((B, T, nh, hd))
         new_k, new_v = [], []
@@ -250,8 +317,24 @@ class OracleModel:
             raise ValueError("token id out of range")
         positions = np.arange(self.length, self.length + T)
         x = rms_norm(self.E[tokens], s.rms_eps)                     # embedding, then norm
+        ex = self.ex
+        if "smear_gate" in ex:                                      # smear (R14)
+            prev = np.zeros_like(x)
+            prev[:, 1:] = x[:, :-1]
+            if self.length > 0:
+                prev[:, 0] = rms_norm(self.E[self.prev_tok], s.rms_eps)
+            gate = ex["smear_lambda"] * sigmoid(x[..., :s.smear_channels] @ ex["smear_gate"])
+            x = x + gate[..., None] * prev
+        self.prev_tok = tokens[:, -1].copy()
+        x0, x_mid = x, None
         for li in range(s.n_layer):
-            x = self._block(li, x, positions)
+            if "resid" in ex:                                       # residual / x0 lambdas (R14)
+                x = ex["resid"][li] * x + ex["x0"][li] * x0
+            x = self._block(li, x, positions, tokens)
+            if li == s.n_layer // 2 - 1:
+                x_mid = x
+        if "backout_lambda" in ex:                                  # backout (R14)
+            x = x - ex["backout_lambda"] * (x_mid if x_mid is not None else 0.0)
         self.length += T
         if logit_positions is not None:
             x = x[:, logit_positions, :]
@@ -284,6 +367,7 @@ class OracleModel:
         for li in range(self.s.n_layer):
             self.k_cache[li] = np.repeat(self.k_cache[li][src:src + 1], n, axis=0)
             self.v_cache[li] = np.repeat(self.v_cache[li][src:src + 1], n, axis=0)
+        self.prev_tok = np.repeat(self.prev_tok[src:src + 1], n, axis=0)
 
 
 # --------------------------------------------------------------------------- #
