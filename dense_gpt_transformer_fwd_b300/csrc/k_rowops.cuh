@@ -246,6 +246,94 @@ __global__ void quantize_e4m3_kernel(const float* __restrict__ src, size_t n, fl
   }
 }
 
+// ------------------------------------------------ later-architecture extras
+// (apidog.com/th "how nanochat works" item 1: value embeddings, per-layer
+// residual lambdas, smear, backout; parity-only features of a later version)
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + __expf(-z)); }
+
+// Smear, one warp per row m = b*T + t of a call whose row b starts at
+// position pos0[b]: x[m] += lambda * sigmoid(x[m][:SC] . w) * x_prev, x_prev
+// the previous token's normed embedding rms(E[prev]) (the previous token of
+// the call, or prev_tok[b] from the row's earlier calls; none at position 0).
+// x[m] holds rms(E[tok[m]]) on entry (written by the embedding kernel).
+template <typename TW>
+__global__ void smear_kernel(const int32_t* __restrict__ tok, const TW* __restrict__ E, float* __restrict__ x,
+                             int M, int T, int d, int vocab, const int* __restrict__ pos0,
+                             const int32_t* __restrict__ prev_tok, const float* __restrict__ w,
+                             const float* __restrict__ lambda, int SC, float eps) {
+  const int m = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (m >= M) return;
+  const int b = m / T, t = m - b * T;
+  int prev = t > 0 ? tok[m - 1] : (pos0[b] > 0 ? prev_tok[b] : -1);
+  if (prev < 0) return;
+  if (prev >= vocab) prev = 0;                     // flagged by the embedding kernel
+  float* xr = x + (size_t)m * d;
+  float g = 0.f;
+  for (int c = lane; c < SC; c += 32) g = fmaf(xr[c], w[c], g);
+  g = warp_sum(g);
+  const TW* e = E + (size_t)prev * d;
+  float ss = 0.f;
+  for (int j = lane; j < d; j += 32) {
+    const float v = to_f(e[j]);
+    ss = fmaf(v, v, ss);
+  }
+  ss = warp_sum(ss);
+  const float f = *lambda * sigmoidf_(g) * rsqrtf(ss / d + eps);
+  __syncwarp();
+  for (int j = lane; j < d; j += 32) xr[j] = fmaf(f, to_f(e[j]), xr[j]);
+}
+
+// x = a x + c x0 elementwise, a = *pa, c = *pc (the residual and x0 lambdas of a layer)
+__global__ void lambda_mix_kernel(float* __restrict__ x, const float* __restrict__ x0, size_t n,
+                                  const float* __restrict__ pa, const float* __restrict__ pc) {
+  const float a = *pa, c = *pc;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    x[i] = fmaf(a, x[i], c * x0[i]);
+}
+
+// x -= lambda * x_mid elementwise (backout)
+__global__ void backout_kernel(float* __restrict__ x, const float* __restrict__ x_mid, size_t n,
+                               const float* __restrict__ lambda) {
+  const float l = *lambda;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    x[i] = fmaf(-l, x_mid[i], x[i]);
+}
+
+// Value embedding of a layer, one warp per (row m, K/V head g): gate =
+// 3 sigmoid(h[m][:C] . G[g]) and the cached value row (b, g, pos) becomes
+// v + gate * VE[tok[m]][g]; the same in the transposed copy V^T when given.
+// h is the block's normed input (the operand of the QKV projection).
+template <typename TA, typename TC>
+__global__ void value_embed_kernel(const TA* __restrict__ h, int d, const int32_t* __restrict__ tok, int vocab,
+                                   const float* __restrict__ ve, const float* __restrict__ gate_w, int C,
+                                   TC* __restrict__ v_cache, TC* __restrict__ vt, int vt_S, int M, int T,
+                                   int n_kv, int hd, int cache_S, const int* __restrict__ pos0) {
+  const int wi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wi >= M * n_kv) return;
+  const int m = wi / n_kv, g = wi - m * n_kv;
+  const int b = m / T, pos = pos0[b] + (m - b * T);
+  int tk = tok[m];
+  if (tk < 0 || tk >= vocab) tk = 0;               // flagged by the embedding kernel
+  float z = 0.f;
+  for (int c = lane; c < C; c += 32) z = fmaf(to_f(h[(size_t)m * d + c]), gate_w[(size_t)g * C + c], z);
+  z = warp_sum(z);
+  const float gate = 3.f * sigmoidf_(z);
+  const float* e = ve + ((size_t)tk * n_kv + g) * hd;
+  TC* vr = v_cache + (((size_t)b * n_kv + g) * cache_S + pos) * hd;
+  for (int j = lane; j < hd; j += 32) {
+    const TC nv = from_f<TC>(fmaf(gate, e[j], to_f(vr[j])));
+    vr[j] = nv;
+    if (vt) vt[((size_t)(b * n_kv + g) * hd + j) * vt_S + pos] = nv;
+  }
+}
+
+// prev_tok[b] = the last token of row b in this call (index last[b], or T - 1)
+__global__ void set_prev_tok_kernel(const int32_t* __restrict__ tok, int B, int T, const int* __restrict__ last,
+                                    int32_t* __restrict__ prev_tok) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) prev_tok[b] = tok[(size_t)b * T + (last ? last[b] : T - 1)];
+}
+
 // fp32 -> bf16 (round to nearest even) weight conversion
 __global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
                                    size_t n) {

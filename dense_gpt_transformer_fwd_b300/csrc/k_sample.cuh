@@ -204,14 +204,18 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_kernel(const float* __r
 
 // Batch generation: rows [0, n) of every layer's K and V cache become copies
 // of row `src` (each of its n_kv K/V heads: the first copy_bytes bytes of a
-// head's sequence of seq_bytes), and every row's device length becomes len.
+// head's sequence of seq_bytes), and every row's device length becomes len
+// (and, when given, its last token prev_tok[b] becomes src's).
 // grid = (n, n_layer, 2 * n_kv: K or V, then the head).
 __global__ void kv_clone_kernel(char* __restrict__ k_base, char* __restrict__ v_base, size_t layer_bytes,
                                 size_t seq_bytes, int n_kv, int src, size_t copy_bytes, int* __restrict__ d_len,
-                                int len) {
+                                int len, int32_t* __restrict__ prev_tok) {
   const int b = blockIdx.x, l = blockIdx.y;
   const int is_v = (int)blockIdx.z / n_kv, g = (int)blockIdx.z % n_kv;
-  if (l == 0 && blockIdx.z == 0 && threadIdx.x == 0) d_len[b] = len;
+  if (l == 0 && blockIdx.z == 0 && threadIdx.x == 0) {
+    d_len[b] = len;
+    if (prev_tok && b != src) prev_tok[b] = prev_tok[src];   // the smear's previous token
+  }
   if (b == src) return;
   char* base = (is_v ? v_base : k_base) + (size_t)l * layer_bytes;
   const uint4* from = reinterpret_cast<const uint4*>(base + ((size_t)src * n_kv + g) * seq_bytes);

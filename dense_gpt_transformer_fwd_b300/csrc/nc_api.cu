@@ -263,6 +263,19 @@ struct nc_model {
   // buffer above holds their exact dequantized image for the prefill
   bool fp8 = false;
   void* w8 = nullptr;
+  // later-architecture extras (NC_EXTRA_* bits): their fp32 parameters
+  // (the packed tail after Wu) and the buffers they need
+  int extras = 0;
+  float* ex_params = nullptr;          // device copy of the tail (bf16 models; fp32 models point into weights)
+  std::vector<const float*> ve_table, ve_gate;   // per layer (null where no value embedding)
+  const float* resid_l = nullptr;      // [L]
+  const float* x0_l = nullptr;         // [L]
+  const float* smear_w = nullptr;      // [smear_channels]
+  const float* smear_lambda = nullptr;
+  const float* backout_lambda = nullptr;
+  float* x0 = nullptr;                 // [max_rows][d] the residual entering block 0
+  float* x_mid = nullptr;              // [max_rows][d] the residual after block L/2 - 1
+  int32_t* prev_tok = nullptr;         // [max_batch] each row's last token (smear)
   std::vector<float> w8_scale;
   std::vector<CUtensorMap> tm_w8;
   DecodeBufs dbuf;                     // the decode step's intermediates in the workspace above
@@ -298,7 +311,7 @@ void free_model(nc_model* m) {
                   m->k_alloc, m->v_alloc, m->x,
                   m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
                   m->tok_stage, m->logit_stage, m->err, m->vt, m->d_len, m->d_pos0, m->d_last, m->ss_part,
-                  m->w8};
+                  m->w8, m->ex_params, m->x0, m->x_mid, m->prev_tok};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete m;
@@ -399,6 +412,11 @@ nc_status validate(const nc_config* c) {
     return NC_ERR_INVALID_ARG;
   if (c->n_kv_head < 1 || c->n_head % c->n_kv_head || c->window < 0) return NC_ERR_INVALID_ARG;
   if (c->window > 0 && c->n_layer > 64) return NC_ERR_UNSUPPORTED;   // one bit per layer
+  if (c->extras & ~NC_EXTRA_ALL) return NC_ERR_INVALID_ARG;
+  if ((c->extras & NC_EXTRA_VALUE_EMBED) && (c->ve_gate_channels < 1 || c->ve_gate_channels > c->d_model))
+    return NC_ERR_INVALID_ARG;
+  if ((c->extras & NC_EXTRA_SMEAR) && (c->smear_channels < 1 || c->smear_channels > c->d_model))
+    return NC_ERR_INVALID_ARG;
   if (c->dtype == NC_BF16 || c->dtype == NC_FP8) {
     if (c->head_dim != 128 || c->d_model % 256 || c->d_mlp % 256 || c->vocab % 256 ||
         ((c->n_head + 2 * c->n_kv_head) * 128) % 256 || c->n_head > 16 || c->n_head % 2)
@@ -602,7 +620,51 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
     m->launches++;
     NC_TRY(cudaGetLastError());
   }
+  // later-architecture extras (the parameters are fp32 on the device)
+  const size_t xn = (size_t)M * d;
+  const unsigned ew_blocks = (unsigned)std::min<size_t>((xn + 255) / 256, (size_t)8 * m->num_sms);
+  auto renorm = [&]() -> cudaError_t {              // h = rms(x) after x changed
+    if (bf)
+      rmsnorm_kernel<bf16><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<bf16*>(m->h), M, d, 1, nullptr,
+                                                               eps, nullptr);
+    else
+      rmsnorm_kernel<float><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<float*>(m->h), M, d, 1, nullptr,
+                                                                eps, nullptr);
+    m->launches++;
+    return cudaGetLastError();
+  };
+  if (m->extras) {
+    KScope ks(m, NC_K_EMBED, s);
+    if (m->extras & NC_EXTRA_SMEAR) {
+      // x_t += lambda sigmoid(x_t[:SC] . w) rms(E[previous token]); then the
+      // rows' last tokens are kept for the next call
+      if (bf)
+        smear_kernel<bf16><<<blocks_for_warps(M), 256, 0, s>>>(tok, static_cast<const bf16*>(m->E), m->x, M, T, d,
+                                                               V, pos0, m->prev_tok, m->smear_w, m->smear_lambda,
+                                                               c.smear_channels, eps);
+      else
+        smear_kernel<float><<<blocks_for_warps(M), 256, 0, s>>>(tok, static_cast<const float*>(m->E), m->x, M, T,
+                                                                d, V, pos0, m->prev_tok, m->smear_w,
+                                                                m->smear_lambda, c.smear_channels, eps);
+      m->launches++;
+      NC_TRY(cudaGetLastError());
+      set_prev_tok_kernel<<<1, 256, 0, s>>>(tok, B, T, decode ? nullptr : m->d_last, m->prev_tok);
+      m->launches++;
+      NC_TRY(cudaGetLastError());
+      if (!(m->extras & NC_EXTRA_RESID_LAMBDAS)) NC_TRY(renorm());
+    }
+    if (m->extras & NC_EXTRA_RESID_LAMBDAS)
+      NC_TRY(cudaMemcpyAsync(m->x0, m->x, xn * 4, cudaMemcpyDeviceToDevice, s));
+  }
   for (int l = 0; l < c.n_layer; ++l) {
+    if (m->extras & NC_EXTRA_RESID_LAMBDAS) {
+      // x = resid_l x + x0_l x0 before the block, then its normed input
+      KScope ks(m, NC_K_NORM, s);
+      lambda_mix_kernel<<<ew_blocks, 256, 0, s>>>(m->x, m->x0, xn, m->resid_l + l, m->x0_l + l);
+      m->launches++;
+      NC_TRY(cudaGetLastError());
+      NC_TRY(renorm());
+    }
     if (bf && T > 1 && max_p0 > 0) {
       // a later prefill chunk: the attention's V^T operand of the positions
       // cached before it (the QKV epilogue below writes the chunk's own)
@@ -642,6 +704,21 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
             m->c32, static_cast<float*>(m->q), static_cast<float*>(m->kc(l)),
             static_cast<float*>(m->vc(l)), m->rope_cos, m->rope_sin, M, nh, nkv, hd, T, pos0, c.max_seq,
             eps);
+        m->launches++;
+        NC_TRY(cudaGetLastError());
+      }
+      if (m->ve_table.size() && m->ve_table[l]) {
+        // value embedding: v += 3 sigmoid(h[:C] G^T) VE[tok] in the cache (and V^T)
+        const int warps = M * nkv;
+        if (bf)
+          value_embed_kernel<bf16, bf16><<<blocks_for_warps(warps), 256, 0, s>>>(
+              static_cast<const bf16*>(m->h), d, tok, V, m->ve_table[l], m->ve_gate[l], c.ve_gate_channels,
+              static_cast<bf16*>(m->vc(l)), T > 1 ? static_cast<bf16*>(m->vt) : nullptr, m->vt_S, M, T, nkv, hd,
+              c.max_seq, pos0);
+        else
+          value_embed_kernel<float, float><<<blocks_for_warps(warps), 256, 0, s>>>(
+              static_cast<const float*>(m->h), d, tok, V, m->ve_table[l], m->ve_gate[l], c.ve_gate_channels,
+              static_cast<float*>(m->vc(l)), nullptr, 0, M, T, nkv, hd, c.max_seq, pos0);
         m->launches++;
         NC_TRY(cudaGetLastError());
       }
@@ -724,6 +801,17 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->u),
                                             static_cast<const float*>(m->wproj[l]), m->x, M, d, F, d, s));
+      }
+    }
+    if (m->extras & NC_EXTRA_BACKOUT) {
+      // keep the residual after the first half; subtract it after the last block
+      const int mid = c.n_layer / 2 - 1;
+      if (l == mid) NC_TRY(cudaMemcpyAsync(m->x_mid, m->x, xn * 4, cudaMemcpyDeviceToDevice, s));
+      if (l == c.n_layer - 1 && mid >= 0) {
+        KScope ks(m, NC_K_NORM, s);
+        backout_kernel<<<ew_blocks, 256, 0, s>>>(m->x, m->x_mid, xn, m->backout_lambda);
+        m->launches++;
+        NC_TRY(cudaGetLastError());
       }
     }
     {  // h = rms(x): next block's pre-attention norm, or the final norm
@@ -977,10 +1065,23 @@ cudaError_t configure_kernels(const nc_model* m) {
   }
   step(load_kernel(sample_kernel));
   step(load_kernel(kv_clone_kernel));
+  if (m->extras) {
+    step(load_kernel(smear_kernel<__nv_bfloat16>));
+    step(load_kernel(smear_kernel<float>));
+    step(load_kernel(lambda_mix_kernel));
+    step(load_kernel(backout_kernel));
+    step(load_kernel(value_embed_kernel<__nv_bfloat16, __nv_bfloat16>));
+    step(load_kernel(value_embed_kernel<float, float>));
+    step(load_kernel(set_prev_tok_kernel));
+  }
   return e;
 }
 
-bool decode_on_skinny(const nc_model* m, int B) { return m->bf16 && m->sk_nb > 0 && B <= m->sk_nb; }
+// the decode GEMMs fold the RMSNorms into their epilogues; models with the
+// later-architecture extras decode on the generic one-position pass
+bool decode_on_skinny(const nc_model* m, int B) {
+  return m->bf16 && m->sk_nb > 0 && B <= m->sk_nb && m->extras == 0;
+}
 
 nc_status forward_decode(nc_model* m, const int32_t* tok, int B, float* logits, cudaStream_t s,
                          const DecodeBufs* db = nullptr) {
@@ -1131,7 +1232,16 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   const int64_t nkv = c.n_kv_head;
   const int64_t NQKV = (nh + 2 * nkv) * hd, NQ = nh * hd;
   const int64_t layer_params = NQKV * d + d * NQ + F * d + d * F;
-  const int64_t n_params = 2 * V * d + c.n_layer * layer_params;
+  const int64_t n_params = 2 * V * d + c.n_layer * layer_params;   // E, the blocks, Wu
+  // the extras' parameters follow Wu: value-embedding tables of the even
+  // layers [V][n_kv * hd], their gates [n_kv][C]; residual and x0 lambdas [L]
+  // each; smear gate [SC] and lambda; backout lambda
+  const int n_ve = (cfg->extras & NC_EXTRA_VALUE_EMBED) ? (c.n_layer + 1) / 2 : 0;
+  const int64_t n_extra = n_ve * (V * nkv * hd + nkv * (int64_t)c.ve_gate_channels) +
+                          ((cfg->extras & NC_EXTRA_RESID_LAMBDAS) ? 2 * c.n_layer : 0) +
+                          ((cfg->extras & NC_EXTRA_SMEAR) ? c.smear_channels + 1 : 0) +
+                          ((cfg->extras & NC_EXTRA_BACKOUT) ? 1 : 0);
+  m->extras = cfg->extras;
 
 #define CREATE_TRY(expr)                       \
   do {                                         \
@@ -1156,8 +1266,8 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
     }
     const bool dev_src = wk == PTR_DEVICE;
     if (!dev_src) {
-      CREATE_TRY(cudaMalloc(&tmp, n_params * 4));
-      cudaError_t e = cudaMemcpy(tmp, weights, n_params * 4, cudaMemcpyHostToDevice);
+      CREATE_TRY(cudaMalloc(&tmp, (n_params + n_extra) * 4));
+      cudaError_t e = cudaMemcpy(tmp, weights, (n_params + n_extra) * 4, cudaMemcpyHostToDevice);
       if (e != cudaSuccess) {
         cudaFree(tmp);
         free_model(m);
@@ -1168,11 +1278,44 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
                                                  static_cast<__nv_bfloat16*>(m->weights), n_params);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess && m->fp8) e = quantize_fp8_weights(m, dev_src ? weights : tmp);
+    if (e == cudaSuccess && n_extra > 0) {
+      // the extras stay fp32
+      e = cudaMalloc(&m->ex_params, n_extra * 4);
+      if (e == cudaSuccess)
+        e = cudaMemcpy(m->ex_params, (dev_src ? weights : tmp) + n_params, n_extra * 4, cudaMemcpyDeviceToDevice);
+    }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (tmp) cudaFree(tmp);
     CREATE_TRY(e);
   } else {
+    CREATE_TRY(cudaMalloc(&m->ex_params, (n_extra > 0 ? n_extra : 1) * 4));
     CREATE_TRY(cudaMemcpy(m->weights, weights, n_params * 4, cudaMemcpyDefault));
+    if (n_extra > 0) CREATE_TRY(cudaMemcpy(m->ex_params, weights + n_params, n_extra * 4, cudaMemcpyDefault));
+  }
+  if (n_extra > 0) {
+    const float* p = m->ex_params;
+    m->ve_table.assign(c.n_layer, nullptr);
+    m->ve_gate.assign(c.n_layer, nullptr);
+    for (int l = 0; l < c.n_layer && n_ve; l += 2) {
+      m->ve_table[l] = p;
+      p += V * nkv * hd;
+    }
+    for (int l = 0; l < c.n_layer && n_ve; l += 2) {
+      m->ve_gate[l] = p;
+      p += nkv * c.ve_gate_channels;
+    }
+    if (m->extras & NC_EXTRA_RESID_LAMBDAS) {
+      m->resid_l = p;
+      m->x0_l = p + c.n_layer;
+      p += 2 * c.n_layer;
+    }
+    if (m->extras & NC_EXTRA_SMEAR) {
+      m->smear_w = p;
+      m->smear_lambda = p + c.smear_channels;
+      p += c.smear_channels + 1;
+    }
+    if (m->extras & NC_EXTRA_BACKOUT) m->backout_lambda = p;
+    if (!n_ve) m->ve_table.clear();
   }
   {
     const char* p = static_cast<const char*>(m->weights);
@@ -1239,6 +1382,12 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   CREATE_TRY(cudaMalloc(&m->ss_part, (int64_t)(d / 128 + 1) * c.max_batch * 4));
   if (!m->bf16) CREATE_TRY(cudaMalloc(&m->c32, R * NQKV * 4));
   CREATE_TRY(cudaMalloc(&m->tok_stage, R * 4));
+  if (m->extras & NC_EXTRA_RESID_LAMBDAS) CREATE_TRY(cudaMalloc(&m->x0, R * d * 4));
+  if (m->extras & NC_EXTRA_BACKOUT) CREATE_TRY(cudaMalloc(&m->x_mid, R * d * 4));
+  if (m->extras & NC_EXTRA_SMEAR) {
+    CREATE_TRY(cudaMalloc(&m->prev_tok, (size_t)c.max_batch * 4));
+    CREATE_TRY(cudaMemset(m->prev_tok, 0, (size_t)c.max_batch * 4));
+  }
   if (m->bf16) {
     m->vt_S = (c.max_seq + 127) / 128 * 128;
     CREATE_TRY(cudaMalloc(&m->vt, (int64_t)c.max_batch * nkv * 128 * m->vt_S * 2));
@@ -1464,7 +1613,7 @@ nc_status nc_kv_clone(nc_model* m, int32_t src, int32_t n, nc_stream_t stream) {
   const int nkv = m->cfg.n_kv_head;
   kv_clone_kernel<<<dim3(n, m->cfg.n_layer, 2 * nkv), 256, 0, stream>>>(
       k0, v0, (size_t)m->layer_elems * wb, (size_t)m->cfg.max_seq * hd * wb, nkv, src, (size_t)len * hd * wb,
-      m->d_len, len);
+      m->d_len, len, m->prev_tok);
   m->launches++;
   NC_TRY(cudaGetLastError());
   for (int b = 0; b < n; ++b) m->lens[b] = len;

@@ -36,7 +36,8 @@ class NcConfig(ctypes.Structure):
                 ("n_layer", "d_model", "n_head", "n_kv_head", "head_dim", "d_mlp", "vocab")] + \
                [(n, ctypes.c_float) for n in ("rope_base", "softcap", "rms_eps")] + \
                [(n, ctypes.c_int32) for n in ("dtype", "max_batch", "max_seq", "window", "reserved")] + \
-               [("window_layers", ctypes.c_uint64)]
+               [("window_layers", ctypes.c_uint64)] + \
+               [(n, ctypes.c_int32) for n in ("extras", "ve_gate_channels", "smear_channels", "reserved2")]
 
 
 _lib = None
@@ -131,10 +132,14 @@ def make_config(shape, max_batch: int, max_seq: int) -> NcConfig:
     """nc_config from a shape object with the nc_inputs.ModelShape fields."""
     window = int(getattr(shape, "window", 0) or 0)
     pattern = getattr(shape, "window_pattern", "") or ""
+    extras = sum(bit for bit, flag in ((1, "value_embeds"), (2, "resid_lambdas"), (4, "smear"), (8, "backout"))
+                 if getattr(shape, flag, False))
     return NcConfig(shape.n_layer, shape.d_model, shape.n_head, shape.n_kv_head, shape.head_dim,
                     shape.d_mlp, shape.vocab, shape.rope_base, shape.softcap, shape.rms_eps,
                     DTYPES[shape.dtype], max_batch, max_seq,
-                    window if pattern else 0, 0, window_layers(pattern, shape.n_layer) if window else 0)
+                    window if pattern else 0, 0, window_layers(pattern, shape.n_layer) if window else 0,
+                    extras, int(getattr(shape, "ve_gate_channels", 32)), int(getattr(shape, "smear_channels", 24)),
+                    0)
 
 
 class Model:

@@ -90,6 +90,36 @@ typedef enum { NC_F32 = 0, NC_BF16 = 1, NC_FP8 = 2 } nc_dtype;
  *   max_batch / max_seq size the KV cache [n_layer][max_batch][n_kv_head][max_seq][head_dim]
  *   (K and V each) and the activation workspace (max_batch * max_seq rows).
  */
+/*
+ * Later-architecture extras (apidog.com/th "how nanochat works" item 1 and
+ * its list of automated improvements; parity-only features of a later
+ * version of the model).  Bits of nc_config.extras:
+ *   NC_EXTRA_VALUE_EMBED   layers 0, 2, 4, ... add 3 sigmoid(h[:C] G_l^T) VE_l[tok]
+ *                          to v per K/V head (h the block's normed input,
+ *                          C = ve_gate_channels)
+ *   NC_EXTRA_RESID_LAMBDAS before block l: x = resid_l x + x0_l x0, x0 the
+ *                          residual that enters block 0
+ *   NC_EXTRA_SMEAR         after the embedding norm: x_t += lambda
+ *                          sigmoid(x_t[:smear_channels] . w) x_{t-1}, x_{t-1}
+ *                          the previous token's normed embedding (none before
+ *                          a sequence's first token)
+ *   NC_EXTRA_BACKOUT       after the last block: x -= lambda x_mid, x_mid the
+ *                          residual after block n_layer / 2 - 1
+ * Their fp32 parameters follow Wu in the packed weights, in this order: the
+ * tables VE_l [vocab][n_kv_head * head_dim] of the even layers, then their
+ * gates G_l [n_kv_head][ve_gate_channels]; resid lambdas [n_layer], x0
+ * lambdas [n_layer]; the smear gate [smear_channels] and lambda [1]; the
+ * backout lambda [1] (each group present only when its bit is set).  Decode
+ * steps of such a model run the generic one-position pass.
+ */
+enum {
+  NC_EXTRA_VALUE_EMBED = 1,
+  NC_EXTRA_RESID_LAMBDAS = 2,
+  NC_EXTRA_SMEAR = 4,
+  NC_EXTRA_BACKOUT = 8,
+  NC_EXTRA_ALL = 15
+};
+
 typedef struct {
   int32_t n_layer, d_model, n_head, n_kv_head, head_dim, d_mlp, vocab;
   float rope_base, softcap, rms_eps;
@@ -98,6 +128,9 @@ typedef struct {
   int32_t window;          /* sliding window in positions; 0 = every layer sees its whole causal context */
   int32_t reserved;        /* 0 */
   uint64_t window_layers;  /* bit l set: layer l uses the sliding window (n_layer <= 64 when window > 0) */
+  int32_t extras;          /* NC_EXTRA_* bits; 0 = the base model */
+  int32_t ve_gate_channels, smear_channels;
+  int32_t reserved2;       /* 0 */
 } nc_config;
 
 typedef struct nc_model nc_model;
