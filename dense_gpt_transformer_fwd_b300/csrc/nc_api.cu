@@ -129,9 +129,14 @@ PtrKind ptr_kind(const void* p, int dev) {
 // last CUDA error this thread turned into NC_ERR_CUDA / NC_ERR_OOM
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
+// A failed allocation (or launch configuration) also stays in the runtime's
+// per-thread last-error slot, where the next cudaGetLastError() check of a
+// later call would find it: clear it here.  Sticky errors (a faulted
+// context) cannot be cleared this way and are reported again by later calls.
 nc_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return NC_OK;
   g_last_cuda_error = e;
+  cudaGetLastError();
   return e == cudaErrorMemoryAllocation ? NC_ERR_OOM : NC_ERR_CUDA;
 }
 

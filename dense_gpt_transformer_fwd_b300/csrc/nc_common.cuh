@@ -19,7 +19,6 @@ namespace nc {
 // bits of the device error word (reported by nc_sync_status)
 constexpr int NC_DEVFLAG_TOKEN = 1;     // a token id outside [0, vocab)
 constexpr int NC_DEVFLAG_TIMEOUT = 2;   // a bounded pipeline wait expired
-constexpr int NC_DEVFLAG_BOUNDS = 4;    // an index check failed (access skipped)
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ __nv_bfloat16 f2bf(float v) { return __float2bfloat16_rn(v); }

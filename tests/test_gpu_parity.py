@@ -250,6 +250,24 @@ def test_state_and_capacity_errors():
     m.close()
 
 
+def test_oom_reported_and_context_survives():
+    """A cache larger than the device (2^18 rows x 8192 positions x 128 bf16 =
+    512 GiB per tensor, the first large allocation) fails with NC_ERR_OOM,
+    frees what was allocated, and the next model still computes."""
+    sh = small_bf16_shape(n_layer=1, vocab=512)
+    w = nc_inputs.gen_weights(sh, 44)
+    free0 = torch.cuda.mem_get_info()[0]
+    with pytest.raises(ncp.NcError) as e:
+        ncp.Model(sh, w, max_batch=1 << 18, max_seq=8192)
+    assert e.value.name == "NC_ERR_OOM"
+    assert "memory" in str(e.value)
+    assert torch.cuda.mem_get_info()[0] >= free0 - (64 << 20)
+    tok = nc_inputs.gen_tokens(sh.vocab, (1, 12), 45)
+    m = ncp.Model(sh, w, max_batch=1, max_seq=12)
+    check_close(m.prefill(to_dev(tok)).cpu().numpy(), oracle_for(w, sh).prefill(tok), "bf16", "after OOM")
+    m.close()
+
+
 def test_bad_token_reported_by_sync():
     sh = small_bf16_shape(n_layer=1, vocab=512)
     m = ncp.Model(sh, nc_inputs.gen_weights(sh, 43), max_batch=1, max_seq=8)
