@@ -20,9 +20,15 @@
 // whole prompt; a later chunk continues each row's cache).  Per 128-key
 // block j:
 //   S_t   = Q_t K_j^T          tcgen05.mma M=128 N=128 K=128   (TMEM, fp32)
-//   P_t   = exp2(S_t * c - m)  softmax threads, bf16, into shared memory
-//   O_t  += P_t V_j            tcgen05.mma M=128 N=128 K=128   (TMEM, fp32)
-// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+//   P_t   = exp2(S_t * c - m)  softmax threads, bf16, back into TMEM over S_t
+//   O_t  += P_t V_j            tcgen05.mma M=128 N=128 K=128, A (= P_t) from
+//                              TMEM, B (= V_j^T) from shared memory
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512); P_t
+// takes the first 64 columns of S_t (two bf16 per column, row r in lane r)
+// once the softmax has read S_t.  Keeping P out of shared memory leaves the
+// P V product one shared-memory operand instead of two.  The tensor core
+// runs the MMAs one thread issues in issue order, so S_t(j+1), issued after
+// P_t(j) V_j, overwrites P_t(j) only after that product has read it.
 // The running max m is only raised when a block's max exceeds it by more
 // than 2^8 (in the exp2 domain); O and the running sum are then rescaled by
 // the same thread (it owns that TMEM lane).  The final O / l is exact either
@@ -38,7 +44,8 @@
 //
 // Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA
 // issuer, warps 2..5 softmax of tile A, warps 6..9 softmax of tile B (warp w
-// reads TMEM lanes 32*(w%4) .. +31, i.e. rows of its quarter).
+// reads TMEM lanes 32*(w%4) .. +31, i.e. rows of its quarter).  The shared
+// memory buffer of each tile stages its output for the TMA store.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // NC_DEVFLAG_TIMEOUT, lets its copies and MMAs drain, frees TMEM and returns.
 #pragma once
@@ -107,6 +114,27 @@ __device__ __forceinline__ uint32_t pack_bf16_2(float lo, float hi) {
   __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&t);
 }
+// D (TMEM) (+)= A B^T with A read from tensor memory (M = 128 lanes, K = 16:
+// 8 columns of bf16 pairs) and B from shared memory
+__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns, registers -> TMEM
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
 // byte address of bf16 element (row r, column c) of a 128 x 128 tile stored
 // as two K-major 128-byte-swizzled halves (columns 0..63, 64..127)
 __device__ __forceinline__ uint32_t atc_addr(uint32_t tile, int r, int c) {
@@ -175,6 +203,10 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     tma_prefetch_desc(&tmVt);
     tma_prefetch_desc(&tmO);
   }
+  // programmatic dependent of the QKV projection: wait for its results before
+  // taking tensor memory (see the GEMM kernel)
+  pdl_trigger();
+  pdl_wait();
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
@@ -248,13 +280,13 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
         tc_commit(bar(SFULL + t));
       };
       auto issue_pv = [&](int t, int j) {
-        const uint64_t dp = smem_desc_sw128(s0 + ATC_OFF_P + t * ATC_TILE);
+        // P_t in TMEM columns t*128 + 8kk .. +7 for keys 16kk .. 16kk+15
         const uint64_t dv = smem_desc_sw128(s0 + ATC_OFF_KV + ((2 * j + 1) % 3) * ATC_TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * ATC_HALF + (kk & 3) * 32;
-          tc_mma_f16(tmem_base + 256 + t * 128, desc_add(dp, off), desc_add(dv, off), idesc,
-                     (j | kk) != 0);
+          tc_mma_f16_tmem_a(tmem_base + 256 + t * 128, tmem_base + t * 128 + 8 * kk, desc_add(dv, off), idesc,
+                            (j | kk) != 0);
         }
         tc_commit(bar(PVDONE + t));
       };
@@ -349,19 +381,22 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
       // P_t of the previous block must have been consumed (and O_t written)
       if (j > 0 && !wait_warp(PVDONE + t, (j - 1) & 1)) { ok = false; break; }
       tc_fence_after();
-      // P = exp2(s * sl2 - m * sl2) in bf16, 8 columns (one 16-byte chunk) at
-      // a time straight into shared memory; row sum in 8 partial sums
+      // P = exp2(s * sl2 - m * sl2) in bf16, 32 columns at a time into the
+      // first half of the row's S_t columns (S_t has been read); row sum in 8
+      // partial sums
       float lk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 128; c += 8) {
-        float p[8];
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          p[i] = ex2_approx(fmaf(v[c + i], sl2, -mb));
-          lk[i] += p[i];
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(v[c + 2 * i], sl2, -mb));
+          const float p1 = ex2_approx(fmaf(v[c + 2 * i + 1], sl2, -mb));
+          lk[(2 * i) & 7] += p0;
+          lk[(2 * i + 1) & 7] += p1;
+          pk[i] = pack_bf16_2(p0, p1);
         }
-        st_shared_v4u(atc_addr(pbuf, r, c), pack_bf16_2(p[0], p[1]), pack_bf16_2(p[2], p[3]),
-                      pack_bf16_2(p[4], p[5]), pack_bf16_2(p[6], p[7]));
+        tmem_st16u(tS + (c >> 1), pk);
       }
       l += ((lk[0] + lk[1]) + (lk[2] + lk[3])) + ((lk[4] + lk[5]) + (lk[6] + lk[7]));
       // tcgen05.ld / tcgen05.st are warp-collective: the whole warp takes the
@@ -377,9 +412,8 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
           for (int i = 0; i < 32; ++i) o[i] *= f;
           tmem_st32(tO + c, o);
         }
-        tmem_wait_st();
       }
-      fence_async_smem();                           // P visible to the tensor core
+      tmem_wait_st();                               // P (and a rescaled O) written
       tc_fence_before();
       mbar_arrive(bar(PFULL + t));
     }

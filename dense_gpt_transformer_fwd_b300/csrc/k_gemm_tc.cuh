@@ -59,6 +59,20 @@ struct GemmArgs {
   float eps;
   // EPI_LOGITS
   float softcap;
+  // RMSNorm folded into the projections (the identity (r x) W^T = r (x W^T)):
+  // with row_ss, the A operand holds bf16(x) unnormalised and the consumer
+  // epilogues (EPI_QKV, EPI_RELU2, EPI_LOGITS) scale accumulator row m by
+  // r_m = rsqrt(sum_t row_ss[t * ss_ld + m] * inv_d + eps), the sums of
+  // squares of x's 128-column blocks t < ss_blocks.  With h_out, EPI_RESID
+  // reads x (x_in, [M][N] fp32), stores x + acc by TMA, and writes bf16(x + acc)
+  // to h_out ([M][N]) and each row's sum of squares over every 128-column
+  // block to ss_out[block * ss_ld + m].
+  const float* row_ss;
+  int ss_blocks, ss_ld;
+  float inv_d;
+  const float* x_in;
+  __nv_bfloat16* h_out;
+  float* ss_out;
   // tile order: 0 = m fastest (CTAs running together share a W tile),
   // 1 = n fastest (they share an A panel, each read from DRAM once)
   int n_fast;
@@ -244,6 +258,12 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
   }
+  // Launched as a programmatic dependent of the previous kernel: every
+  // thread waits for that kernel's results here, after the set-up above and
+  // before taking tensor memory, so that a CTA waiting here never holds TMEM
+  // a CTA of the previous kernel on the same SM may still need.
+  pdl_trigger();
+  pdl_wait();
   if constexpr (PAIR) {
     // the peer's barriers are initialised before any remote arrive or copy
     __syncthreads();
@@ -400,16 +420,111 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
       const int row0 = m0 + 32 * q;                 // first row of this warp
       const int my_row = row0 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc * BN + ch0;
+      // folded RMSNorm: this row's 1 / rms(x)
+      float rscale = 1.f;
+      if (args.row_ss != nullptr) {
+        const float* ssr = args.row_ss + (my_row < args.M ? my_row : args.M - 1);
+        float t = 0.f;
+        for (int bi = 0; bi < args.ss_blocks; ++bi) t += __ldcg(ssr + (size_t)bi * args.ss_ld);
+        rscale = rsqrtf(t * args.inv_d + args.eps);
+      }
 
-      if constexpr (EPI == EPI_LOGITS || EPI == EPI_STORE || EPI == EPI_RESID) {
+      if constexpr (EPI == EPI_RESID) {
+        if (args.h_out != nullptr) {
+          // x = x + acc, read here and stored by TMA; bf16(x) and the row's
+          // sum of squares over this warp's 128 columns for the next norm.
+          // 32 columns per chunk.  x is read coalesced (8 lanes per 128-byte
+          // row, 4 rows per load) one chunk ahead, staged in the swizzled
+          // buffer, and read back one row per lane, where the sum is formed
+          // in place; bf16(x) is read from there in the coalesced layout
+          // again and stored, and the TMA stores the fp32 x.
+          static_assert(HALF == 128, "one 128-column norm block per warp");
+          const bool row_ok = my_row < args.M;
+          const int lr = lane >> 3, lp = lane & 7;      // coalesced role: row 4i + lr, 16-byte piece lp
+          const float* xw = args.x_in + (size_t)n0 + ch0 + 4 * lp;
+          auto load_x = [&](int c, float4 (&xv)[8]) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = row0 + 4 * i + lr;
+              xv[i] = r < args.M ? *reinterpret_cast<const float4*>(xw + (size_t)r * args.N + c)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          };
+          __nv_bfloat16* hw = args.h_out + (size_t)n0 + ch0 + 4 * lp;
+          float4 xc[8], xn[8];
+          load_x(0, xc);
+          float ss = 0.f;
+#pragma unroll
+          for (int c = 0; c < HALF; c += 32) {
+            if (c + 32 < HALF) load_x(c + 32, xn);
+            float v[32];
+            tmem_ld32(taddr + c, v);
+            if (lane == 0) bulk_wait_read<0>();     // the previous store has read the buffer
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) st_shared_v4(ep_addr(buf0, 4 * i + lr, lp), xc[i].x, xc[i].y, xc[i].z, xc[i].w);
+            __syncwarp();
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+              const float4 t = ld_shared_v4(ep_addr(buf0, lane, cc));
+              v[4 * cc] += t.x;
+              v[4 * cc + 1] += t.y;
+              v[4 * cc + 2] += t.z;
+              v[4 * cc + 3] += t.w;
+              st_shared_v4(ep_addr(buf0, lane, cc), v[4 * cc], v[4 * cc + 1], v[4 * cc + 2], v[4 * cc + 3]);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = row0 + 4 * i + lr;
+              const float4 t = ld_shared_v4(ep_addr(buf0, 4 * i + lr, lp));
+              if (r < args.M)
+                *reinterpret_cast<uint2*>(hw + (size_t)r * args.N + c) =
+                    make_uint2(pack_bf16x2(t.x, t.y), pack_bf16x2(t.z, t.w));
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, buf0, n0 + ch0 + c, row0);
+              bulk_commit();
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+            if (c + 32 < HALF) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) xc[i] = xn[i];
+            }
+          }
+          if (row_ok) args.ss_out[(size_t)((n0 + ch0) >> 7) * args.ss_ld + my_row] = ss;
+        } else {
+          // x += acc as a TMA reduce-add in L2 (x is not read into the SM)
+#pragma unroll 1
+          for (int c = 0; c < HALF; c += 32) {
+            float v[32];
+            tmem_ld32(taddr + c, v);
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+              st_shared_v4(ep_addr(buf0, lane, cc), v[4 * cc], v[4 * cc + 1], v[4 * cc + 2], v[4 * cc + 3]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_2d(&tmC, buf0, n0 + ch0 + c, row0);
+              bulk_commit();
+            }
+          }
+        }
+      } else if constexpr (EPI == EPI_LOGITS || EPI == EPI_STORE) {
         // 32 fp32 columns per chunk
+        const float sc = inv_cap * rscale;
 #pragma unroll 1
         for (int c = 0; c < HALF; c += 32) {
           float v[32];
           tmem_ld32(taddr + c, v);
           if constexpr (EPI == EPI_LOGITS) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = softcap_f(v[j], inv_cap, args.softcap);
+            for (int j = 0; j < 32; ++j) v[j] = args.softcap * tanh_approx(v[j] * sc);
           }
           if (lane == 0) bulk_wait_read<0>();       // the previous store has read the buffer
           __syncwarp();
@@ -419,10 +534,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if constexpr (EPI == EPI_RESID)
-              tma_reduce_add_2d(&tmC, buf0, n0 + ch0 + c, row0);
-            else
-              tma_store_2d(&tmC, buf0, n0 + ch0 + c, row0);
+            tma_store_2d(&tmC, buf0, n0 + ch0 + c, row0);
             bulk_commit();
           }
         }
@@ -436,8 +548,9 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
           uint32_t w[32];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float a0 = fmaxf(v0[2 * j], 0.f), a1 = fmaxf(v0[2 * j + 1], 0.f);
-            const float b0 = fmaxf(v1[2 * j], 0.f), b1 = fmaxf(v1[2 * j + 1], 0.f);
+            // relu(r z)^2 with the row's norm scale r > 0
+            const float a0 = fmaxf(v0[2 * j] * rscale, 0.f), a1 = fmaxf(v0[2 * j + 1] * rscale, 0.f);
+            const float b0 = fmaxf(v1[2 * j] * rscale, 0.f), b1 = fmaxf(v1[2 * j + 1] * rscale, 0.f);
             w[j] = pack_bf16x2(a0 * a0, a1 * a1);
             w[16 + j] = pack_bf16x2(b0 * b0, b1 * b1);
           }
@@ -486,7 +599,9 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
               rs[j] = __ldg(args.rope_sin_t + (size_t)(c + j) * args.cache_S + pos_c);
             }
           };
-          float scale = 1.f;
+          // the row's norm scale r, then for q and k heads the QK-norm of
+          // r * acc: r * rsqrt(r^2 mean(acc^2) + eps)
+          float scale = rscale;
           if (!is_v) {
             load_rope(0);
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -497,7 +612,8 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) s4[j & 3] = fmaf(v[j], v[j], s4[j & 3]);
             }
-            scale = rsqrtf(((s4[0] + s4[1]) + (s4[2] + s4[3])) * (1.f / 128.f) + args.eps);
+            const float ms = ((s4[0] + s4[1]) + (s4[2] + s4[3])) * (1.f / 128.f);
+            scale = rscale * rsqrtf(rscale * rscale * ms + args.eps);
           }
           if (lane == 0) bulk_wait_read<0>();       // both buffers free
           __syncwarp();
@@ -513,6 +629,12 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
                 const float x0 = a[j] * scale, x1 = bb[j] * scale;
                 a[j] = x0 * rc[j] - x1 * rs[j];
                 bb[j] = x0 * rs[j] + x1 * rc[j];
+              }
+            } else if (args.row_ss != nullptr) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                a[j] *= scale;
+                bb[j] *= scale;
               }
             }
             if (is_v && args.vt != nullptr && my_row < args.M) {

@@ -99,6 +99,27 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, TA* __restrict__ h, 
   for (int j = lane; j < d; j += 32) hr[j] = from_f<TA>(xr[j] * r);
 }
 
+// Last position of each row with the RMSNorm folded into the unembedding:
+// h_out[i] = h[src(i)] and ss_out[t * ss_ld_out + i] = ss[t * ss_ld + src(i)]
+// for the n_ss column blocks t, src(i) = i * stride + last[i].  A copy of what
+// the last residual epilogue wrote, so the last-position logits are the same
+// bits as the all-position ones.  One warp per row, 16-byte copies (d a
+// multiple of 8).
+template <typename TA>
+__global__ void gather_last_kernel(const TA* __restrict__ h, const float* __restrict__ ss, int ss_ld, int n_ss,
+                                   TA* __restrict__ h_out, float* __restrict__ ss_out, int ss_ld_out, int rows,
+                                   int d, int stride, const int* __restrict__ last) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
+  if (warp >= rows) return;
+  const int src = warp * stride + last[warp];
+  const uint4* hs = reinterpret_cast<const uint4*>(h + (size_t)src * d);
+  uint4* hd = reinterpret_cast<uint4*>(h_out + (size_t)warp * d);
+  for (int j = lane; j < d * (int)sizeof(TA) / 16; j += 32) hd[j] = hs[j];
+  for (int t = lane; t < n_ss; t += 32) ss_out[(size_t)t * ss_ld_out + warp] = ss[(size_t)t * ss_ld + src];
+}
+
 // fp32 SIMT GEMM, C = A W^T with an elementwise epilogue.  64x64 tile per
 // 256-thread block, 4x4 outputs per thread.
 enum SimtEpi : int { SEPI_STORE = 0, SEPI_RESID = 1, SEPI_RELU2 = 2, SEPI_LOGITS = 3 };

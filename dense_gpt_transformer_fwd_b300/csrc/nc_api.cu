@@ -234,6 +234,7 @@ struct nc_model {
   float* c32 = nullptr;                // fp32 path: raw QKV [max_rows][(n_head+2)*hd]
   void* h_last = nullptr;              // [max_batch][d]
   float* ss_part = nullptr;            // decode: [d / 128][max_batch] per-block sums of squares of x
+  float* ss_rows = nullptr;            // prefill (16-bit models): [d / 128][max_rows] the same per row
   int32_t* tok_stage = nullptr;
   float* logit_stage = nullptr;
   size_t logit_stage_bytes = 0;
@@ -315,7 +316,7 @@ void free_model(nc_model* m) {
   void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->rope_cos_t, m->rope_sin_t, m->d_tm_kv,
                   m->k_alloc, m->v_alloc, m->x,
                   m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
-                  m->tok_stage, m->logit_stage, m->err, m->vt, m->d_len, m->d_pos0, m->d_last, m->ss_part,
+                  m->tok_stage, m->logit_stage, m->err, m->vt, m->d_len, m->d_pos0, m->d_last, m->ss_part, m->ss_rows,
                   m->w8, m->ex_params, m->x0, m->x_mid, m->prev_tok};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -494,13 +495,15 @@ cudaError_t launch_gemm_cl(nc_model* m, const CUtensorMap& ta, const CUtensorMap
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, EPI, CL>, ta, tb, tc, a);
   m->launches++;
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -515,9 +518,10 @@ cudaError_t launch_gemm_tc(nc_model* m, const CUtensorMap& ta, const CUtensorMap
   using C = TcCfg<BN, EPI, 0>;
   const int tiles = num_m * num_n;
   const int grid = tiles < m->num_sms ? tiles : m->num_sms;
-  gemm_tc_kernel<BN, EPI, 0><<<grid, C::THREADS, C::SMEM, s>>>(ta, tb, tc, a);
+  const cudaError_t e = launch_k(true, gemm_tc_kernel<BN, EPI, 0>, dim3(grid), dim3(C::THREADS), C::SMEM, s, ta, tb,
+                                 tc, a);
   m->launches++;
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // K split for a decode-step GEMM with `tiles` weight tiles and `kb` 64-wide
@@ -603,6 +607,27 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
   const bool bf = m->bf16;
   const int* pos0 = decode ? m->d_len : m->d_pos0;    // [B] first position of each row's tokens
   using bf16 = __nv_bfloat16;
+  // 16-bit models without the extras fold the RMSNorms into the projections:
+  // the embedding kernel and every residual epilogue write h = bf16(x) and
+  // the per-128-column sums of squares of x (ss_rows, [d/128][M]), and the
+  // next projection scales its rows by 1/rms(x), the unembedding included
+  // (last_only: each row's last position of h and its sums are gathered
+  // first).  A decode step on this path keeps its final norm kernel, which
+  // also advances the rows' lengths.
+  const bool fold = bf && !m->extras;
+  const bool fold_final = fold && !decode;
+  auto fold_in = [&](GemmArgs& a) {
+    a.row_ss = m->ss_rows;
+    a.ss_blocks = d / 128;
+    a.ss_ld = M;
+    a.inv_d = 1.f / (float)d;
+  };
+  auto fold_out = [&](GemmArgs& a) {
+    a.x_in = m->x;
+    a.h_out = static_cast<bf16*>(m->h);
+    a.ss_out = m->ss_rows;
+    a.ss_ld = M;
+  };
 
   CUtensorMap tm_qa[2];  // q and att viewed as [B][T][n_head*128], box 64 x 128 rows
   if (bf && T > 1) {
@@ -617,7 +642,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
     if (bf)
       embed_rmsnorm_kernel<bf16, bf16><<<blocks_for_warps(M), 256, 0, s>>>(
           tok, static_cast<const bf16*>(m->E), m->x, static_cast<bf16*>(m->h), M, d, V, eps, m->err,
-          (float*)nullptr, 0);
+          fold ? m->ss_rows : (float*)nullptr, M);
     else
       embed_rmsnorm_kernel<float, float><<<blocks_for_warps(M), 256, 0, s>>>(
           tok, static_cast<const float*>(m->E), m->x, static_cast<float*>(m->h), M, d, V, eps, m->err,
@@ -700,6 +725,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
           a.vt = static_cast<bf16*>(m->vt);
           a.vt_S = m->vt_S;
         }
+        if (fold) fold_in(a);
         NC_TRY((launch_gemm_tc<256, EPI_QKV>(m, m->tm_h, m->tm_w128[4 * l + 0], m->tm_q_st, a, s, kPrefillCluster)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_STORE>(m, static_cast<const float*>(m->h),
@@ -743,8 +769,8 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
         aa.err = m->err;
         aa.wait_limit_ns = m->wait_limit_ns;
         // CTAs: query tiles x rows x K/V heads x head pairs of a group
-        attn_prefill_tc_kernel<<<aa.n_qt * B * nkv * ((nh / nkv + 1) / 2), ATC_THREADS, ATC_SMEM, s>>>(
-            tm_qa[0], m->tm_kc[l], m->tm_vt, tm_qa[1], aa);
+        NC_TRY(launch_k(true, attn_prefill_tc_kernel, dim3(aa.n_qt * B * nkv * ((nh / nkv + 1) / 2)),
+                        dim3(ATC_THREADS), ATC_SMEM, s, tm_qa[0], m->tm_kc[l], m->tm_vt, tm_qa[1], aa));
         m->launches++;
         NC_TRY(cudaGetLastError());
       } else if (bf) {
@@ -770,13 +796,14 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
       KScope ks(m, NC_K_OPROJ, s);
       if (bf) {
         GemmArgs a = base_args(m, M, d, NQ);
+        if (fold) fold_out(a);
         NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_att, m->tm_w128[4 * l + 1], m->tm_x_st, a, s, kPrefillCluster)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->att),
                                             static_cast<const float*>(m->wo[l]), m->x, M, d, NQ, d, s));
       }
     }
-    {  // h = rms(x)
+    if (!fold) {  // h = rms(x)
       KScope ks(m, NC_K_NORM, s);
       if (bf)
         rmsnorm_kernel<bf16><<<blocks_for_warps(M), 256, 0, s>>>(m->x, static_cast<bf16*>(m->h), M, d, 1,
@@ -791,6 +818,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
       KScope ks(m, NC_K_FC, s);
       if (bf) {
         GemmArgs a = base_args(m, M, F, d);
+        if (fold) fold_in(a);
         NC_TRY((launch_gemm_tc<256, EPI_RELU2>(m, m->tm_h, m->tm_w128[4 * l + 2], m->tm_u_st, a, s, kPrefillCluster)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RELU2>(m, static_cast<const float*>(m->h),
@@ -802,6 +830,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
       KScope ks(m, NC_K_PROJ, s);
       if (bf) {
         GemmArgs a = base_args(m, M, d, F);
+        if (fold) fold_out(a);
         NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_u, m->tm_w128[4 * l + 3], m->tm_x_st, a, s, kPrefillCluster)));
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->u),
@@ -819,7 +848,17 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
         NC_TRY(cudaGetLastError());
       }
     }
-    {  // h = rms(x): next block's pre-attention norm, or the final norm
+    if (fold_final && last_only && l == c.n_layer - 1) {
+      // the last position of each row: bf16(x) and its sums of squares
+      KScope ks(m, NC_K_NORM, s);
+      gather_last_kernel<bf16><<<blocks_for_warps(B), 256, 0, s>>>(
+          static_cast<const bf16*>(m->h), m->ss_rows, M, d / 128, static_cast<bf16*>(m->h_last), m->ss_part, B, B,
+          d, T, m->d_last);
+      m->launches++;
+      NC_TRY(cudaGetLastError());
+    }
+    if (!fold || (l == c.n_layer - 1 && !fold_final)) {
+      // h = rms(x): next block's pre-attention norm, or the final norm
       KScope ks(m, NC_K_NORM, s);
       const bool final_last = last_only && l == c.n_layer - 1;
       const int rows = final_last ? B : M;
@@ -842,6 +881,13 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
     KScope ks(m, NC_K_LMHEAD, s);
     if (bf) {
       GemmArgs a = base_args(m, out_rows, V, d);
+      if (fold_final) {
+        fold_in(a);
+        if (last_only) {
+          a.row_ss = m->ss_part;
+          a.ss_ld = B;
+        }
+      }
       CUtensorMap tm_out;
       if (!make_tmap(&tm_out, logits, out_rows, V, 32, true)) return NC_ERR_INVALID_ARG;
       NC_TRY((launch_gemm_tc<256, EPI_LOGITS>(m, last_only ? m->tm_hlast : m->tm_h, m->tm_wu128, tm_out, a, s, kPrefillCluster)));
@@ -1384,7 +1430,9 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   CREATE_TRY(cudaMalloc(&m->att, R * NQ * m->wbytes));
   CREATE_TRY(cudaMalloc(&m->u, R * F * m->wbytes));
   CREATE_TRY(cudaMalloc(&m->h_last, (int64_t)c.max_batch * d * m->wbytes));
-  CREATE_TRY(cudaMalloc(&m->ss_part, (int64_t)(d / 128 + 1) * c.max_batch * 4));
+  // (decode: [d/128 + 1][max_batch]; a last-position prefill gathers up to d/96 blocks)
+  CREATE_TRY(cudaMalloc(&m->ss_part, (int64_t)(d / 64 + 1) * c.max_batch * 4));
+  if (m->bf16) CREATE_TRY(cudaMalloc(&m->ss_rows, (d / 128) * R * 4));
   if (!m->bf16) CREATE_TRY(cudaMalloc(&m->c32, R * NQKV * 4));
   CREATE_TRY(cudaMalloc(&m->tok_stage, R * 4));
   if (m->extras & NC_EXTRA_RESID_LAMBDAS) CREATE_TRY(cudaMalloc(&m->x0, R * d * 4));
