@@ -63,10 +63,10 @@ struct GemmArgs {
   // with row_ss, the A operand holds bf16(x) unnormalised and the consumer
   // epilogues (EPI_QKV, EPI_RELU2, EPI_LOGITS) scale accumulator row m by
   // r_m = rsqrt(sum_t row_ss[t * ss_ld + m] * inv_d + eps), the sums of
-  // squares of x's 128-column blocks t < ss_blocks.  With h_out, EPI_RESID
-  // reads x (x_in, [M][N] fp32), stores x + acc by TMA, and writes bf16(x + acc)
-  // to h_out ([M][N]) and each row's sum of squares over every 128-column
-  // block to ss_out[block * ss_ld + m].
+  // squares of x's column blocks t < ss_blocks.  With h_out, EPI_RESID reads
+  // x (x_in, [M][N] fp32), stores x + acc by TMA, and writes bf16(x + acc) to
+  // h_out ([M][N]) and each row's sum of squares over every block of BN / 2
+  // columns to ss_out[block * ss_ld + m].
   const float* row_ss;
   int ss_blocks, ss_ld;
   float inv_d;
@@ -102,7 +102,11 @@ struct TcCfg {
   static constexpr size_t SMEM_CAP = 232448 - 1024 - 256;
   static constexpr int STAGES_FIT = (int)((SMEM_CAP - EP_TOTAL) / STAGE_BYTES);
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+  // two accumulators of BN columns, allocated as a power of two (>= 32)
+  static constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+  static_assert(BN % 32 == 0 && 2 * BN <= 512, "two accumulators must fit tensor memory");
+  static_assert(EPI != EPI_QKV || BN % 256 == 0, "the QKV epilogue takes whole heads per warp");
+  static_assert(EPI != EPI_RELU2 || BN % 128 == 0, "the ReLU^2 epilogue works in 64-column chunks");
   static constexpr size_t SMEM = 1024 + STAGES * (size_t)STAGE_BYTES + EP_TOTAL + 256;
   static_assert(STAGES >= 2, "shared memory too small for the pipeline");
   static_assert(SMEM <= 232448, "shared memory over the sm_103a per-block limit");
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
           // buffer, and read back one row per lane, where the sum is formed
           // in place; bf16(x) is read from there in the coalesced layout
           // again and stored, and the TMA stores the fp32 x.
-          static_assert(HALF == 128, "one 128-column norm block per warp");
+          // this warp's columns are one norm block of HALF columns
           const bool row_ok = my_row < args.M;
           const int lr = lane >> 3, lp = lane & 7;      // coalesced role: row 4i + lr, 16-byte piece lp
           const float* xw = args.x_in + (size_t)n0 + ch0 + 4 * lp;
@@ -495,7 +499,7 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
               for (int i = 0; i < 8; ++i) xc[i] = xn[i];
             }
           }
-          if (row_ok) args.ss_out[(size_t)((n0 + ch0) >> 7) * args.ss_ld + my_row] = ss;
+          if (row_ok) args.ss_out[(size_t)((n0 + ch0) / HALF) * args.ss_ld + my_row] = ss;
         } else {
           // x += acc as a TMA reduce-add in L2 (x is not read into the SM)
 #pragma unroll 1

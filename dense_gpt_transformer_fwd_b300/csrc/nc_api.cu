@@ -234,7 +234,8 @@ struct nc_model {
   float* c32 = nullptr;                // fp32 path: raw QKV [max_rows][(n_head+2)*hd]
   void* h_last = nullptr;              // [max_batch][d]
   float* ss_part = nullptr;            // decode: [d / 128][max_batch] per-block sums of squares of x
-  float* ss_rows = nullptr;            // prefill (16-bit models): [d / 128][max_rows] the same per row
+  float* ss_rows = nullptr;            // prefill (16-bit models): [d / 96 at most][max_rows] the same per
+                                       // row, over blocks of 128 or 96 columns
   int32_t* tok_stage = nullptr;
   float* logit_stage = nullptr;
   size_t logit_stage_bytes = 0;
@@ -262,6 +263,8 @@ struct nc_model {
   int sk_nb = 0;                       // padded batch of the MMA N operand: 32, 64 or 128 (0 = off)
   int sk_splits[4] = {1, 1, 1, 1};     // K splits of QKV, O-proj, FC, PROJ
   std::vector<CUtensorMap> tm_w128;    // per layer Wqkv, Wo, Wfc, Wproj, box 64 x 128 rows
+  std::vector<CUtensorMap> tm_w96;     // per layer Wo, Wproj, box 64 x 96 rows (192-wide residual tiles;
+                                       // empty unless d_model % 192 == 0)
   CUtensorMap tm_wu128{};
   // FP8 models: the projection weights as E4M3 bytes (per layer Wqkv, Wo, Wfc,
   // Wproj, then Wu), one power-of-two scale per matrix, and their tensor maps
@@ -567,6 +570,19 @@ int layer_window(const nc_model* m, int l) {
   return (c.window > 0 && l < 64 && ((c.window_layers >> l) & 1ull)) ? c.window : 0;
 }
 
+// Tile width of a residual projection (N = d_model columns) on CTA pairs:
+// 192 where weight maps for it exist and it finishes in fewer column-time
+// units, i.e. ceil(units / pairs) * BN is smaller (the last wave of 256-wide
+// tiles can leave most pairs idle: d_model 1536 at 16384 rows is 384 units
+// of 256 on 74 pairs, 5.2 waves, against 512 units of 192, 6.9 waves).
+int resid_bn(const nc_model* m, int M, int N) {
+  const int num_m = (M + 127) / 128;
+  if (m->tm_w96.empty() || N % 192 || num_m < 2) return 256;
+  const int pairs = m->num_sms / 2, m2 = (num_m + 1) / 2;
+  auto cost = [&](int bn) { return (int64_t)((m2 * (N / bn) + pairs - 1) / pairs) * bn; };
+  return cost(192) < cost(256) ? 192 : 256;
+}
+
 GemmArgs base_args(nc_model* m, int M, int N, int K) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -616,9 +632,10 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
   // also advances the rows' lengths.
   const bool fold = bf && !m->extras;
   const bool fold_final = fold && !decode;
+  int ss_w = 128;                     // columns per sum-of-squares block of the last writer of h
   auto fold_in = [&](GemmArgs& a) {
     a.row_ss = m->ss_rows;
-    a.ss_blocks = d / 128;
+    a.ss_blocks = d / ss_w;
     a.ss_ld = M;
     a.inv_d = 1.f / (float)d;
   };
@@ -797,7 +814,13 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
       if (bf) {
         GemmArgs a = base_args(m, M, d, NQ);
         if (fold) fold_out(a);
-        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_att, m->tm_w128[4 * l + 1], m->tm_x_st, a, s, kPrefillCluster)));
+        if (resid_bn(m, M, d) == 192) {
+          NC_TRY((launch_gemm_tc<192, EPI_RESID>(m, m->tm_att, m->tm_w96[2 * l + 0], m->tm_x_st, a, s, kPrefillCluster)));
+          ss_w = 96;
+        } else {
+          NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_att, m->tm_w128[4 * l + 1], m->tm_x_st, a, s, kPrefillCluster)));
+          ss_w = 128;
+        }
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->att),
                                             static_cast<const float*>(m->wo[l]), m->x, M, d, NQ, d, s));
@@ -831,7 +854,13 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
       if (bf) {
         GemmArgs a = base_args(m, M, d, F);
         if (fold) fold_out(a);
-        NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_u, m->tm_w128[4 * l + 3], m->tm_x_st, a, s, kPrefillCluster)));
+        if (resid_bn(m, M, d) == 192) {
+          NC_TRY((launch_gemm_tc<192, EPI_RESID>(m, m->tm_u, m->tm_w96[2 * l + 1], m->tm_x_st, a, s, kPrefillCluster)));
+          ss_w = 96;
+        } else {
+          NC_TRY((launch_gemm_tc<256, EPI_RESID>(m, m->tm_u, m->tm_w128[4 * l + 3], m->tm_x_st, a, s, kPrefillCluster)));
+          ss_w = 128;
+        }
       } else {
         NC_TRY(launch_simt_gemm<SEPI_RESID>(m, static_cast<const float*>(m->u),
                                             static_cast<const float*>(m->wproj[l]), m->x, M, d, F, d, s));
@@ -852,7 +881,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
       // the last position of each row: bf16(x) and its sums of squares
       KScope ks(m, NC_K_NORM, s);
       gather_last_kernel<bf16><<<blocks_for_warps(B), 256, 0, s>>>(
-          static_cast<const bf16*>(m->h), m->ss_rows, M, d / 128, static_cast<bf16*>(m->h_last), m->ss_part, B, B,
+          static_cast<const bf16*>(m->h), m->ss_rows, M, d / ss_w, static_cast<bf16*>(m->h_last), m->ss_part, B, B,
           d, T, m->d_last);
       m->launches++;
       NC_TRY(cudaGetLastError());
@@ -1052,7 +1081,10 @@ nc_status forward_decode_nb(nc_model* m, const DecodeBufs& db, const int32_t* to
 template <int EPI>
 cudaError_t configure_gemm_tc() {
   cudaError_t e = set_gemm_smem<256, EPI, 0>();
-  return e != cudaSuccess ? e : set_gemm_smem<256, EPI, 2>();
+  if (e == cudaSuccess) e = set_gemm_smem<256, EPI, 2>();
+  if (e == cudaSuccess && EPI == EPI_RESID) e = set_gemm_smem<192, EPI_RESID, 0>();
+  if (e == cudaSuccess && EPI == EPI_RESID) e = set_gemm_smem<192, EPI_RESID, 2>();
+  return e;
 }
 template <int NB, bool FP8>
 cudaError_t configure_skinny() {
@@ -1432,7 +1464,7 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
   CREATE_TRY(cudaMalloc(&m->h_last, (int64_t)c.max_batch * d * m->wbytes));
   // (decode: [d/128 + 1][max_batch]; a last-position prefill gathers up to d/96 blocks)
   CREATE_TRY(cudaMalloc(&m->ss_part, (int64_t)(d / 64 + 1) * c.max_batch * 4));
-  if (m->bf16) CREATE_TRY(cudaMalloc(&m->ss_rows, (d / 128) * R * 4));
+  if (m->bf16) CREATE_TRY(cudaMalloc(&m->ss_rows, (d / 64) * R * 4));
   if (!m->bf16) CREATE_TRY(cudaMalloc(&m->c32, R * NQKV * 4));
   CREATE_TRY(cudaMalloc(&m->tok_stage, R * 4));
   if (m->extras & NC_EXTRA_RESID_LAMBDAS) CREATE_TRY(cudaMalloc(&m->x0, R * d * 4));
@@ -1516,6 +1548,12 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
            make_tmap(&m->tm_w128[4 * l + 1], m->wo[l], d, NQ, 128) &&
            make_tmap(&m->tm_w128[4 * l + 2], m->wfc[l], F, d, 128) &&
            make_tmap(&m->tm_w128[4 * l + 3], m->wproj[l], d, F, 128);
+    if (ok && d % 192 == 0) {
+      m->tm_w96.resize(2 * c.n_layer);
+      for (int l = 0; ok && l < c.n_layer; ++l)
+        ok = make_tmap(&m->tm_w96[2 * l + 0], m->wo[l], d, NQ, 96) &&
+             make_tmap(&m->tm_w96[2 * l + 1], m->wproj[l], d, F, 96);
+    }
     if (ok && m->fp8) {
       // E4M3 matrices in the order quantize_fp8_weights wrote them
       m->tm_w8.resize(4 * c.n_layer + 1);
