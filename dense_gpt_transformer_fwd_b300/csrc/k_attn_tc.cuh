@@ -11,10 +11,13 @@
 // head h reads K/V head h / G, G = n_head / n_kv (G = n_head is multi-query
 // attention), and a layer with a window sees only the last `window` keys.
 //
-// One CTA = one batch row, one tile of 128 query positions and TWO query
-// heads of one K/V group (tiles "A" and "B"), which share every K and V tile
-// it loads (with G odd, the last pair of a group repeats its one head in tile
-// B and does not store it).  The
+// One work item = one batch row, one tile of 128 query positions and TWO
+// query heads of one K/V group (tiles "A" and "B"), which share every K and V
+// tile it loads (with G odd, the last pair of a group repeats its one head in
+// tile B and does not store it).  The kernel is persistent: one CTA per SM
+// runs its items one after another with the same barriers, tensor memory and
+// K/V ring, and loads the next item's queries while the current item's last
+// products run.  The
 // queries of row b of a prefill chunk sit at positions p0 .. p0 + T - 1,
 // p0 = pos0[b], and read the keys 0 .. p0 + T - 1 of the cache (p0 = 0 for a
 // whole prompt; a later chunk continues each row's cache).  Per 128-key
@@ -141,6 +144,27 @@ __device__ __forceinline__ uint32_t atc_addr(uint32_t tile, int r, int c) {
   return tile + (c >> 6) * ATC_HALF + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2;
 }
 
+// bar.red.or over the `n` threads of named barrier `id`: every thread gets
+// the OR of the predicates (a barrier like bar.sync)
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// One work item: a batch row, a tile of 128 query positions and a pair of
+// query heads of one K/V group.
+struct AtcItem {
+  int b, h0, h1, bkv, q0, qpos0, jfirst, nb;
+};
+
 __global__ void __launch_bounds__(ATC_THREADS, 1)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,   // q   [B][T][NQ]
                            const __grid_constant__ CUtensorMap tmK,   // K   [B_max][S][128]
@@ -151,38 +175,51 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(atc_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s0 = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ATC_OFF_BAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   auto bar = [&](int i) { return smem_u32(bars + i); };
   // barrier indices
   const int QFULL = 0, KVFULL = 1, KVFREE = 4, SFULL = 7, SFREE = 9, PFULL = 11, PVDONE = 13,
-            DRAIN = 15;
+            DRAIN = 15, QFREE = 16;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.n_head / args.n_kv;             // query heads per K/V head
   const int pg_n = (G + 1) >> 1;                     // head pairs per group
   const int pairs = args.n_kv * pg_n;
-  // heavy query tiles first: item -> (query tile, batch row, K/V group, pair)
   const int per_qt = args.B * pairs;
-  const int qt = args.n_qt - 1 - (int)(blockIdx.x / per_qt);
-  const int rest = (int)(blockIdx.x % per_qt);
-  const int b = rest / pairs, hp = rest % pairs;
-  const int g = hp / pg_n;
-  const int h0 = g * G + 2 * (hp % pg_n);            // tile A's head
-  const int h1 = min(h0 + 1, g * G + G - 1);         // tile B's head (== h0: not stored)
-  const int bkv = b * args.n_kv + g;                 // K/V cache sequence of this CTA
-  const int q0 = qt * 128;
-  // query row r sits at position qpos0 + r and sees keys max(0, qpos0 + r -
-  // window + 1) .. qpos0 + r; the keys of the cache end at pos0 + T - 1
-  const int p0 = args.pos0[b];
-  const int qpos0 = p0 + q0;
-  const int last_key = min(qpos0 + 127, p0 + args.T - 1);
-  const int jfirst = args.window > 0 ? max(0, qpos0 - args.window + 1) / 128 : 0;
-  const int nb = last_key / 128 + 1 - jfirst;        // key blocks jfirst .. jfirst + nb - 1
+  const int n_items = args.n_qt * per_qt;
   const uint64_t limit = args.wait_limit_ns;
+  // Persistent: CTA c takes the items of rounds k = 0, 1, ...: item
+  // k * grid + c, or k * grid + grid - 1 - c in odd rounds (heavy query tiles
+  // come first, so the snake order evens out the key blocks per CTA)
+  auto item_index = [&](int k) {
+    const int G2 = (int)gridDim.x, c = (int)blockIdx.x;
+    return k * G2 + ((k & 1) ? G2 - 1 - c : c);
+  };
+  auto item_of = [&](int w) {
+    AtcItem it;
+    const int qt = args.n_qt - 1 - w / per_qt;
+    const int rest = w % per_qt;
+    it.b = rest / pairs;
+    const int hp = rest % pairs;
+    const int g = hp / pg_n;
+    it.h0 = g * G + 2 * (hp % pg_n);                 // tile A's head
+    it.h1 = min(it.h0 + 1, g * G + G - 1);           // tile B's head (== h0: not stored)
+    it.bkv = it.b * args.n_kv + g;                   // K/V cache sequence
+    it.q0 = qt * 128;
+    // query row r sits at position qpos0 + r and sees keys max(0, qpos0 + r -
+    // window + 1) .. qpos0 + r; the keys of the cache end at pos0 + T - 1
+    const int p0 = args.pos0[it.b];
+    it.qpos0 = p0 + it.q0;
+    const int last_key = min(it.qpos0 + 127, p0 + args.T - 1);
+    it.jfirst = args.window > 0 ? max(0, it.qpos0 - args.window + 1) / 128 : 0;
+    it.nb = last_key / 128 + 1 - it.jfirst;          // key blocks jfirst .. jfirst + nb - 1
+    return it;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(QFULL), 1);
+    mbar_init(bar(QFREE), 1);
     for (int i = 0; i < 3; ++i) {
       mbar_init(bar(KVFULL + i), 1);
       mbar_init(bar(KVFREE + i), 1);
@@ -232,41 +269,52 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // tiles K_0, V_0, K_1, V_1, ... go round a ring of three slots: slot of
-    // tile i is i % 3, so V_{j+1} reuses the slot of K_j (free once both
-    // heads' S_j are done) and is in flight long before P V_{j+1} needs it
+    // per item: Q (once the previous item's S products have read the Q
+    // tiles), then K_0, V_0, K_1, V_1, ... round a ring of three slots: ring
+    // tile i (counted over all items) uses slot i % 3, so V_{j+1} reuses the
+    // slot of K_j (free once both heads' S_j are done) and is in flight long
+    // before P V_{j+1} needs it
     if (lane == 0) {
       bool ok = true;
       int inflight[3] = {-1, -1, -1};                // parity of loads in flight
-      mbar_arrive_expect_tx(bar(QFULL), 2 * ATC_TILE);
-      for (int t = 0; t < 2; ++t)
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(s0 + ATC_OFF_Q + t * ATC_TILE + h * ATC_HALF, &tmQ, bar(QFULL),
-                      (t == 0 ? h0 : h1) * 128 + 64 * h, q0, b);
-      for (int i = 0; ok && i < 2 * nb; ++i) {
-        const int slot = i % 3, round = i / 3, j = jfirst + (i >> 1);
-        if (!wait(KVFREE + slot, (round & 1) ^ 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(KVFULL + slot), ATC_TILE);
-        const uint32_t dst = s0 + ATC_OFF_KV + slot * ATC_TILE;
-        for (int h = 0; h < 2; ++h) {
-          if ((i & 1) == 0)
-            tma_load_3d(dst + h * ATC_HALF, &tmK, bar(KVFULL + slot), 64 * h, j * 128, bkv);
-          else
-            tma_load_3d(dst + h * ATC_HALF, &tmVt, bar(KVFULL + slot), j * 128 + 64 * h, 0, bkv);
+      int q_inflight = -1;
+      int kv_i = 0;
+      for (int k = 0; ok; ++k) {
+        const int w = item_index(k);
+        if (w >= n_items) break;
+        const AtcItem it = item_of(w);
+        if (k > 0 && !wait(QFREE, (k - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(QFULL), 2 * ATC_TILE);
+        for (int t = 0; t < 2; ++t)
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(s0 + ATC_OFF_Q + t * ATC_TILE + h * ATC_HALF, &tmQ, bar(QFULL),
+                        (t == 0 ? it.h0 : it.h1) * 128 + 64 * h, it.q0, it.b);
+        q_inflight = k & 1;
+        for (int i = 0; i < 2 * it.nb; ++i, ++kv_i) {
+          const int slot = kv_i % 3, round = kv_i / 3, j = it.jfirst + (i >> 1);
+          if (!wait(KVFREE + slot, (round & 1) ^ 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(KVFULL + slot), ATC_TILE);
+          const uint32_t dst = s0 + ATC_OFF_KV + slot * ATC_TILE;
+          for (int h = 0; h < 2; ++h) {
+            if ((i & 1) == 0)
+              tma_load_3d(dst + h * ATC_HALF, &tmK, bar(KVFULL + slot), 64 * h, j * 128, it.bkv);
+            else
+              tma_load_3d(dst + h * ATC_HALF, &tmVt, bar(KVFULL + slot), j * 128 + 64 * h, 0, it.bkv);
+          }
+          inflight[slot] = round & 1;
         }
-        inflight[slot] = round & 1;
       }
       if (!ok) {
         // let every copy still in flight land before the CTA exits
-        mbar_wait(bar(QFULL), 0, limit);
+        if (q_inflight >= 0) mbar_wait(bar(QFULL), (uint32_t)q_inflight, limit);
         for (int sl = 0; sl < 3; ++sl)
           if (inflight[sl] >= 0) mbar_wait(bar(KVFULL + sl), (uint32_t)inflight[sl], limit);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    // order: S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...  so that
-    // the softmax of one head overlaps the tensor-core work of the other
+    // per item: S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...  so
+    // that the softmax of one head overlaps the tensor-core work of the other
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
       auto issue_s = [&](int t, int ks) {
@@ -279,43 +327,62 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
         }
         tc_commit(bar(SFULL + t));
       };
-      auto issue_pv = [&](int t, int j) {
+      auto issue_pv = [&](int t, int vs, bool first) {
         // P_t in TMEM columns t*128 + 8kk .. +7 for keys 16kk .. 16kk+15
-        const uint64_t dv = smem_desc_sw128(s0 + ATC_OFF_KV + ((2 * j + 1) % 3) * ATC_TILE);
+        const uint64_t dv = smem_desc_sw128(s0 + ATC_OFF_KV + vs * ATC_TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * ATC_HALF + (kk & 3) * 32;
           tc_mma_f16_tmem_a(tmem_base + 256 + t * 128, tmem_base + t * 128 + 8 * kk, desc_add(dv, off), idesc,
-                            (j | kk) != 0);
+                            (!first || kk != 0) ? 1u : 0u);
         }
         tc_commit(bar(PVDONE + t));
       };
-      // K_j is ring tile 2j, V_j ring tile 2j + 1 (slot i % 3, phase (i / 3) & 1)
-      bool ok = wait(QFULL, 0) && wait(KVFULL + 0, 0), any = false;
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
-        tc_commit(bar(KVFREE + 0));
-        any = true;
-      }
-      for (int j = 0; ok && j < nb; ++j) {
-        const bool more = j + 1 < nb;
-        const int iv = 2 * j + 1, ik = 2 * j + 2;
-        if (!wait(KVFULL + iv % 3, (iv / 3) & 1)) { ok = false; break; }
+      // counted over all items: S products issued and P tiles consumed per
+      // tile; ring tile kv_base is this item's K_0 (slot i % 3, phase (i / 3) & 1)
+      int sn[2] = {0, 0}, pn[2] = {0, 0};
+      int kv_base = 0;
+      bool ok = true, any = false;
+      for (int k = 0; ok; ++k) {
+        const int w = item_index(k);
+        if (w >= n_items) break;
+        const int nb = item_of(w).nb;
+        if (!wait(QFULL, k & 1) || !wait(KVFULL + kv_base % 3, (kv_base / 3) & 1)) { ok = false; break; }
         for (int t = 0; ok && t < 2; ++t) {
-          if (!wait(PFULL + t, j & 1)) { ok = false; break; }
+          // S_t (and P_t over it) free: the softmax has read the previous S_t
+          if (sn[t] > 0 && !wait(SFREE + t, (sn[t] - 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          issue_pv(t, j);
-          if (t == 1) tc_commit(bar(KVFREE + iv % 3));
-          if (more) {
-            if (t == 0 && !wait(KVFULL + ik % 3, (ik / 3) & 1)) { ok = false; break; }
-            if (!wait(SFREE + t, j & 1)) { ok = false; break; }
+          issue_s(t, kv_base % 3);
+          ++sn[t];
+          any = true;
+        }
+        if (!ok) break;
+        tc_commit(bar(KVFREE + kv_base % 3));
+        if (nb == 1) tc_commit(bar(QFREE));           // the item's last S products were issued
+        for (int j = 0; ok && j < nb; ++j) {
+          const bool more = j + 1 < nb;
+          const int iv = kv_base + 2 * j + 1, ik = kv_base + 2 * j + 2;
+          if (!wait(KVFULL + iv % 3, (iv / 3) & 1)) { ok = false; break; }
+          for (int t = 0; ok && t < 2; ++t) {
+            if (!wait(PFULL + t, pn[t] & 1)) { ok = false; break; }
             tc_fence_after();
-            issue_s(t, ik % 3);
-            if (t == 1) tc_commit(bar(KVFREE + ik % 3));
+            issue_pv(t, iv % 3, j == 0);
+            ++pn[t];
+            if (t == 1) tc_commit(bar(KVFREE + iv % 3));
+            if (more) {
+              if (t == 0 && !wait(KVFULL + ik % 3, (ik / 3) & 1)) { ok = false; break; }
+              if (!wait(SFREE + t, (sn[t] - 1) & 1)) { ok = false; break; }
+              tc_fence_after();
+              issue_s(t, ik % 3);
+              ++sn[t];
+              if (t == 1) {
+                tc_commit(bar(KVFREE + ik % 3));
+                if (j + 2 == nb) tc_commit(bar(QFREE));
+              }
+            }
           }
         }
+        kv_base += 2 * nb;
       }
       if (!ok && any) {
         // every issued MMA must finish before TMEM is released
@@ -333,116 +400,126 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     const uint32_t tO = tmem_base + lane_off + 256 + t * 128;
     const uint32_t pbuf = s0 + ATC_OFF_P + t * ATC_TILE;
     const float sl2 = args.scale_log2;
-    float m = -INFINITY;                            // reference max (raw score units)
-    float l = 0.f;                                  // running sum of exp2((s - m) * sl2)
+    int sc = 0;                                     // S_t tiles consumed over all items
     bool ok = true;
-    for (int j = 0; ok && j < nb; ++j) {
-      if (!wait_warp(SFULL + t, j & 1)) { ok = false; break; }
-      tc_fence_after();
-      float v[128];
-      tmem_ld128(tS, v);                            // the whole row of S_t
-      tc_fence_before();
-      mbar_arrive(bar(SFREE + t));                  // S_t may be overwritten
-      const int jb = jfirst + j;                    // the key block
-      const int lim = qpos0 + r - jb * 128;         // last key of the block this row may see
-      if (lim < 127) {                              // a diagonal block: later keys are in the future
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > lim) v[c] = -INFINITY;
-      }
-      if (args.window > 0) {
-        const int lo = lim - args.window + 1;       // first key of the block inside the window
-        if (lo > 0) {
+    for (int k = 0;; ++k) {
+      const int w = item_index(k);
+      if (w >= n_items) break;
+      const AtcItem it = item_of(w);
+      float m = -INFINITY;                          // reference max (raw score units)
+      float l = 0.f;                                // running sum of exp2((s - m) * sl2)
+      for (int j = 0; ok && j < it.nb; ++j, ++sc) {
+        if (!wait_warp(SFULL + t, sc & 1)) { ok = false; break; }
+        tc_fence_after();
+        float v[128];
+        tmem_ld128(tS, v);                          // the whole row of S_t
+        tc_fence_before();
+        mbar_arrive(bar(SFREE + t));                // S_t may be overwritten
+        const int jb = it.jfirst + j;               // the key block
+        const int lim = it.qpos0 + r - jb * 128;    // last key of the block this row may see
+        if (lim < 127) {                            // a diagonal block: later keys are in the future
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (c < lo) v[c] = -INFINITY;
+            if (c > lim) v[c] = -INFINITY;
         }
-      }
-      // row max as a tree (8 independent chains) to keep the latency short
-      float mk[8];
+        if (args.window > 0) {
+          const int lo = lim - args.window + 1;     // first key of the block inside the window
+          if (lo > 0) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mk[i] = v[i];
-#pragma unroll
-      for (int c = 8; c < 128; c += 8)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mk[i] = fmaxf(mk[i], v[c + i]);
-      const float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
-                             fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
-      bool rescale = false;
-      float factor = 1.f;
-      if (mx > m && (m == -INFINITY || (mx - m) * sl2 > 8.f)) {
-        factor = ex2_approx((m - mx) * sl2);        // 0 when m = -inf
-        l *= factor;
-        m = mx;
-        rescale = j > 0;
-      }
-      // no key seen yet (a window can mask a whole block of a row): P = 0
-      const float mb = m == -INFINITY ? 0.f : m * sl2;
-      // P_t of the previous block must have been consumed (and O_t written)
-      if (j > 0 && !wait_warp(PVDONE + t, (j - 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      // P = exp2(s * sl2 - m * sl2) in bf16, 32 columns at a time into the
-      // first half of the row's S_t columns (S_t has been read); row sum in 8
-      // partial sums
-      float lk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(v[c + 2 * i], sl2, -mb));
-          const float p1 = ex2_approx(fmaf(v[c + 2 * i + 1], sl2, -mb));
-          lk[(2 * i) & 7] += p0;
-          lk[(2 * i + 1) & 7] += p1;
-          pk[i] = pack_bf16_2(p0, p1);
+            for (int c = 0; c < 128; ++c)
+              if (c < lo) v[c] = -INFINITY;
+          }
         }
-        tmem_st16u(tS + (c >> 1), pk);
-      }
-      l += ((lk[0] + lk[1]) + (lk[2] + lk[3])) + ((lk[4] + lk[5]) + (lk[6] + lk[7]));
-      // tcgen05.ld / tcgen05.st are warp-collective: the whole warp takes the
-      // rescale path when any of its rows needs it, each row with its own
-      // factor (1 for rows that keep their reference max)
-      if (__any_sync(0xffffffffu, rescale)) {
-        const float f = rescale ? factor : 1.f;
-#pragma unroll 1
+        // row max as a tree (8 independent chains) to keep the latency short
+        float mk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mk[i] = v[i];
+#pragma unroll
+        for (int c = 8; c < 128; c += 8)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mk[i] = fmaxf(mk[i], v[c + i]);
+        const float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
+                               fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
+        bool rescale = false;
+        float factor = 1.f;
+        if (mx > m && (m == -INFINITY || (mx - m) * sl2 > 8.f)) {
+          factor = ex2_approx((m - mx) * sl2);      // 0 when m = -inf
+          l *= factor;
+          m = mx;
+          rescale = j > 0;
+        }
+        // no key seen yet (a window can mask a whole block of a row): P = 0
+        const float mb = m == -INFINITY ? 0.f : m * sl2;
+        // the previous P_t V product has finished: P_t and O_t may be written
+        if (sc > 0 && !wait_warp(PVDONE + t, (sc - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        // P = exp2(s * sl2 - m * sl2) in bf16, 32 columns at a time into the
+        // first half of the row's S_t columns (S_t has been read); row sum in
+        // 8 partial sums
+        float lk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
         for (int c = 0; c < 128; c += 32) {
-          float o[32];
-          tmem_ld32(tO + c, o);
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= f;
-          tmem_st32(tO + c, o);
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2_approx(fmaf(v[c + 2 * i], sl2, -mb));
+            const float p1 = ex2_approx(fmaf(v[c + 2 * i + 1], sl2, -mb));
+            lk[(2 * i) & 7] += p0;
+            lk[(2 * i + 1) & 7] += p1;
+            pk[i] = pack_bf16_2(p0, p1);
+          }
+          tmem_st16u(tS + (c >> 1), pk);
         }
-      }
-      tmem_wait_st();                               // P (and a rescaled O) written
-      tc_fence_before();
-      mbar_arrive(bar(PFULL + t));
-    }
-    // ---- epilogue: O / l -> bf16 -> P buffer -> TMA store
-    if (ok && !wait_warp(PVDONE + t, (nb - 1) & 1)) ok = false;
-    if (ok) {
-      tc_fence_after();
-      const float inv = 1.f / l;
-      float v[128];
-      tmem_ld128(tO, v);
+        l += ((lk[0] + lk[1]) + (lk[2] + lk[3])) + ((lk[4] + lk[5]) + (lk[6] + lk[7]));
+        // tcgen05.ld / tcgen05.st are warp-collective: the whole warp takes the
+        // rescale path when any of its rows needs it, each row with its own
+        // factor (1 for rows that keep their reference max)
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float f = rescale ? factor : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < 128; c += 32) {
+            float o[32];
+            tmem_ld32(tO + c, o);
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        st_shared_v4u(atc_addr(pbuf, r, 8 * k), pack_bf16_2(v[8 * k] * inv, v[8 * k + 1] * inv),
-                      pack_bf16_2(v[8 * k + 2] * inv, v[8 * k + 3] * inv),
-                      pack_bf16_2(v[8 * k + 4] * inv, v[8 * k + 5] * inv),
-                      pack_bf16_2(v[8 * k + 6] * inv, v[8 * k + 7] * inv));
-      fence_async_smem();
-    }
-    // every thread of the tile reaches this barrier exactly once
-    named_bar_sync(1 + t, 128);
-    if (threadIdx.x == 64 + 128 * t) {
-      if (ok && !*abort_flag && (t == 0 || h1 != h0)) {
-        const int head = t == 0 ? h0 : h1;
-        tma_store_3d(&tmO, pbuf, head * 128, q0, b);
-        tma_store_3d(&tmO, pbuf + ATC_HALF, head * 128 + 64, q0, b);
-        bulk_commit();
+            for (int i = 0; i < 32; ++i) o[i] *= f;
+            tmem_st32(tO + c, o);
+          }
+        }
+        tmem_wait_st();                             // P (and a rescaled O) written
+        tc_fence_before();
+        mbar_arrive(bar(PFULL + t));
       }
-      bulk_wait_all();
+      // ---- the item's output: O / l -> bf16 -> staging tile -> TMA store
+      if (ok && !wait_warp(PVDONE + t, (sc - 1) & 1)) ok = false;
+      // every thread of the tile meets both barriers once per item; the
+      // second one also decides, for all of them alike, whether to go on
+      named_bar_sync(1 + t, 128);                   // the previous item's store has read the tile
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        float v[128];
+        tmem_ld128(tO, v);
+#pragma unroll
+        for (int kq = 0; kq < 16; ++kq)
+          st_shared_v4u(atc_addr(pbuf, r, 8 * kq), pack_bf16_2(v[8 * kq] * inv, v[8 * kq + 1] * inv),
+                        pack_bf16_2(v[8 * kq + 2] * inv, v[8 * kq + 3] * inv),
+                        pack_bf16_2(v[8 * kq + 4] * inv, v[8 * kq + 5] * inv),
+                        pack_bf16_2(v[8 * kq + 6] * inv, v[8 * kq + 7] * inv));
+        fence_async_smem();
+      }
+      const bool stop = named_bar_or(1 + t, 128, !ok || *abort_flag);
+      if (threadIdx.x == 64 + 128 * t) {
+        if (!stop && (t == 0 || it.h1 != it.h0)) {
+          const int head = t == 0 ? it.h0 : it.h1;
+          tma_store_3d(&tmO, pbuf, head * 128, it.q0, it.b);
+          tma_store_3d(&tmO, pbuf + ATC_HALF, head * 128 + 64, it.q0, it.b);
+          bulk_commit();
+        }
+        bulk_wait_read<0>();
+      }
+      if (stop) break;
     }
+    if (threadIdx.x == 64 + 128 * t) bulk_wait_all();
   }
 
   tc_fence_before();

@@ -786,8 +786,11 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
         aa.err = m->err;
         aa.wait_limit_ns = m->wait_limit_ns;
         // CTAs: query tiles x rows x K/V heads x head pairs of a group
-        NC_TRY(launch_k(true, attn_prefill_tc_kernel, dim3(aa.n_qt * B * nkv * ((nh / nkv + 1) / 2)),
-                        dim3(ATC_THREADS), ATC_SMEM, s, tm_qa[0], m->tm_kc[l], m->tm_vt, tm_qa[1], aa));
+        // persistent: one CTA per SM over the items (query tiles x rows x K/V
+        // heads x head pairs of a group)
+        const int items = aa.n_qt * B * nkv * ((nh / nkv + 1) / 2);
+        NC_TRY(launch_k(true, attn_prefill_tc_kernel, dim3(std::min(items, m->num_sms)), dim3(ATC_THREADS), ATC_SMEM,
+                        s, tm_qa[0], m->tm_kc[l], m->tm_vt, tm_qa[1], aa));
         m->launches++;
         NC_TRY(cudaGetLastError());
       } else if (bf) {
