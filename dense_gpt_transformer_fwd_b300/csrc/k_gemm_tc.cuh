@@ -45,8 +45,7 @@ struct GemmArgs {
   __nv_bfloat16* v_cache;         // this layer's V: [B_max][n_kv][S][128]
   const float* rope_cos;          // [S][64]
   const float* rope_sin;          // [S][64]
-  const float* rope_cos_t;        // the same tables dim-major: [64][S]
-  const float* rope_sin_t;
+  const float2* rope_cs_t;        // the same factors dim-major as (cos, sin) pairs: [64][S]
   // K and V caches of all layers as [rows][128] bf16 tensor maps in device
   // memory ([0] K, [1] V; 32 x 64 boxes); this layer's cache row (b, g, pos)
   // of K/V head g is kv_row0 + (b * n_kv + g) * cache_S + pos
@@ -599,8 +598,9 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
           auto load_rope = [&](int c) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              rc[j] = __ldg(args.rope_cos_t + (size_t)(c + j) * args.cache_S + pos_c);
-              rs[j] = __ldg(args.rope_sin_t + (size_t)(c + j) * args.cache_S + pos_c);
+              const float2 t = __ldg(args.rope_cs_t + (size_t)(c + j) * args.cache_S + pos_c);
+              rc[j] = t.x;
+              rs[j] = t.y;
             }
           };
           // the row's norm scale r, then for q and k heads the QK-norm of

@@ -218,8 +218,7 @@ struct nc_model {
   std::vector<const void*> wqkv, wo, wfc, wproj;
   float* rope_cos = nullptr;           // [max_seq][hd/2]
   float* rope_sin = nullptr;
-  float* rope_cos_t = nullptr;         // [hd/2][max_seq] (dim-major copies)
-  float* rope_sin_t = nullptr;
+  float2* rope_cs_t = nullptr;         // [hd/2][max_seq] (cos, sin): the dim-major copy for the prefill QKV epilogue
   CUtensorMap* d_tm_kv = nullptr;      // device: K and V caches of all layers as [rows][128] bf16
   void* k_alloc = nullptr;             // [guard][L][B_max][S][hd][guard]
   void* v_alloc = nullptr;
@@ -316,7 +315,7 @@ void free_model(nc_model* m) {
   for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
   if (m->g_exec) cudaGraphExecDestroy(m->g_exec);
   if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
-  void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->rope_cos_t, m->rope_sin_t, m->d_tm_kv,
+  void* ptrs[] = {m->weights, m->rope_cos, m->rope_sin, m->rope_cs_t, m->d_tm_kv,
                   m->k_alloc, m->v_alloc, m->x,
                   m->h,       m->q,        m->att,      m->u,       m->c32,     m->h_last,
                   m->tok_stage, m->logit_stage, m->err, m->vt, m->d_len, m->d_pos0, m->d_last, m->ss_part, m->ss_rows,
@@ -729,8 +728,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
         a.v_cache = static_cast<bf16*>(m->vc(l));
         a.rope_cos = m->rope_cos;
         a.rope_sin = m->rope_sin;
-        a.rope_cos_t = m->rope_cos_t;
-        a.rope_sin_t = m->rope_sin_t;
+        a.rope_cs_t = m->rope_cs_t;
         a.tm_kv = m->d_tm_kv;
         a.kv_row0 = kGuardElems / 128 + (long long)l * c.max_batch * nkv * c.max_seq;
         a.n_head = nh;
@@ -1436,16 +1434,11 @@ nc_status nc_model_create(const nc_config* cfg, const float* weights, nc_model**
     CREATE_TRY(cudaMalloc(&m->rope_sin, sn.size() * 4));
     CREATE_TRY(cudaMemcpy(m->rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
     CREATE_TRY(cudaMemcpy(m->rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
-    std::vector<float> cst(cs.size()), snt(sn.size());
+    std::vector<float2> cst(cs.size());
     for (int64_t p = 0; p < c.max_seq; ++p)
-      for (int64_t j = 0; j < half; ++j) {
-        cst[j * c.max_seq + p] = cs[p * half + j];
-        snt[j * c.max_seq + p] = sn[p * half + j];
-      }
-    CREATE_TRY(cudaMalloc(&m->rope_cos_t, cst.size() * 4));
-    CREATE_TRY(cudaMalloc(&m->rope_sin_t, snt.size() * 4));
-    CREATE_TRY(cudaMemcpy(m->rope_cos_t, cst.data(), cst.size() * 4, cudaMemcpyHostToDevice));
-    CREATE_TRY(cudaMemcpy(m->rope_sin_t, snt.data(), snt.size() * 4, cudaMemcpyHostToDevice));
+      for (int64_t j = 0; j < half; ++j) cst[j * c.max_seq + p] = make_float2(cs[p * half + j], sn[p * half + j]);
+    CREATE_TRY(cudaMalloc(&m->rope_cs_t, cst.size() * sizeof(float2)));
+    CREATE_TRY(cudaMemcpy(m->rope_cs_t, cst.data(), cst.size() * sizeof(float2), cudaMemcpyHostToDevice));
   }
 
   // KV cache with sentinel guards

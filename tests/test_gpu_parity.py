@@ -144,6 +144,36 @@ def test_decode_attention_cluster_of_eight_groups():
     e.close()
 
 
+def test_decode_attention_ragged_long_rows():
+    """Rows of very different lengths (1 .. 1500 keys at B = 40) in one decode
+    graph: each row's cluster of group CTAs covers its own context, so groups
+    past a short row's keys hold nothing and long rows use every group.
+    Sampled rows (the longest, the one-key row, a row of 129 keys and others)
+    against their one-row oracles."""
+    sh = small_bf16_shape(n_layer=2, vocab=2048)
+    flat = nc_inputs.gen_weights(sh, 146)
+    rng = np.random.default_rng(147)
+    B, T, steps = 40, 1500, 3
+    lens = rng.integers(1, T + 1, size=B)
+    lens[0], lens[1], lens[-1] = T, 1, 129
+    prompt = nc_inputs.gen_tokens(sh.vocab, (B, T), 148)
+    nxt = nc_inputs.gen_tokens(sh.vocab, (steps, B), 149)
+    rows = [0, 1, 7, 20, B - 1]
+    orc = {b: oracle_for(flat, sh) for b in rows}
+    m = ncp.Model(sh, flat, max_batch=B, max_seq=T + steps)
+    m.prefill_rows(to_dev(prompt), lens, last_only=True)
+    for b in rows:
+        orc[b].prefill(prompt[b:b + 1, :lens[b]], logit_positions=[lens[b] - 1])
+    out = torch.empty((B, sh.vocab), device="cuda")
+    for t in range(steps):
+        got = m.decode_step(to_dev(nxt[t]), out=out).cpu().numpy()
+        for b in rows:
+            check_close(got[b], orc[b].decode(nxt[t][b:b + 1])[0], "bf16", "decode attention, ragged long rows")
+    m.sync()
+    assert m.row_lengths() == (lens + steps).tolist()
+    m.close()
+
+
 def test_small_bf16_last_only_and_host_buffers():
     sh = small_bf16_shape()
     flat = nc_inputs.gen_weights(sh, 23)
