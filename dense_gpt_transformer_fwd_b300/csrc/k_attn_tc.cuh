@@ -73,7 +73,7 @@ constexpr uint32_t ATC_HALF = 16384;                 // 128 rows x 128 B
 constexpr uint32_t ATC_TILE = 2 * ATC_HALF;          // 128 rows x 128 bf16
 constexpr uint32_t ATC_OFF_Q = 0;                    // 2 tiles
 constexpr uint32_t ATC_OFF_KV = 2 * ATC_TILE;        // ring of 3 slots: K_0 V_0 K_1 V_1 ...
-constexpr uint32_t ATC_OFF_P = 5 * ATC_TILE;         // 2 tiles
+constexpr uint32_t ATC_OFF_P = 5 * ATC_TILE;         // 2 tiles: the output staging of each head
 constexpr uint32_t ATC_OFF_BAR = 7 * ATC_TILE;
 constexpr size_t ATC_SMEM = 1024 + 7 * (size_t)ATC_TILE + 256;
 
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
     const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
     const uint32_t tS = tmem_base + lane_off + t * 128;
     const uint32_t tO = tmem_base + lane_off + 256 + t * 128;
-    const uint32_t pbuf = s0 + ATC_OFF_P + t * ATC_TILE;
+    const uint32_t pbuf = s0 + ATC_OFF_P + t * ATC_TILE;  // this head's output staging tile
     const float sl2 = args.scale_log2;
     int sc = 0;                                     // S_t tiles consumed over all items
     bool ok = true;

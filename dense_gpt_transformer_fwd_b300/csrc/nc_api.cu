@@ -10,6 +10,9 @@
 //              x += attn(q, cache) Wo^T;  h = rms(x)
 //              x += relu(h Wfc^T)^2 Wproj^T;  h = rms(x)
 //   logits = cap * tanh(h Wu^T / cap)
+// The 16-bit path folds every h = rms(x) into the projection that consumes
+// h: it multiplies its fp32 result by 1/rms(x), and its operand is bf16(x)
+// (written, with per-block sums of squares, by the kernel that produced x).
 #include "nc.h"
 
 #include <cuda.h>
@@ -226,7 +229,7 @@ struct nc_model {
   int32_t length = 0, batch = 0;
   int64_t max_rows = 0;
   float* x = nullptr;                  // fp32 residual [max_rows][d]
-  void* h = nullptr;                   // normed activations [max_rows][d]
+  void* h = nullptr;                   // GEMM input [max_rows][d]: bf16(x), or rms(x) where no fold applies
   void* q = nullptr;                   // [max_rows][n_head*hd]
   void* att = nullptr;                 // [max_rows][n_head*hd]
   void* u = nullptr;                   // [max_rows][d_mlp]
@@ -653,7 +656,7 @@ nc_status forward(nc_model* m, const int32_t* tok, int B, int T, int max_p0, flo
     if (!make_tmap3(&tm_qa[0], m->q, dims, strides, box) || !make_tmap3(&tm_qa[1], m->att, dims, strides, box))
       return NC_ERR_CUDA;
   }
-  {  // x = rms(E[tok]); h = rms(x)
+  {  // x = rms(E[tok]); h = bf16(x) and its sums of squares (folded), or h = rms(x)
     KScope ks(m, NC_K_EMBED, s);
     if (bf)
       embed_rmsnorm_kernel<bf16, bf16><<<blocks_for_warps(M), 256, 0, s>>>(
