@@ -138,6 +138,34 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[1
       : "memory");
 }
 
+// Packed pairs of fp32 (sm_100 family): two lanes of fma / add per
+// instruction, each rounded as the scalar operation; and a three-input max.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // byte address of bf16 element (row r, column c) of a 128 x 128 tile stored
 // as two K-major 128-byte-swizzled halves (columns 0..63, 64..127)
 __device__ __forceinline__ uint32_t atc_addr(uint32_t tile, int r, int c) {
@@ -430,14 +458,14 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
               if (c < lo) v[c] = -INFINITY;
           }
         }
-        // row max as a tree (8 independent chains) to keep the latency short
+        // row max as a tree (8 independent chains of three-input maxima)
         float mk[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mk[i] = v[i];
+        for (int i = 0; i < 8; ++i) mk[i] = fmaxf(v[i], v[8 + i]);
 #pragma unroll
-        for (int c = 8; c < 128; c += 8)
+        for (int c = 16; c < 128; c += 16)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) mk[i] = fmaxf(mk[i], v[c + i]);
+          for (int i = 0; i < 8; ++i) mk[i] = fmax3(mk[i], v[c + i], v[c + 8 + i]);
         const float mx = fmaxf(fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3])),
                                fmaxf(fmaxf(mk[4], mk[5]), fmaxf(mk[6], mk[7])));
         bool rescale = false;
@@ -455,20 +483,27 @@ __global__ void __launch_bounds__(ATC_THREADS, 1)
         tc_fence_after();
         // P = exp2(s * sl2 - m * sl2) in bf16, 32 columns at a time into the
         // first half of the row's S_t columns (S_t has been read); row sum in
-        // 8 partial sums
-        float lk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // 8 partial sums, kept as 4 pairs (column c goes to partial c % 8)
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nmbx2 = f2_pack(-mb, -mb);
+        uint64_t lk2[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 128; c += 32) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2_approx(fmaf(v[c + 2 * i], sl2, -mb));
-            const float p1 = ex2_approx(fmaf(v[c + 2 * i + 1], sl2, -mb));
-            lk[(2 * i) & 7] += p0;
-            lk[(2 * i + 1) & 7] += p1;
+            const float2 a = f2_unpack(f2_fma(f2_pack(v[c + 2 * i], v[c + 2 * i + 1]), sl2x2, nmbx2));
+            const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+            lk2[i & 3] = f2_add(lk2[i & 3], f2_pack(p0, p1));
             pk[i] = pack_bf16_2(p0, p1);
           }
           tmem_st16u(tS + (c >> 1), pk);
+        }
+        float lk[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 t = f2_unpack(lk2[i]);
+          lk[2 * i] = t.x;
+          lk[2 * i + 1] = t.y;
         }
         l += ((lk[0] + lk[1]) + (lk[2] + lk[3])) + ((lk[4] + lk[5]) + (lk[6] + lk[7]));
         // tcgen05.ld / tcgen05.st are warp-collective: the whole warp takes the
