@@ -408,6 +408,23 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
     const int ch0 = (e >> 2) * HALF;                // first owned column in the tile
     const uint32_t buf0 = smem_u32(sE + e * C::EP_BUFS * C::EP_BUF);
     const float inv_cap = 1.0f / args.softcap;
+    // folded RMSNorm: 1 / rms(x) of row r, its block sums added in block order
+    auto row_rscale = [&](int r) {
+      const float* ssr = args.row_ss + (r < args.M ? r : args.M - 1);
+      float t = 0.f;
+      for (int bi = 0; bi < args.ss_blocks; ++bi) t += __ldcg(ssr + (size_t)bi * args.ss_ld);
+      return rsqrtf(t * args.inv_d + args.eps);
+    };
+    // The ReLU^2 and logits epilogues request the next unit's block sums at
+    // the start of a unit and add them at its end, so that their latency
+    // overlaps this unit's work (these epilogues are short next to their
+    // loads when K is small).
+    constexpr bool SS_AHEAD = EPI == EPI_RELU2 || EPI == EPI_LOGITS;
+    constexpr int SS_MAXB = 16;
+    const bool ss_ahead = SS_AHEAD && args.row_ss != nullptr && args.ss_blocks <= SS_MAXB;
+    float ss_next[SS_AHEAD ? SS_MAXB : 1];
+    float rscale_next = 1.f;
+    if (ss_ahead && unit0 < num_units) rscale_next = row_rscale(unit_m0(unit0) + 32 * q + lane);
     int local = 0;
     for (int u = unit0; u < num_units; u += ustride, ++local) {
       const int acc = local & 1;
@@ -425,11 +442,22 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + acc * BN + ch0;
       // folded RMSNorm: this row's 1 / rms(x)
       float rscale = 1.f;
-      if (args.row_ss != nullptr) {
-        const float* ssr = args.row_ss + (my_row < args.M ? my_row : args.M - 1);
-        float t = 0.f;
-        for (int bi = 0; bi < args.ss_blocks; ++bi) t += __ldcg(ssr + (size_t)bi * args.ss_ld);
-        rscale = rsqrtf(t * args.inv_d + args.eps);
+      if constexpr (SS_AHEAD) {
+        if (ss_ahead) {
+          rscale = rscale_next;
+          const int un = u + ustride;
+          if (un < num_units) {
+            const int rn = unit_m0(un) + 32 * q + lane;
+            const float* ssr = args.row_ss + (rn < args.M ? rn : args.M - 1);
+#pragma unroll
+            for (int bi = 0; bi < SS_MAXB; ++bi)
+              ss_next[bi] = bi < args.ss_blocks ? __ldcg(ssr + (size_t)bi * args.ss_ld) : 0.f;
+          }
+        } else if (args.row_ss != nullptr) {
+          rscale = row_rscale(my_row);
+        }
+      } else if (args.row_ss != nullptr) {
+        rscale = row_rscale(my_row);
       }
 
       if constexpr (EPI == EPI_RESID) {
@@ -709,6 +737,16 @@ __global__ void __launch_bounds__(TcCfg<BN, EPI, CL>::THREADS, 1)
         if (lane == 0) mbar_arrive_cluster(cluster_addr(bar(TEMPTY + acc), 0));
       } else {
         mbar_arrive(bar(TEMPTY + acc));
+      }
+      if constexpr (SS_AHEAD) {
+        if (ss_ahead && u + ustride < num_units) {
+          // the same block order as row_rscale: the same value
+          float t = 0.f;
+#pragma unroll
+          for (int bi = 0; bi < SS_MAXB; ++bi)
+            if (bi < args.ss_blocks) t += ss_next[bi];
+          rscale_next = rsqrtf(t * args.inv_d + args.eps);
+        }
       }
     }
     if (lane == 0) bulk_wait_all();                 // stores done before the CTA exits
