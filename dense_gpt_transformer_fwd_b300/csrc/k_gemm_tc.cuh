@@ -17,9 +17,12 @@
 //                 read the 32 TMEM lanes of its quarter, warp % 4), each
 //                 owning half of the tile's columns: tcgen05.ld, fused math,
 //                 then 32-row x 128-byte chunks staged in a swizzled shared
-//                 buffer and written by TMA bulk tensor stores.  The residual
-//                 epilogue uses the TMA reduce-add store, so x += acc happens
-//                 in L2 without reading x into the SM.
+//                 buffer and written by TMA bulk tensor stores.  With the
+//                 RMSNorm folded into the projections, the residual epilogue
+//                 reads x (coalesced, through the staging buffer), stores
+//                 x + acc, bf16(x + acc) and the rows' sums of squares, and
+//                 the next projection scales its rows by 1/rms(x); without
+//                 it, x += acc is a TMA reduce-add in L2.
 // Tiles are visited m-fastest, so that CTAs resident at the same time share
 // the W tile, or n-fastest when the A operand is the larger one (it is then
 // read from DRAM once while the W tiles stay in L2).

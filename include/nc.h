@@ -355,7 +355,9 @@ enum {
   NC_K_QKV = 1,     /* QKV projection + RoPE + QK-norm + cache write */
   NC_K_ATTN = 2,    /* causal MQA attention (all its kernels)       */
   NC_K_OPROJ = 3,   /* output projection + residual                 */
-  NC_K_NORM = 4,    /* RMSNorm before the MLP / the next block      */
+  NC_K_NORM = 4,    /* RMSNorm kernels where no projection folds the norm
+                       (fp32 model, the extras, the last-position gather,
+                       the final norm of a generic decode step)        */
   NC_K_FC = 5,      /* MLP up-projection + ReLU^2                    */
   NC_K_PROJ = 6,    /* MLP down-projection + residual               */
   NC_K_LMHEAD = 7,  /* unembedding + softcap                        */
