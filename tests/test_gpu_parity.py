@@ -83,6 +83,25 @@ def test_small_bf16_prefill_decode(B, T, steps):
     m.close()
 
 
+@pytest.mark.parametrize("n_kv", [1, 3])
+def test_persistent_prefill_attention_several_items_per_cta(n_kv):
+    """More attention work items than SMs: 40 rows x 2 query tiles x 3 head
+    pairs = 240 items on 148 persistent CTAs, so most CTAs run a second item
+    of a different length (one or two key blocks), reloading the queries while
+    the K/V ring continues; T = 200 leaves a ragged last query tile.  Every
+    position of every row against the oracle, with one and with three K/V
+    heads."""
+    sh = small_bf16_shape(n_layer=2, vocab=512).with_(n_kv_head=n_kv)
+    flat = nc_inputs.gen_weights(sh, 151 + n_kv)
+    B, T = 40, 200
+    prompt = nc_inputs.gen_tokens(sh.vocab, (B, T), 153)
+    m = ncp.Model(sh, flat, max_batch=B, max_seq=T)
+    got = m.prefill(to_dev(prompt)).cpu().numpy()
+    check_close(got, oracle_for(flat, sh).prefill(prompt), "bf16", f"persistent attention, 240 items (n_kv={n_kv})")
+    m.sync()
+    m.close()
+
+
 @pytest.mark.parametrize("B,T,steps", [(5, 130, 6), (40, 64, 4), (100, 33, 3)])
 def test_decode_graph_replay_matches_oracle_and_eager(B, T, steps):
     """Decode steps into one fixed logits buffer are captured as a CUDA graph
