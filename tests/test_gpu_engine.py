@@ -177,6 +177,22 @@ def test_sampling_matches_oracle_bit_exactly(temperature, top_k):
     m.close()
 
 
+@pytest.mark.parametrize("temperature,top_k", [(0.0, 0), (0.8, 50), (1.0, 1024)])
+def test_sampling_full_vocabulary_bit_exactly(temperature, top_k):
+    """The sampling kernel over the workloads' 65,536-token vocabulary (its
+    radix select ranks 16x more candidates than in the test above), on the
+    same kind of seeded logits with planted ties."""
+    sh = small_bf16_shape(n_layer=1, vocab=65536)
+    B, V = 8, sh.vocab
+    m = ncp.Model(sh, nc_inputs.gen_weights(sh, 131), max_batch=B, max_seq=8)
+    logits = _planted_logits(B, V, 132)
+    u = np.random.default_rng(133).random(B)
+    got = m.sample(to_dev(logits), temperature, top_k, to_dev(u)).cpu().numpy()
+    m.sync()
+    np.testing.assert_array_equal(got, sample_tokens(logits.astype(np.float64), temperature, top_k, u))
+    m.close()
+
+
 def test_sampling_whole_vocabulary_and_limits():
     """top_k = 0 keeps every candidate: on the device only while the
     vocabulary has at most 1024 entries (the tiny model's 512); otherwise the

@@ -91,3 +91,27 @@ def test_smear_with_rows_of_different_lengths():
             check_close(got[b], orc[b].decode(nxt[t][b:b + 1])[0], "bf16", "extras ragged rows: decode")
     m.sync()
     m.close()
+
+
+def test_extras_with_fp8_weights_groups_and_windows():
+    """Every extra together with FP8 projection weights, three K/V heads and
+    a window on alternate layers: prefill, decode steps (the generic decode
+    path, since the extras keep the decode graph off) and a chunk, against
+    the oracle on the same rounded weights."""
+    sh = small_bf16_shape(n_layer=4, vocab=2048).with_(dtype="fp8", n_kv_head=3, window=100, window_pattern="SL",
+                                                        **ALL)
+    flat = nc_inputs.gen_weights(sh, 218)
+    B, T = 2, 180
+    toks = nc_inputs.gen_tokens(sh.vocab, (B, T + 3 + 30), 219)
+    o = oracle_for(flat, sh)
+    m = ncp.Model(sh, flat, max_batch=B, max_seq=T + 3 + 30)
+    check_close(m.prefill(to_dev(toks[:, :T])).cpu().numpy(), o.prefill(toks[:, :T]), "bf16", "extras fp8 gqa window: prefill")
+    p = T
+    for _ in range(3):
+        check_close(m.decode_step(to_dev(toks[:, p])).cpu().numpy(), o.decode(toks[:, p]), "bf16",
+                    "extras fp8 gqa window: decode")
+        p += 1
+    check_close(m.prefill(to_dev(toks[:, p:p + 30])).cpu().numpy(), o.extend(toks[:, p:p + 30]), "bf16",
+                "extras fp8 gqa window: chunk")
+    m.sync()
+    m.close()
