@@ -98,7 +98,9 @@ def decode_bytes(s, B, ctx):
 
 
 def weight_bytes(s):
-    """Bytes of the weights a decode step streams (bf16; FP8 projections)."""
+    """Bytes of the model's weights in device memory: bf16, or FP8 projection
+    matrices with a bf16 embedding table (a decode step gathers only B rows
+    of the embedding; decode_bytes_by_class counts what it streams)."""
     if s.dtype == "fp8":
         return 2 * s.vocab * s.d_model + (nc_inputs.param_count(s) - s.vocab * s.d_model)
     return 2 * nc_inputs.param_count(s)

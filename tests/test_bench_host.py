@@ -64,3 +64,36 @@ def test_decode_bytes_match_the_stated_totals(name, shape, B, ctx0, steps, mbyte
                     + L * B * c * kv_row + L * B * kv_row + B * d * 2 + B * V * 4 for c in ctxs])
     assert got == pytest.approx(want, rel=1e-12)
     assert got / 1e6 == pytest.approx(mbytes, abs=0.6)
+
+
+def test_decode_bytes_with_fp8_weights():
+    """FP8 workload: every projection weight (blocks and unembedding) is one
+    byte; the K/V cache, embedding rows and logits are unchanged."""
+    s8 = nc_inputs.D24.with_(dtype="fp8")
+    B, ctx = 128, 2100
+    L, d, V = s8.n_layer, s8.d_model, s8.vocab
+    kv_row = 2 * 128 * 2
+    want = (1.0 * (BLOCK_PARAMS["d24"] + UNEMBED_PARAMS["d24"]) + L * B * ctx * kv_row + L * B * kv_row
+            + B * d * 2 + B * V * 4)
+    assert bench.decode_bytes(s8, B, ctx) == pytest.approx(want, rel=1e-12)
+    assert bench.decode_bytes(nc_inputs.D24, B, ctx) - bench.decode_bytes(s8, B, ctx) == pytest.approx(
+        BLOCK_PARAMS["d24"] + UNEMBED_PARAMS["d24"], rel=1e-12)
+    # resident weights: bf16 embedding table plus one byte per projection weight
+    assert bench.weight_bytes(s8) == 2 * V * d + BLOCK_PARAMS["d24"] + UNEMBED_PARAMS["d24"]
+
+
+def test_work_counts_with_grouped_query_heads():
+    """n_kv K/V heads: the QKV projection grows by 2 (n_kv - 1) heads, the
+    K/V cache traffic by a factor n_kv; the attention FLOPs (one score and
+    one output product per query head) do not change."""
+    s1 = nc_inputs.D12
+    s3 = nc_inputs.D12.with_(n_kv_head=3)
+    B, T, ctx = 4, 512, 700
+    d, L = s1.d_model, s1.n_layer
+    f1, f3 = bench.prefill_flops(s1, B, T), bench.prefill_flops(s3, B, T)
+    assert f3["qkv"] - f1["qkv"] == pytest.approx(2.0 * B * T * d * (2 * 2 * 128) * L)
+    assert f3["attn"] == f1["attn"]
+    b1, b3 = bench.decode_bytes_by_class(s1, B, ctx), bench.decode_bytes_by_class(s3, B, ctx)
+    assert b3["attn"] == pytest.approx(3 * b1["attn"])
+    assert b3["qkv"] - b1["qkv"] == pytest.approx(2.0 * L * (2 * 2 * 128) * d + L * B * 2 * 2 * 128 * 2.0)
+
