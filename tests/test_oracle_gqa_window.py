@@ -190,6 +190,20 @@ def test_windowed_model_special_cases_and_decode():
     assert check_windowed_model()
 
 
+def test_chunked_prefill_with_windows_and_groups_equals_whole_prefill():
+    """A prompt prefilled in chunks (the second and third starting inside a
+    window) gives the whole prefill's logits, with short "S" layers and
+    grouped K/V heads: the chunk's queries see the window over keys cached by
+    earlier chunks."""
+    s = shape(n_kv_head=2, window=4, window_pattern="SL")
+    flat = nc_inputs.gen_weights(s, 156, std=0.3)
+    tok = nc_inputs.gen_tokens(s.vocab, (2, 13), 157)
+    whole = go.OracleModel(flat, s).prefill(tok)
+    o = go.OracleModel(flat, s)
+    parts = [o.prefill(tok[:, :5]), o.extend(tok[:, 5:7]), o.extend(tok[:, 7:])]
+    np.testing.assert_allclose(np.concatenate(parts, axis=1), whole, rtol=0, atol=1e-12)
+
+
 def test_gqa_equals_mha_with_each_group_replicated():
     s = shape(n_kv_head=2)
     flat = nc_inputs.gen_weights(s, 154, std=0.3).astype(np.float64)
